@@ -1,0 +1,315 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Nothing here reruns the oracle's own formula: each check uses an independent
+route (the printed grid, a library conversion, hand-worked values, invariants,
+brute force, an unquantized fp64 MoE).
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+from nvfp4_token_routed_gb300 import workloads as W
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+GRID = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def bf16_bits_of(values):
+    t = torch.tensor(values, dtype=torch.float32).to(torch.bfloat16)
+    assert torch.equal(t.float(), torch.tensor(values, dtype=torch.float32)), "not bf16-exact"
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+# --------------------------------------------------------------------------- formats
+
+def test_e2m1_decode_is_the_printed_grid():
+    for code in range(16):
+        mag = GRID[code & 7]
+        assert O.e2m1_decode(code) == (-mag if code & 8 else mag)
+
+
+def _nearest_grid_ties_even(v):
+    """Brute force: nearest of the 8 grid magnitudes, ties to the even code index."""
+    a = abs(float(v))
+    best, bestd = None, None
+    for i, g in enumerate(GRID):
+        dd = abs(a - g)
+        if bestd is None or dd < bestd or (dd == bestd and i % 2 == 0):
+            best, bestd = i, dd
+    if a > 6.0:
+        best = 7
+    return best | (8 if np.signbit(v) else 0)
+
+
+def test_e2m1_encode_matches_bruteforce_nearest():
+    rng = np.random.default_rng(0)
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
+    near = np.concatenate([mids, np.nextafter(mids, np.float32(0)), np.nextafter(mids, np.float32(9))])
+    grid = np.array(GRID, np.float32)
+    vals = np.concatenate([near, -near, grid, -grid, np.linspace(-8, 8, 4001, dtype=np.float32),
+                           rng.uniform(-8, 8, 20000).astype(np.float32),
+                           np.array([7.0, 100.0, -1e30, 6.0000005], np.float32)])
+    got = O.e2m1_encode(vals)
+    want = np.array([_nearest_grid_ties_even(v) for v in vals], np.uint8)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, [(vals[i], got[i], want[i]) for i in bad[:10]]
+
+
+def test_e2m1_tie_table_from_the_reading():
+    # ties to even: 0.25->0, 0.75->1.0, 1.25->1.0, 1.75->2, 2.5->2, 3.5->4, 5->4, >5 -> 6
+    ins = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 5.01, 9.0], np.float32)
+    want = [0, 2, 2, 4, 4, 6, 6, 7, 7]
+    assert list(O.e2m1_encode(ins)) == want
+
+
+def test_e4m3_matches_torch_float8_e4m3fn():
+    rng = np.random.default_rng(1)
+    codes = np.arange(0, 0x7F, dtype=np.uint8)            # every finite non-negative E4M3
+    vals = O.e4m3_decode(codes).astype(np.float32)
+    mids = ((vals[1:].astype(np.float64) + vals[:-1]) / 2).astype(np.float32)
+    probe = np.concatenate([vals, mids, np.nextafter(mids, np.float32(0)),
+                            np.nextafter(mids, np.float32(1000)),
+                            rng.uniform(0, 448, 50000).astype(np.float32),
+                            np.exp(rng.uniform(np.log(2.0 ** -12), np.log(448), 50000)).astype(np.float32)])
+    probe = probe[probe <= 448.0]
+    got = O.e4m3_encode(probe)
+    want = torch.from_numpy(probe).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, [(probe[i], got[i], want[i]) for i in bad[:10]]
+    # decode agrees with torch's e4m3fn -> float conversion for every finite code
+    allc = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    tdec = torch.from_numpy(allc).view(torch.float8_e4m3fn).float().numpy()
+    assert np.array_equal(O.e4m3_decode(allc), tdec.astype(np.float64))
+
+
+def test_e4m3_max_is_448_and_saturates():
+    assert O.e4m3_decode(np.array([0x7E], np.uint8))[0] == 448.0
+    assert list(O.e4m3_encode(np.array([448.0, 449.0, 470.0, 1e6, 3e38], np.float32))) == [0x7E] * 5
+    assert O.e4m3_decode(np.array([0x01], np.uint8))[0] == 2.0 ** -9     # smallest subnormal
+    assert O.e4m3_decode(np.array([0x08], np.uint8))[0] == 2.0 ** -6     # smallest normal
+
+
+def test_recipe_constant_is_one_over_448x6():
+    c = O.recipe_c()
+    assert c.dtype == np.float32
+    # the binary32 nearest to 1/2688: within half an ulp of the exact value
+    ulp = np.spacing(np.float32(1.0 / 2688.0))
+    assert abs(float(c) - 1.0 / 2688.0) <= ulp / 2
+
+
+def test_f64_to_bf16_matches_torch_for_float32_inputs():
+    rng = np.random.default_rng(2)
+    v = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.uniform(-30, 30, 20000),
+                        [0.0, -0.0, 1.0, 3.140625, 1.00390625, 1.01171875]]).astype(np.float32)
+    got = O.f64_to_bf16(v.astype(np.float64))
+    want = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, want)
+
+
+# --------------------------------------------------------------------------- quantizers
+
+def _load_cases():
+    with open(os.path.join(GOLD, "quant_roundtrips.json")) as f:
+        return json.load(f)["cases"]
+
+
+@pytest.mark.parametrize("case", _load_cases(), ids=lambda c: c["name"])
+def test_hand_worked_round_trips(case):
+    bits = bf16_bits_of(case["row"]).reshape(1, -1)
+    codes, sf, s = O.quantize_tokens(bits)
+    assert list(sf[0]) == case["sf"]
+    assert list(codes[0]) == case["codes"]
+    amax = case["amax"]
+    if amax == 0:
+        assert s[0] == 0.0
+    else:
+        # the per-token decode scale is amax/(448*6), to within one binary32 rounding step
+        assert abs(float(s[0]) - amax / 2688.0) <= 2 * np.spacing(np.float32(amax / 2688.0))
+
+
+def test_power_of_two_scaling_invariance():
+    """Scaling a token by 2^m leaves codes and block scales unchanged and scales s by 2^m."""
+    x = W.make_x(W.TINY_RELU2)
+    bits = W.bf16_bits(x)
+    c0, f0, s0 = O.quantize_tokens(bits)
+    for m in (-7, -1, 3, 9):
+        xs = (x.float() * 2.0 ** m).to(torch.bfloat16)
+        c1, f1, s1 = O.quantize_tokens(W.bf16_bits(xs))
+        assert np.array_equal(c0, c1) and np.array_equal(f0, f1)
+        assert np.array_equal(s1, (s0 * np.float32(2.0 ** m)).astype(np.float32))
+
+
+def test_dequant_error_within_half_step_of_block_scale():
+    """|x - deq| <= half an E2M1 step (1 for |q| in [4,6]) times the block scale, times s."""
+    x = W.make_x(W.TINY_RELU2)
+    codes, sf, s = O.quantize_tokens(W.bf16_bits(x))
+    deq = O.dequant(codes, sf) * s[:, None].astype(np.float64)
+    xf = x.float().numpy().astype(np.float64)
+    bs = np.repeat(O.e4m3_decode(sf).reshape(sf.shape), 16, axis=1) * s[:, None]
+    # largest E2M1 gap is 2 (between 4 and 6) -> half-gap 1; plus the scale's own rounding
+    assert np.all(np.abs(xf - deq) <= 1.0 * bs * 1.0001 + 1e-30)
+
+
+def test_weight_prep_alpha_and_codes():
+    """An expert whose amax is 6 gets w_scale 448 and alpha 1/448; its codes are the grid."""
+    row = np.array(GRID + [-g for g in GRID], np.float32)      # 16 values, amax 6
+    w = torch.from_numpy(np.tile(row, (1, 4, 2))).to(torch.bfloat16)  # [1, 4, 32]
+    codes, sf, alpha = O.prepare_fc(W.bf16_bits(w))
+    assert alpha[0] == np.float32(1.0) / np.float32(448.0)
+    assert np.all(sf == 0x7E)
+    want = [c | (8 if i >= 8 else 0) for i, c in enumerate(list(range(8)) * 2)]
+    want_bytes = [want[2 * j] | (want[2 * j + 1] << 4) for j in range(8)]
+    assert list(codes[0, 0, :8]) == want_bytes
+
+
+def test_weight_prep_zero_expert():
+    w = torch.zeros(2, 4, 32, dtype=torch.bfloat16)
+    w[1, 2, 5] = 1.0
+    codes, sf, alpha = O.prepare_fc(W.bf16_bits(w))
+    assert alpha[0] == 0 and not codes[0].any() and not sf[0].any()
+    assert alpha[1] == np.float32(1.0) / (np.float32(2688.0) / np.float32(1.0))
+
+
+def test_swizzled_plane_size_and_bijection():
+    """P = round_up(N,128)*round_up(D/16,4) (Tensor and numerical contract) and every
+    (row, scale column) lands on its own byte."""
+    for N, c16 in [(128, 16), (256, 448 // 1), (300, 20), (4096, 128)]:
+        lin = np.arange(N * c16, dtype=np.int64)
+        offs = np.array([O.sf_swizzle_offset(r, j, c16) for r in range(N) for j in range(c16)])
+        P = (N + 127) // 128 * 128 * ((c16 + 3) // 4 * 4)
+        assert offs.min() >= 0 and offs.max() < P
+        assert np.unique(offs).size == lin.size
+        # each 512-byte atom holds 128 rows x 4 consecutive scale columns of one row block
+        r = np.arange(N).repeat(c16)
+        j = np.tile(np.arange(c16), N)
+        assert np.array_equal(offs // 512, (r // 128) * ((c16 + 3) // 4) + j // 4)
+
+
+# --------------------------------------------------------------------------- routing
+
+def test_route_matches_numpy_stable_argsort():
+    rng = np.random.default_rng(3)
+    for T, K, E in [(16, 2, 8), (37, 6, 20), (128, 8, 64)]:
+        ids = rng.integers(-1, E, size=(T, K)).astype(np.int32)
+        ids[0, 0] = E + 5          # invalid id -> empty slot
+        counts, perm, inv = O.route(ids, E)
+        flat = ids.ravel()
+        valid = (flat >= 0) & (flat < E)
+        order = np.argsort(np.where(valid, flat, E + 10), kind="stable")[: valid.sum()]
+        assert np.array_equal(perm, order.astype(np.int32))
+        assert np.array_equal(counts, np.bincount(flat[valid], minlength=E).astype(np.int32))
+        assert np.all(inv[~valid] == -1)
+        assert np.array_equal(inv[perm], np.arange(perm.size))
+
+
+# --------------------------------------------------------------------------- forward
+
+def _tiny(act="relu2", T=16, H=256, I=512, E=8, K=2, seed=0):
+    wl = W.Workload(f"t_{act}", T, H, I, E, K, act)
+    x = W.make_x(wl, seed=seed + 11)
+    w1, w2 = W.make_weights(wl, seed=seed + 20)
+    ids, wts = W.make_routing(wl, seed=seed + 30)
+    return wl, x, w1, w2, ids.numpy(), wts.numpy()
+
+
+def test_forward_equals_dense_bruteforce_exactly():
+    for act in ("relu2", "swiglu"):
+        wl, x, w1, w2, ids, wts = _tiny(act, I=256 if act == "swiglu" else 512)
+        Wt = O.Weights(W.bf16_bits(w1), W.bf16_bits(w2))
+        xc, xsf, xs = O.quantize_tokens(W.bf16_bits(x))
+        routed = O.forward_w4a4(Wt, xc, xsf, xs, ids, wts, wl.E, wl.H, wl.I, act)
+        dense = O.dense_w4a4(Wt, xc, xsf, xs, ids, wts, wl.E, wl.H, wl.I, act)
+        assert np.array_equal(routed["out"], dense)
+
+
+def test_finalize_top1_unit_weight_is_the_route_row():
+    rng = np.random.default_rng(4)
+    T, K, H = 5, 3, 32
+    rows = torch.randn(T, H).to(torch.bfloat16)
+    inv = -np.ones(T * K, np.int32)
+    w = np.zeros(T * K, np.float32)
+    for t in range(T):
+        k = rng.integers(0, K)
+        inv[t * K + k] = t
+        w[t * K + k] = 1.0
+    out = O.finalize(W.bf16_bits(rows), inv, w, T, K)
+    assert np.array_equal(out, W.bf16_bits(rows))
+
+
+def _unquantized_moe(x, w1, w2, ids, wts, act, I):
+    xf = x.double().numpy()
+    out = np.zeros_like(xf)
+    for t in range(xf.shape[0]):
+        for k in range(ids.shape[1]):
+            e = ids[t, k]
+            y = w1[e].double().numpy() @ xf[t]
+            if act == "relu2":
+                a = np.maximum(y, 0) ** 2
+            else:
+                g, u = y[:I], y[I:]
+                a = g / (1 + np.exp(-g)) * u
+            out[t] += wts[t, k] * (w2[e].double().numpy() @ a)
+    return out
+
+
+@pytest.mark.parametrize("act", ["relu2", "swiglu"])
+def test_sanity_against_unquantized_fp64_moe(act):
+    """The pages' accuracy bound for the NVFP4 MoE against an unquantized one:
+    per-token cosine mean > 0.97 and min > 0.95 (What is tested)."""
+    wl, x, w1, w2, ids, wts = _tiny(act, I=256 if act == "swiglu" else 512)
+    Wt = O.Weights(W.bf16_bits(w1), W.bf16_bits(w2))
+    xc, xsf, xs = O.quantize_tokens(W.bf16_bits(x))
+    got = O.bf16_to_f32(O.forward_w4a4(Wt, xc, xsf, xs, ids, wts, wl.E, wl.H, wl.I, act)["out"])
+    ref = _unquantized_moe(x, w1, w2, ids, wts, act, wl.I)
+    cos = (got * ref).sum(1) / np.linalg.norm(got, axis=1) / np.linalg.norm(ref, axis=1)
+    assert cos.mean() > 0.97 and cos.min() > 0.95, cos
+    # the W4A16 variant keeps activations in bf16: tighter
+    got16 = O.bf16_to_f32(O.forward_w4a16(Wt, W.bf16_bits(x), ids, wts, wl.E, wl.H, wl.I, act)["out"])
+    cos16 = (got16 * ref).sum(1) / np.linalg.norm(got16, axis=1) / np.linalg.norm(ref, axis=1)
+    assert cos16.min() > cos.min() - 1e-3 and cos16.mean() > 0.98
+
+
+def test_swiglu_gate_up_split():
+    """up rows zero -> output 0; gate rows zero -> output 0; swapping the halves
+    changes the output (canonical FC1 = [gate; up], Tensor and numerical contract)."""
+    wl, x, w1, w2, ids, wts = _tiny("swiglu", T=4, I=128, E=4, K=1)
+    xc, xsf, xs = O.quantize_tokens(W.bf16_bits(x))
+    I = wl.I
+
+    def run(w1m):
+        Wt = O.Weights(W.bf16_bits(w1m), W.bf16_bits(w2))
+        return O.forward_w4a4(Wt, xc, xsf, xs, ids, wts, wl.E, wl.H, I, "swiglu")["out"]
+
+    up0 = w1.clone()
+    up0[:, I:] = 0
+    assert not O.bf16_to_f32(run(up0)).any()
+    g0 = w1.clone()
+    g0[:, :I] = 0
+    assert not O.bf16_to_f32(run(g0)).any()
+    sw = torch.cat([w1[:, I:], w1[:, :I]], dim=1)
+    assert not np.array_equal(run(sw), run(w1))
+    # and silu(g)*u, not g*silu(u): with the gate forced negative-large, output ~ 0
+    neg = w1.clone()
+    neg[:, :I] = 0
+    neg[:, :I, 0] = -100.0
+    xpos = torch.zeros_like(x)
+    xpos[:, 0] = 1.0
+    xc2, xsf2, xs2 = O.quantize_tokens(W.bf16_bits(xpos))
+    Wt = O.Weights(W.bf16_bits(neg), W.bf16_bits(w2))
+    out = O.forward_w4a4(Wt, xc2, xsf2, xs2, ids, wts, wl.E, wl.H, I, "swiglu")["out"]
+    assert np.abs(O.bf16_to_f32(out)).max() < 1e-20
+
+
+def test_relu2_output_scales_by_four_to_the_m():
+    """Squared ReLU: scaling tokens by 2^m scales each route row (and output) by 4^m exactly."""
+    wl, x, w1, w2, ids, wts = _tiny("relu2", T=6)
+    Wt = O.Weights(W.bf16_bits(w1), W.bf16_bits(w2))
+    r0 = O.forward_w4a4(Wt, *O.quantize_tokens(W.bf16_bits(x)), ids, wts, wl.E, wl.H, wl.I, "relu2")
+    x2 = (x.float() * 4.0).to(torch.bfloat16)
+    r1 = O.forward_w4a4(Wt, *O.quantize_tokens(W.bf16_bits(x2)), ids, wts, wl.E, wl.H, wl.I, "relu2")
+    assert np.array_equal(O.bf16_to_f32(r1["route"]), O.bf16_to_f32(r0["route"]) * 16.0)
+    assert np.array_equal(r1["fc2c"], r0["fc2c"]) and np.array_equal(r1["fc2sf"], r0["fc2sf"])
