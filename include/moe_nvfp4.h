@@ -1,0 +1,201 @@
+/*
+ * moe_nvfp4.h -- C ABI of libmoe_nvfp4.so: a single-GPU routed mixture-of-
+ * experts expert layer in NVFP4 for GB300 (sm_103a).
+ *
+ * Sources (web pages, cited by title and section):
+ *   [MLM] Megatron-LM PR #8262 "per-token NVFP4 squared-ReLU and SwiGLU MoE via
+ *         FlashInfer CuTe DSL" -- Background, What is added, How to extend.
+ *   [FI]  FlashInfer PR #5019 "CuTe DSL NVFP4 W4A16 MegaMoE" -- Tensor and
+ *         numerical contract.
+ *
+ * Conventions for every entry point:
+ *   - All data pointers are DEVICE pointers of the current CUDA device unless
+ *     stated otherwise; the caller owns every buffer.  The library never
+ *     allocates, frees or synchronises in prepare / quantize / forward, so those
+ *     calls can be captured in a CUDA graph once the device check below has run
+ *     (it runs on the first call on each device; make that call outside capture).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *     enqueued on it; results are valid once the stream reaches that point.
+ *   - Host-side validation runs first.  On any error nothing is launched and
+ *     nothing is written, and the status code says why.
+ *   - bf16 is IEEE bfloat16 stored as 2 bytes; E2M1 codes are packed two per
+ *     byte, element 2j in the low nibble; E4M3 scales are one byte each (the
+ *     "fn" variant: bias 7, max 448, no infinities).
+ *   - Shape limits of this version: 1 <= E <= 1024; H and I multiples of 256 in
+ *     [256, 65536]; 1 <= K <= min(32, E) ([FI] Tensor and numerical contract,
+ *     supported scope); 0 <= T and T*K <= 2^26.
+ */
+#ifndef MOE_NVFP4_H_
+#define MOE_NVFP4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,        /* null pointer, negative size, bad enum      */
+  MOE_ERR_UNSUPPORTED_SHAPE = 2,  /* outside the shape limits above             */
+  MOE_ERR_MISALIGNED = 3,         /* a pointer is not aligned as documented     */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 4,
+  MOE_ERR_UNSUPPORTED_DEVICE = 5, /* current device is not compute capability 10.3 */
+  MOE_ERR_CUDA = 6,               /* a CUDA runtime/driver call failed          */
+  MOE_ERR_BAD_EXPERT_ID = 7,      /* device-reported: an id outside [-1, E)     */
+  MOE_ERR_DEVICE_TIMEOUT = 8      /* device-reported: a bounded wait gave up    */
+} moe_status;
+
+typedef enum { MOE_ACT_RELU2 = 0, MOE_ACT_SWIGLU = 1 } moe_act;
+
+/* Layer shape.  N1 = I for squared ReLU, 2I for SwiGLU ([MLM] What is added:
+ * SwiGLU's FC1 has twice FC2's input width; [FI]: gate-then-up FC1). */
+typedef struct {
+  int32_t E; /* experts                 */
+  int32_t H; /* hidden size             */
+  int32_t I; /* intermediate size       */
+  int32_t act; /* moe_act               */
+} moe_dims;
+
+/* Prepared NVFP4 weights ([MLM] What is added: packed E2M1, 128x4-swizzled E4M3
+ * block scales, per-expert FP32 alphas; [FI] Tensor and numerical contract:
+ * scale plane of P = round_up(N,128)*round_up(D/16,4) bytes per expert, alpha
+ * kept separate, never folded into scales).  All device pointers, 16-byte
+ * aligned (alphas 4-byte).  Stored layouts:
+ *   fc1_codes [E][N1][H/2]  K-contiguous rows.  For SwiGLU the stored row order
+ *                           interleaves 128-row blocks: stored rows
+ *                           [256f, 256f+128) are gate rows [128f, 128f+128) and
+ *                           stored rows [256f+128, 256f+256) are up rows
+ *                           I+[128f, 128f+128).  Squared ReLU keeps row order.
+ *   fc1_sf    [E][N1*H/16]  swizzled: byte of (stored row r, scale column j) is
+ *                           ((r/128)*(H/64) + j/4)*512 + (r%32)*16 + ((r/32)%4)*4 + j%4
+ *   fc1_alpha [E]           1 / w_scale, w_scale = 2688 / amax(expert FC1)
+ *   fc2_codes [E][H][I/2], fc2_sf [E][H*I/16] (same swizzle), fc2_alpha [E]. */
+typedef struct {
+  uint8_t* fc1_codes;
+  uint8_t* fc1_sf;
+  float* fc1_alpha;
+  uint8_t* fc2_codes;
+  uint8_t* fc2_sf;
+  float* fc2_alpha;
+} moe_nvfp4_weights;
+
+/* Byte offsets of the workspace regions for one (dims, T, K, variant); used by
+ * tests and debuggers to read intermediate results.  Offsets are from the
+ * workspace base; a region that the variant does not use has size 0. */
+typedef struct {
+  size_t total;
+  int64_t rows_cap;      /* padded permuted rows reserved (multiple of 128) */
+  size_t status;         /* int32[16]: [0] error bits, [1] token tiles, [2] padded rows */
+  size_t counts;         /* int32[E] routes per expert                     */
+  size_t group_row0;     /* int32[E] first permuted row of each expert     */
+  size_t tile_expert;    /* int32[rows_cap/128]                            */
+  size_t tile_rows;      /* int32[rows_cap/128] valid rows of each tile    */
+  size_t chunk_counts;   /* int32[ceil(T*K/256)][E]                        */
+  size_t chunk_prefix;   /* int32[ceil(T*K/256)][E]                        */
+  size_t inv;            /* int32[T*K] permuted row of route t*K+k, or -1   */
+  size_t perm;           /* int32[rows_cap] route id t*K+k of a valid row   */
+  size_t xq_codes;       /* W4A4: u8[rows_cap][H/2] permuted token codes    */
+  size_t xq_sf;          /* W4A4: u8 swizzled over permuted rows, H/16 cols */
+  size_t xq_scale;       /* W4A4: f32[rows_cap] per-row token scale        */
+  size_t act;            /* W4A4: f32[rows_cap][I] activated FC1 rows       */
+  size_t fc2q_codes;     /* W4A4: u8[rows_cap][I/2] requantized FC2 input   */
+  size_t fc2q_sf;        /* W4A4: u8 swizzled over permuted rows, I/16 cols */
+  size_t fc2q_scale;     /* W4A4: f32[rows_cap] FC2-input row scale s2      */
+  size_t x_perm;         /* W4A16: bf16[rows_cap][H] permuted token rows    */
+  size_t act_bf16;       /* W4A16: bf16[rows_cap][I] activated FC1 rows     */
+  size_t route;          /* bf16[rows_cap][H] per-route FC2 rows            */
+} moe_ws_layout;
+
+/* ABI version of this header (bumped on any incompatible change). */
+#define MOE_NVFP4_ABI_VERSION 1
+int32_t moe_nvfp4_abi_version(void);
+
+/* Human-readable text of a status code (static storage). */
+const char* moe_nvfp4_status_string(moe_status s);
+
+/* Byte sizes of the six prepared-weight buffers, in the order of
+ * moe_nvfp4_weights' members.  Host only, no CUDA calls. */
+moe_status moe_nvfp4_weight_sizes(const moe_dims* d, size_t bytes_out[6]);
+
+/* Stage 1, weight prep ([MLM] What is added: prepare_routed_nvfp4_weights;
+ * How to extend: alpha = 1/w_scale).  fc1_bf16 is [E][N1][H] in canonical row
+ * order ([gate; up] for SwiGLU), fc2_bf16 is [E][H][I]; both 16-byte aligned.
+ * Writes every byte of `out` (in place: re-running refreshes the same buffers,
+ * so addresses captured by CUDA graphs stay valid).  Per expert and FC:
+ * amax over the matrix, w_scale = 2688/amax, rows quantized with enc = w_scale,
+ * alpha = 1/w_scale (0 and all-zero codes for an all-zero expert). */
+moe_status moe_nvfp4_prepare_weights(const moe_dims* d, const void* fc1_bf16,
+                                     const void* fc2_bf16, const moe_nvfp4_weights* out,
+                                     moe_stream_t stream);
+
+/* Stage 2, per-token activation quantization ([MLM] Background: one FP32 scale
+ * per token; What is added: global scale = recipe constant 1/(448*6), no host
+ * sync).  x_bf16 [T][H] -> codes [T][H/2], linear block scales sf [T][H/16],
+ * scale [T] = amax_t / 2688 (0 for an all-zero row).  x, codes, sf 16-byte
+ * aligned; scale 4-byte aligned.  T == 0 is a no-op. */
+moe_status moe_nvfp4_quantize_tokens(int32_t T, int32_t H, const void* x_bf16, uint8_t* codes,
+                                     uint8_t* sf, float* scale, moe_stream_t stream);
+
+/* Workspace bytes that moe_nvfp4_forward (w4a16 = 0) or
+ * moe_nvfp4_forward_w4a16 (w4a16 = 1) needs for up to T_max tokens with top-K.
+ * Host only.  Returns 0 for invalid arguments. */
+size_t moe_nvfp4_workspace_bytes(const moe_dims* d, int32_t T_max, int32_t K, int32_t w4a16);
+
+/* Region offsets of the workspace for exactly T tokens (host only). */
+moe_status moe_nvfp4_workspace_layout(const moe_dims* d, int32_t T, int32_t K, int32_t w4a16,
+                                      moe_ws_layout* out);
+
+/* Stages 3-6, W4A4 forward ([MLM] What is added: flashinfer_routed_nvfp4_moe
+ * with the two-stage finalize; How to extend: fc1_alpha = fc2_alpha =
+ * 1/w_scale, per_token_scale from the quantizer, fc2_input_scale = 1/(448*6)).
+ *   codes/sf/scale: the output of moe_nvfp4_quantize_tokens for the T tokens.
+ *   topk_ids int32 [T][K]: expert of each slot, -1 = empty slot; an id outside
+ *     [-1, E) is treated as empty and reported by moe_nvfp4_read_status.
+ *   topk_w fp32 [T][K]: routing score of each slot.
+ *   out_bf16 [T][H]: out[t] = bf16( sum_{k ascending} topk_w[t,k] * route(t,k) )
+ *     with route(t,k) = bf16( FC2(requant(act(FC1(x_t)))) ) of expert
+ *     topk_ids[t,k]; an fp32 accumulator from +0; no route -> zeros.  The sum
+ *     order and every per-route value are independent of the other tokens in
+ *     the batch, so each token's output is bitwise batch invariant.
+ *   ws: at least moe_nvfp4_workspace_bytes(d, T, K, 0) bytes, 256-byte aligned;
+ *     one workspace per stream (concurrent calls need distinct workspaces).
+ * T == 0 is a no-op. */
+moe_status moe_nvfp4_forward(const moe_dims* d, const moe_nvfp4_weights* w, int32_t T, int32_t K,
+                             const uint8_t* codes, const uint8_t* sf, const float* scale,
+                             const int32_t* topk_ids, const float* topk_w, void* out_bf16,
+                             void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* W4A16 forward ([MLM] How to extend: BF16 x NVFP4 'weight_only'; [FI] Tensor
+ * and numerical contract, compute order): BF16 activations x_bf16 [T][H] meet
+ * the same prepared weights, decoded on chip (E2M1 x E4M3 is exact in bf16);
+ * fp32 accumulation; FC1 times alpha1, activation, bf16 handoff; FC2 times
+ * alpha2, bf16 route rows; the same finalize.  Other arguments as
+ * moe_nvfp4_forward; ws sized with w4a16 = 1. */
+moe_status moe_nvfp4_forward_w4a16(const moe_dims* d, const moe_nvfp4_weights* w, int32_t T,
+                                   int32_t K, const void* x_bf16, const int32_t* topk_ids,
+                                   const float* topk_w, void* out_bf16, void* ws,
+                                   size_t ws_bytes, moe_stream_t stream);
+
+/* Device-reported status of the last forward that used `ws`: synchronises
+ * `stream`, then returns MOE_ERR_BAD_EXPERT_ID, MOE_ERR_DEVICE_TIMEOUT or
+ * MOE_OK.  The flags are cleared at the start of every forward.  Debug/test
+ * helper; not capturable. */
+moe_status moe_nvfp4_read_status(const void* ws, moe_stream_t stream);
+
+/* Profiling hook: register `n` cudaEvent_t handles (host pointer to an array of
+ * event handles; n == 0 or events == NULL unregisters).  While registered,
+ * every forward records events[0] before its first stage and events[i] after
+ * stage i (1 routing, 2 FC1, 3 FC2-input requant or nothing for W4A16,
+ * 4 FC2, 5 finalize) on its stream, for i < n.  Process-wide, not thread-safe;
+ * for benchmarks only.  The events must stay alive while registered. */
+moe_status moe_nvfp4_profile_events(void* const* events, int32_t n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_NVFP4_H_ */

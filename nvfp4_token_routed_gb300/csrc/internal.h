@@ -1,0 +1,83 @@
+// internal.h -- declarations shared by the host runtime and the kernel files.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace moe {
+
+// Rows of one token tile of the grouped GEMMs.  Every expert group in the
+// permuted buffers starts at a multiple of this, so a tile has one expert.
+constexpr int kTileRows = 128;
+
+// Workspace status words (int32).
+constexpr int kStatusFlags = 0;   // error bits, see below
+constexpr int kStatusTiles = 1;   // number of token tiles after the scan
+constexpr int kStatusRows = 2;    // padded rows in use after the scan
+constexpr int kStatusWords = 16;
+
+constexpr int kFlagBadExpertId = 1;   // an id outside [-1, E) was seen (slot ignored)
+constexpr int kFlagWaitTimeout = 2;   // a bounded in-kernel wait gave up
+
+struct RouteArgs {
+  int TK, K, E, H;
+  int w4a16;
+  const int32_t* ids;
+  int32_t* status;
+  int32_t* chunk_counts;
+  int32_t* chunk_prefix;
+  int32_t* counts;
+  int32_t* group_row0;
+  int32_t* tile_expert;
+  int32_t* tile_rows;
+  int32_t* inv;
+  int32_t* perm;
+  // W4A4 gather
+  const uint8_t* xc;
+  const uint8_t* xsf;
+  const float* xs;
+  uint8_t* pc;
+  uint8_t* psf;
+  float* ps;
+  // W4A16 gather
+  const void* xb;
+  void* pb;
+};
+
+// Grouped GEMM over the token tiles produced by the routing scan.
+// A = weights (rows of one expert, K-major), B = permuted token rows (K-major).
+enum GemmMode { kFc1Relu2 = 0, kFc1Swiglu = 1, kFc2 = 2 };
+
+struct GemmArgs {
+  int mode;            // GemmMode
+  int K;               // reduction length (H for FC1, I for FC2)
+  int m_tiles;         // 256-row weight tiles per expert
+  int w_rows;          // weight rows per expert (N1 for FC1, H for FC2)
+  const uint8_t* sfa;  // weight scales, swizzled, [E][w_rows * K/16]
+  const uint8_t* sfb;  // token scales, swizzled over permuted rows
+  const float* alpha;  // [E]
+  const float* row_scale;  // per permuted row: s_t (FC1) or s2 (FC2)
+  const int32_t* tile_expert;
+  const int32_t* tile_rows;
+  int32_t* status;
+  float* act_out;      // FC1: [rows][I] fp32
+  int I;
+  uint16_t* route_out; // FC2: [rows][H] bf16
+  int H;
+};
+
+void launch_quantize_tokens(int T, int H, const void* x, uint8_t* codes, uint8_t* sf, float* scale,
+                            cudaStream_t s);
+void launch_prepare_fc(int E, int N, int D, int swiglu_I, const void* w, uint8_t* codes,
+                       uint8_t* sf, float* alpha, cudaStream_t s);
+void launch_route(const RouteArgs& a, cudaStream_t s);
+void launch_requant(int TK, int I, const int32_t* inv, const float* act, uint8_t* qc, uint8_t* qsf,
+                    float* qs, cudaStream_t s);
+void launch_finalize(int T, int K, int H, const int32_t* inv, const float* w, const void* route,
+                     void* out, cudaStream_t s);
+cudaError_t launch_gemm_w4a4(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+                             int grid, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,406 @@
+// moe_api.cu -- host runtime behind include/moe_nvfp4.h: argument validation,
+// workspace layout, tensor-map construction and the launch sequence of each
+// entry point.  No allocation, no host synchronisation on the forward path.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <algorithm>
+
+#include "../../include/moe_nvfp4.h"
+#include "internal.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  int checked = 0;  // 0 unknown, 1 ok, -1 unsupported
+  int sms = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+moe_status check_device(int* sms_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  DeviceInfo& di = g_dev[dev];
+  if (di.checked == 0) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (di.checked == 0) {
+      int major = 0, minor = 0, sms = 0;
+      if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      di.sms = sms;
+      di.checked = (major == 10 && minor == 3) ? 1 : -1;
+    }
+  }
+  if (di.checked < 0) return MOE_ERR_UNSUPPORTED_DEVICE;
+  if (sms_out) *sms_out = di.sms;
+  return MOE_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+moe_status check_dims(const moe_dims* d) {
+  if (!d) return MOE_ERR_INVALID_ARG;
+  if (d->act != MOE_ACT_RELU2 && d->act != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
+  if (d->E < 1 || d->E > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d->H < 256 || d->H > 65536 || d->H % 256) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d->I < 256 || d->I > 65536 || d->I % 256) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+moe_status check_tk(const moe_dims* d, int32_t T, int32_t K) {
+  if (T < 0 || K < 1) return MOE_ERR_INVALID_ARG;
+  if (K > 32 || K > d->E) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((int64_t)T * K > (int64_t(1) << 26)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+int64_t n1_of(const moe_dims* d) { return d->act == MOE_ACT_SWIGLU ? 2LL * d->I : d->I; }
+
+size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+void compute_layout(const moe_dims* d, int32_t T, int32_t K, int32_t w4a16, moe_ws_layout* L) {
+  std::memset(L, 0, sizeof(*L));
+  const int64_t TK = (int64_t)T * K;
+  const int64_t E = d->E, H = d->H, I = d->I;
+  const int64_t pad_groups = TK < E ? TK : E;
+  int64_t rows = TK + pad_groups * (kTileRows - 1);
+  rows = (rows + kTileRows - 1) / kTileRows * kTileRows;
+  const int64_t tiles = rows / kTileRows;
+  const int64_t nchunks = (TK + 255) / 256;
+  L->rows_cap = rows;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = up256(off + bytes);
+    return o;
+  };
+  L->status = take(sizeof(int32_t) * kStatusWords);
+  L->counts = take(sizeof(int32_t) * E);
+  L->group_row0 = take(sizeof(int32_t) * E);
+  L->tile_expert = take(sizeof(int32_t) * (tiles ? tiles : 1));
+  L->tile_rows = take(sizeof(int32_t) * (tiles ? tiles : 1));
+  L->chunk_counts = take(sizeof(int32_t) * nchunks * E);
+  L->chunk_prefix = take(sizeof(int32_t) * nchunks * E);
+  L->inv = take(sizeof(int32_t) * TK);
+  L->perm = take(sizeof(int32_t) * rows);
+  if (!w4a16) {
+    L->xq_codes = take((size_t)rows * (H / 2));
+    L->xq_sf = take((size_t)rows * (H / 16));
+    L->xq_scale = take(sizeof(float) * rows);
+    L->act = take(sizeof(float) * (size_t)rows * I);
+    L->fc2q_codes = take((size_t)rows * (I / 2));
+    L->fc2q_sf = take((size_t)rows * (I / 16));
+    L->fc2q_scale = take(sizeof(float) * rows);
+  } else {
+    L->x_perm = take(sizeof(uint16_t) * (size_t)rows * H);
+    L->act_bf16 = take(sizeof(uint16_t) * (size_t)rows * I);
+  }
+  L->route = take(sizeof(uint16_t) * (size_t)rows * H);
+  L->total = off;
+}
+
+// ---------------------------------------------------------------- tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D byte tensor [rows][row_bytes] (row stride = row_bytes), box of
+// box_rows x 128 bytes with the 128-byte swizzle.
+bool make_tmap_bytes(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows,
+                     uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {row_bytes, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+moe_status check_weights(const moe_nvfp4_weights* w) {
+  if (!w || !w->fc1_codes || !w->fc1_sf || !w->fc1_alpha || !w->fc2_codes || !w->fc2_sf ||
+      !w->fc2_alpha)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(w->fc1_codes, 16) || !aligned(w->fc1_sf, 16) || !aligned(w->fc2_codes, 16) ||
+      !aligned(w->fc2_sf, 16) || !aligned(w->fc1_alpha, 4) || !aligned(w->fc2_alpha, 4))
+    return MOE_ERR_MISALIGNED;
+  return MOE_OK;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// Profiling events (moe_nvfp4_profile_events).
+constexpr int kMaxProfileEvents = 8;
+cudaEvent_t g_prof[kMaxProfileEvents];
+int g_nprof = 0;
+
+void mark(int i, cudaStream_t s) {
+  if (i < g_nprof && g_prof[i]) cudaEventRecord(g_prof[i], s);
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t moe_nvfp4_abi_version(void) { return MOE_NVFP4_ABI_VERSION; }
+
+const char* moe_nvfp4_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_MISALIGNED: return "misaligned pointer";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3)";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_BAD_EXPERT_ID: return "expert id outside [-1, E) (slot ignored)";
+    case MOE_ERR_DEVICE_TIMEOUT: return "an in-kernel wait timed out";
+  }
+  return "unknown status";
+}
+
+moe_status moe_nvfp4_weight_sizes(const moe_dims* d, size_t bytes_out[6]) {
+  moe_status st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if (!bytes_out) return MOE_ERR_INVALID_ARG;
+  const size_t E = d->E, H = d->H, I = d->I, N1 = (size_t)n1_of(d);
+  bytes_out[0] = E * N1 * (H / 2);
+  bytes_out[1] = E * N1 * (H / 16);
+  bytes_out[2] = E * sizeof(float);
+  bytes_out[3] = E * H * (I / 2);
+  bytes_out[4] = E * H * (I / 16);
+  bytes_out[5] = E * sizeof(float);
+  return MOE_OK;
+}
+
+moe_status moe_nvfp4_prepare_weights(const moe_dims* d, const void* fc1_bf16,
+                                     const void* fc2_bf16, const moe_nvfp4_weights* out,
+                                     moe_stream_t stream) {
+  moe_status st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if (!fc1_bf16 || !fc2_bf16) return MOE_ERR_INVALID_ARG;
+  if (!aligned(fc1_bf16, 16) || !aligned(fc2_bf16, 16)) return MOE_ERR_MISALIGNED;
+  if ((st = check_weights(out)) != MOE_OK) return st;
+  if ((st = check_device(nullptr)) != MOE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int N1 = (int)n1_of(d);
+  launch_prepare_fc(d->E, N1, d->H, d->act == MOE_ACT_SWIGLU ? d->I : 0, fc1_bf16, out->fc1_codes,
+                    out->fc1_sf, out->fc1_alpha, s);
+  launch_prepare_fc(d->E, d->H, d->I, 0, fc2_bf16, out->fc2_codes, out->fc2_sf, out->fc2_alpha, s);
+  return cuda_status(cudaGetLastError());
+}
+
+moe_status moe_nvfp4_quantize_tokens(int32_t T, int32_t H, const void* x_bf16, uint8_t* codes,
+                                     uint8_t* sf, float* scale, moe_stream_t stream) {
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (H < 256 || H > 65536 || H % 256) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (T == 0) return MOE_OK;
+  if (!x_bf16 || !codes || !sf || !scale) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x_bf16, 16) || !aligned(codes, 16) || !aligned(sf, 16) || !aligned(scale, 4))
+    return MOE_ERR_MISALIGNED;
+  moe_status st = check_device(nullptr);
+  if (st != MOE_OK) return st;
+  launch_quantize_tokens(T, H, x_bf16, codes, sf, scale, reinterpret_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
+}
+
+size_t moe_nvfp4_workspace_bytes(const moe_dims* d, int32_t T_max, int32_t K, int32_t w4a16) {
+  if (check_dims(d) != MOE_OK || check_tk(d, T_max, K) != MOE_OK) return 0;
+  moe_ws_layout L;
+  compute_layout(d, T_max, K, w4a16 ? 1 : 0, &L);
+  return L.total;
+}
+
+moe_status moe_nvfp4_workspace_layout(const moe_dims* d, int32_t T, int32_t K, int32_t w4a16,
+                                      moe_ws_layout* out) {
+  moe_status st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if ((st = check_tk(d, T, K)) != MOE_OK) return st;
+  if (!out) return MOE_ERR_INVALID_ARG;
+  compute_layout(d, T, K, w4a16 ? 1 : 0, out);
+  return MOE_OK;
+}
+
+static moe_status forward_common(const moe_dims* d, const moe_nvfp4_weights* w, int32_t T,
+                                 int32_t K, const int32_t* topk_ids, const float* topk_w,
+                                 void* out_bf16, void* ws, size_t ws_bytes, int w4a16,
+                                 moe_ws_layout* L, int* sms) {
+  moe_status st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if ((st = check_tk(d, T, K)) != MOE_OK) return st;
+  if ((st = check_weights(w)) != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  if (!topk_ids || !topk_w || !out_bf16 || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned(topk_ids, 4) || !aligned(topk_w, 4) || !aligned(out_bf16, 16) || !aligned(ws, 256))
+    return MOE_ERR_MISALIGNED;
+  compute_layout(d, T, K, w4a16, L);
+  if (ws_bytes < L->total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return check_device(sms);
+}
+
+static RouteArgs route_args(const moe_dims* d, int32_t T, int32_t K, const int32_t* ids, void* ws,
+                            const moe_ws_layout& L, int w4a16) {
+  RouteArgs r{};
+  r.TK = T * K;
+  r.K = K;
+  r.E = d->E;
+  r.H = d->H;
+  r.w4a16 = w4a16;
+  r.ids = ids;
+  r.status = at<int32_t>(ws, L.status);
+  r.chunk_counts = at<int32_t>(ws, L.chunk_counts);
+  r.chunk_prefix = at<int32_t>(ws, L.chunk_prefix);
+  r.counts = at<int32_t>(ws, L.counts);
+  r.group_row0 = at<int32_t>(ws, L.group_row0);
+  r.tile_expert = at<int32_t>(ws, L.tile_expert);
+  r.tile_rows = at<int32_t>(ws, L.tile_rows);
+  r.inv = at<int32_t>(ws, L.inv);
+  r.perm = at<int32_t>(ws, L.perm);
+  return r;
+}
+
+moe_status moe_nvfp4_forward(const moe_dims* d, const moe_nvfp4_weights* w, int32_t T, int32_t K,
+                             const uint8_t* codes, const uint8_t* sf, const float* scale,
+                             const int32_t* topk_ids, const float* topk_w, void* out_bf16,
+                             void* ws, size_t ws_bytes, moe_stream_t stream) {
+  moe_ws_layout L;
+  int sms = 0;
+  moe_status st =
+      forward_common(d, w, T, K, topk_ids, topk_w, out_bf16, ws, ws_bytes, 0, &L, &sms);
+  if (st != MOE_OK || T == 0) return st;
+  if (!codes || !sf || !scale) return MOE_ERR_INVALID_ARG;
+  if (!aligned(codes, 16) || !aligned(sf, 16) || !aligned(scale, 4)) return MOE_ERR_MISALIGNED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int H = d->H, I = d->I, N1 = (int)n1_of(d);
+
+  CUtensorMap tmA1, tmB1, tmA2, tmB2;
+  if (!make_tmap_bytes(&tmA1, w->fc1_codes, H / 2, (uint64_t)d->E * N1, 128) ||
+      !make_tmap_bytes(&tmB1, at<uint8_t>(ws, L.xq_codes), H / 2, L.rows_cap, 16) ||
+      !make_tmap_bytes(&tmA2, w->fc2_codes, I / 2, (uint64_t)d->E * H, 128) ||
+      !make_tmap_bytes(&tmB2, at<uint8_t>(ws, L.fc2q_codes), I / 2, L.rows_cap, 16))
+    return MOE_ERR_CUDA;
+
+  cudaError_t err = cudaMemsetAsync(at<int32_t>(ws, L.status), 0, sizeof(int32_t) * kStatusWords, s);
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
+
+  mark(0, s);
+  RouteArgs r = route_args(d, T, K, topk_ids, ws, L, 0);
+  r.xc = codes;
+  r.xsf = sf;
+  r.xs = scale;
+  r.pc = at<uint8_t>(ws, L.xq_codes);
+  r.psf = at<uint8_t>(ws, L.xq_sf);
+  r.ps = at<float>(ws, L.xq_scale);
+  launch_route(r, s);
+  mark(1, s);
+
+  const int64_t tiles_cap = L.rows_cap / kTileRows;
+  GemmArgs g{};
+  g.mode = d->act == MOE_ACT_SWIGLU ? kFc1Swiglu : kFc1Relu2;
+  g.K = H;
+  g.m_tiles = N1 / 256;
+  g.w_rows = N1;
+  g.sfa = w->fc1_sf;
+  g.sfb = at<uint8_t>(ws, L.xq_sf);
+  g.alpha = w->fc1_alpha;
+  g.row_scale = at<float>(ws, L.xq_scale);
+  g.tile_expert = at<int32_t>(ws, L.tile_expert);
+  g.tile_rows = at<int32_t>(ws, L.tile_rows);
+  g.status = at<int32_t>(ws, L.status);
+  g.act_out = at<float>(ws, L.act);
+  g.I = I;
+  g.H = H;
+  int grid = (int)std::min<int64_t>(sms, tiles_cap * g.m_tiles);
+  if ((err = launch_gemm_w4a4(tmA1, tmB1, g, grid, s)) != cudaSuccess) return MOE_ERR_CUDA;
+  mark(2, s);
+
+  launch_requant(T * K, I, at<int32_t>(ws, L.inv), at<float>(ws, L.act),
+                 at<uint8_t>(ws, L.fc2q_codes), at<uint8_t>(ws, L.fc2q_sf),
+                 at<float>(ws, L.fc2q_scale), s);
+  mark(3, s);
+
+  GemmArgs g2 = g;
+  g2.mode = kFc2;
+  g2.K = I;
+  g2.m_tiles = H / 256;
+  g2.w_rows = H;
+  g2.sfa = w->fc2_sf;
+  g2.sfb = at<uint8_t>(ws, L.fc2q_sf);
+  g2.alpha = w->fc2_alpha;
+  g2.row_scale = at<float>(ws, L.fc2q_scale);
+  g2.act_out = nullptr;
+  g2.route_out = at<uint16_t>(ws, L.route);
+  grid = (int)std::min<int64_t>(sms, tiles_cap * g2.m_tiles);
+  if ((err = launch_gemm_w4a4(tmA2, tmB2, g2, grid, s)) != cudaSuccess) return MOE_ERR_CUDA;
+  mark(4, s);
+
+  launch_finalize(T, K, H, at<int32_t>(ws, L.inv), topk_w, at<uint16_t>(ws, L.route), out_bf16, s);
+  mark(5, s);
+  return cuda_status(cudaGetLastError());
+}
+
+moe_status moe_nvfp4_forward_w4a16(const moe_dims* d, const moe_nvfp4_weights* w, int32_t T,
+                                   int32_t K, const void* x_bf16, const int32_t* topk_ids,
+                                   const float* topk_w, void* out_bf16, void* ws,
+                                   size_t ws_bytes, moe_stream_t stream) {
+  moe_ws_layout L;
+  int sms = 0;
+  moe_status st =
+      forward_common(d, w, T, K, topk_ids, topk_w, out_bf16, ws, ws_bytes, 1, &L, &sms);
+  if (st != MOE_OK || T == 0) return st;
+  if (!x_bf16) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x_bf16, 16)) return MOE_ERR_MISALIGNED;
+  (void)stream;
+  return MOE_ERR_UNSUPPORTED_SHAPE;  // filled in by the W4A16 kernels
+}
+
+moe_status moe_nvfp4_profile_events(void* const* events, int32_t n) {
+  if (n < 0 || n > kMaxProfileEvents) return MOE_ERR_INVALID_ARG;
+  if (!events) n = 0;
+  for (int i = 0; i < kMaxProfileEvents; ++i)
+    g_prof[i] = i < n ? static_cast<cudaEvent_t>(events[i]) : nullptr;
+  g_nprof = n;
+  return MOE_OK;
+}
+
+moe_status moe_nvfp4_read_status(const void* ws, moe_stream_t stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  int32_t flags = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&flags, ws, sizeof(flags), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (flags & kFlagWaitTimeout) return MOE_ERR_DEVICE_TIMEOUT;
+  if (flags & kFlagBadExpertId) return MOE_ERR_BAD_EXPERT_ID;
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,390 @@
+// moe_kernels.cu -- the bandwidth-bound stages of the routed NVFP4 MoE layer:
+// per-token quantization, weight preparation, the routing permutation (count,
+// scan, scatter + gather), the FC2-input requantization and the deterministic
+// top-k finalize.  Every kernel moves data in 16-byte vectors, one warp per row.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+#include "quant.cuh"
+
+namespace moe {
+
+// ============================================================== token quantization
+// Megatron-LM PR #8262, "What is added": quantize_routed_nvfp4_input quantizes
+// activations per token with the recipe constant 1/(448*6) as global scale.
+// One warp per token: warp-shuffle amax, then one 16-element block per lane.
+__global__ void __launch_bounds__(256) quantize_tokens_kernel(int T, int H,
+                                                              const uint4* __restrict__ x,
+                                                              uint8_t* __restrict__ codes,
+                                                              uint8_t* __restrict__ sf,
+                                                              float* __restrict__ scale) {
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const uint4* row = x + (size_t)t * (H / 8);
+  float m = 0.0f;
+  for (int i = lane; i < H / 8; i += 32) m = fmaxf(m, bf16x8_absmax(__ldg(row + i)));
+  m = warp_max(m);
+  uint2* crow = reinterpret_cast<uint2*>(codes + (size_t)t * (H / 2));
+  uint8_t* srow = sf + (size_t)t * (H / 16);
+  if (m == 0.0f) {
+    for (int b = lane; b < H / 16; b += 32) {
+      crow[b] = make_uint2(0u, 0u);
+      srow[b] = 0;
+    }
+    if (lane == 0) scale[t] = 0.0f;
+    return;
+  }
+  const float enc = __fdiv_rn(kRecipeMax, m);
+  for (int b = lane; b < H / 16; b += 32) {
+    float v[16];
+    bf16x16_to_f32(__ldg(row + 2 * b), __ldg(row + 2 * b + 1), v);
+    uint2 q;
+    srow[b] = (uint8_t)quant_block16(v, enc, q);
+    crow[b] = q;
+  }
+  if (lane == 0) scale[t] = __fmul_rn(m, kRecipeInv);
+}
+
+void launch_quantize_tokens(int T, int H, const void* x, uint8_t* codes, uint8_t* sf, float* scale,
+                            cudaStream_t s) {
+  const int warps = 8;
+  const int blocks = (T + warps - 1) / warps;
+  quantize_tokens_kernel<<<blocks, warps * 32, 0, s>>>(T, H, static_cast<const uint4*>(x), codes,
+                                                       sf, scale);
+}
+
+// ============================================================== weight preparation
+// Megatron-LM PR #8262, "What is added": prepare_routed_nvfp4_weights -> packed
+// E2M1, 128x4-swizzled E4M3 block scales, one fp32 alpha per expert; "How to
+// extend": alpha = 1 / w_scale.  Stage 1: per-expert amax (order-free max,
+// accumulated as the bit pattern of a non-negative float into alpha[]).
+__global__ void __launch_bounds__(256) expert_amax_kernel(const uint4* __restrict__ w,
+                                                          int64_t vec_per_expert,
+                                                          uint32_t* __restrict__ amax_bits) {
+  const int e = blockIdx.y;
+  const uint4* base = w + (size_t)e * vec_per_expert;
+  float m = 0.0f;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < vec_per_expert;
+       i += (int64_t)gridDim.x * blockDim.x)
+    m = fmaxf(m, bf16x8_absmax(__ldg(base + i)));
+  m = warp_max(m);
+  __shared__ float red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float r = red[0];
+    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) r = fmaxf(r, red[i]);
+    atomicMax(amax_bits + e, __float_as_uint(r));
+  }
+}
+
+// Stage 2: one warp per stored row.  For SwiGLU the stored FC1 row order
+// interleaves 128-row blocks [gate f0..f0+127 | up f0..f0+127], so one 256-row
+// GEMM tile holds matching gate and up rows; canonical order is [gate; up].
+__global__ void __launch_bounds__(256) quantize_weights_kernel(
+    const uint4* __restrict__ w, int E, int N, int D, int swiglu_I,
+    const uint32_t* __restrict__ amax_bits, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+    uint64_t sf_expert_bytes) {
+  const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gw >= (int64_t)E * N) return;
+  const int e = (int)(gw / N);
+  const int ir = (int)(gw % N);
+  int cr = ir;
+  if (swiglu_I > 0) {
+    const int b = ir >> 7;
+    cr = (b & 1) * swiglu_I + (b >> 1) * 128 + (ir & 127);
+  }
+  const float amax = __uint_as_float(amax_bits[e]);
+  const uint4* row = w + ((size_t)e * N + cr) * (D / 8);
+  uint2* crow = reinterpret_cast<uint2*>(codes + ((size_t)e * N + ir) * (D / 2));
+  uint8_t* plane = sf + (size_t)e * sf_expert_bytes;
+  const uint32_t c16 = (uint32_t)(D / 16);
+  if (amax == 0.0f) {
+    for (int b = lane; b < D / 16; b += 32) {
+      crow[b] = make_uint2(0u, 0u);
+      plane[sf_offset(ir, b, c16)] = 0;
+    }
+    return;
+  }
+  const float enc = __fdiv_rn(kRecipeMax, amax);
+  for (int b = lane; b < D / 16; b += 32) {
+    float v[16];
+    bf16x16_to_f32(__ldg(row + 2 * b), __ldg(row + 2 * b + 1), v);
+    uint2 q;
+    plane[sf_offset(ir, b, c16)] = (uint8_t)quant_block16(v, enc, q);
+    crow[b] = q;
+  }
+}
+
+// Stage 3: alpha = 1 / w_scale with w_scale = 2688 / amax (0 for an all-zero expert).
+__global__ void expert_alpha_kernel(int E, float* alpha) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= E) return;
+  const float amax = alpha[e];  // still holds the amax bit pattern
+  alpha[e] = amax == 0.0f ? 0.0f : __fdiv_rn(1.0f, __fdiv_rn(kRecipeMax, amax));
+}
+
+void launch_prepare_fc(int E, int N, int D, int swiglu_I, const void* w, uint8_t* codes,
+                       uint8_t* sf, float* alpha, cudaStream_t s) {
+  cudaMemsetAsync(alpha, 0, sizeof(float) * E, s);
+  const int64_t vec = (int64_t)N * D / 8;
+  int bx = (int)((vec + 256 * 8 - 1) / (256 * 8));
+  if (bx > 64) bx = 64;
+  expert_amax_kernel<<<dim3(bx, E), 256, 0, s>>>(static_cast<const uint4*>(w), vec,
+                                                 reinterpret_cast<uint32_t*>(alpha));
+  const int64_t warps = (int64_t)E * N;
+  const uint64_t sf_bytes = (uint64_t)N * (D / 16);  // N % 128 == 0 and D/16 % 4 == 0: no pad
+  quantize_weights_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(
+      static_cast<const uint4*>(w), E, N, D, swiglu_I, reinterpret_cast<const uint32_t*>(alpha),
+      codes, sf, sf_bytes);
+  expert_alpha_kernel<<<(E + 255) / 256, 256, 0, s>>>(E, alpha);
+}
+
+// ============================================================== routing permutation
+// Stable counting sort of the (token, slot) routes by expert: per-chunk
+// histograms, a per-expert scan over chunks plus an exclusive scan of the
+// 128-row-padded group sizes, then a stable scatter that also gathers the
+// quantized rows into expert-contiguous order.
+constexpr int kChunk = 256;
+
+__global__ void __launch_bounds__(kChunk) route_count_kernel(const int32_t* __restrict__ ids,
+                                                             int TK, int E,
+                                                             int32_t* __restrict__ chunk_counts,
+                                                             int32_t* __restrict__ status) {
+  extern __shared__ int s_cnt[];
+  for (int i = threadIdx.x; i < E; i += blockDim.x) s_cnt[i] = 0;
+  __syncthreads();
+  const int idx = blockIdx.x * kChunk + threadIdx.x;
+  if (idx < TK) {
+    const int e = ids[idx];
+    if (e >= 0 && e < E)
+      atomicAdd(&s_cnt[e], 1);
+    else if (e != -1)
+      atomicOr(status + kStatusFlags, kFlagBadExpertId);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < E; i += blockDim.x) chunk_counts[(size_t)blockIdx.x * E + i] = s_cnt[i];
+}
+
+__global__ void __launch_bounds__(1024) route_scan_kernel(
+    int nchunks, int E, const int32_t* __restrict__ chunk_counts, int32_t* __restrict__ chunk_prefix,
+    int32_t* __restrict__ counts, int32_t* __restrict__ group_row0, int32_t* __restrict__ tile_expert,
+    int32_t* __restrict__ tile_rows, int32_t* __restrict__ status) {
+  const int e = threadIdx.x;
+  int total = 0;
+  if (e < E) {
+    for (int c = 0; c < nchunks; ++c) {
+      chunk_prefix[(size_t)c * E + e] = total;
+      total += chunk_counts[(size_t)c * E + e];
+    }
+  }
+  const int ntiles = (total + kTileRows - 1) / kTileRows;
+  // block-wide exclusive scan of ntiles
+  __shared__ int warp_sum[32];
+  const int lane = e & 31, wid = e >> 5;
+  int incl = ntiles;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sum[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    int v = (lane < (int)(blockDim.x >> 5)) ? warp_sum[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, v, o);
+      if (lane >= o) v += y;
+    }
+    warp_sum[lane] = v;  // inclusive over warps
+  }
+  __syncthreads();
+  const int base = incl - ntiles + (wid > 0 ? warp_sum[wid - 1] : 0);
+  if (e < E) {
+    counts[e] = total;
+    group_row0[e] = base * kTileRows;
+    for (int j = 0; j < ntiles; ++j) {
+      tile_expert[base + j] = e;
+      tile_rows[base + j] = min(kTileRows, total - j * kTileRows);
+    }
+  }
+  if (e == (int)blockDim.x - 1) {
+    status[kStatusTiles] = base + ntiles;
+    status[kStatusRows] = (base + ntiles) * kTileRows;
+  }
+}
+
+template <bool kW4A16>
+__global__ void __launch_bounds__(kChunk) route_scatter_kernel(
+    const int32_t* __restrict__ ids, int TK, int K, int E, const int32_t* __restrict__ chunk_prefix,
+    const int32_t* __restrict__ group_row0, int32_t* __restrict__ inv, int32_t* __restrict__ perm,
+    int H, const uint8_t* __restrict__ xc, const uint8_t* __restrict__ xsf,
+    const float* __restrict__ xs, uint8_t* __restrict__ pc, uint8_t* __restrict__ psf,
+    float* __restrict__ ps, const uint4* __restrict__ xb, uint4* __restrict__ pb) {
+  extern __shared__ int s_wcnt[];  // [kChunk/32][E]
+  constexpr int kWarps = kChunk / 32;
+  for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) s_wcnt[i] = 0;
+  __syncthreads();
+  const int idx = blockIdx.x * kChunk + threadIdx.x;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = idx < TK ? ids[idx] : -1;
+  const bool valid = e >= 0 && e < E;
+  const unsigned peers = __match_any_sync(0xFFFFFFFFu, valid ? e : -1);
+  const int rank = __popc(peers & ((1u << lane) - 1u));
+  if (valid && rank == 0) s_wcnt[w * E + e] = __popc(peers);
+  __syncthreads();
+  int p = -1;
+  if (valid) {
+    int before = 0;
+    for (int v = 0; v < w; ++v) before += s_wcnt[v * E + e];
+    p = group_row0[e] + chunk_prefix[(size_t)blockIdx.x * E + e] + before + rank;
+    perm[p] = idx;
+  }
+  if (idx < TK) inv[idx] = p;
+  // gather: the warp copies each of its routes' token rows to their positions
+  for (int l = 0; l < 32; ++l) {
+    const int pp = __shfl_sync(0xFFFFFFFFu, p, l);
+    const int ii = __shfl_sync(0xFFFFFFFFu, idx, l);
+    if (pp < 0) continue;
+    const int t = ii / K;
+    if constexpr (kW4A16) {
+      const uint4* src = xb + (size_t)t * (H / 8);
+      uint4* dst = pb + (size_t)pp * (H / 8);
+      for (int i = lane; i < H / 8; i += 32) dst[i] = __ldg(src + i);
+    } else {
+      const uint4* src = reinterpret_cast<const uint4*>(xc + (size_t)t * (H / 2));
+      uint4* dst = reinterpret_cast<uint4*>(pc + (size_t)pp * (H / 2));
+      for (int i = lane; i < H / 32; i += 32) dst[i] = __ldg(src + i);
+      const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(xsf + (size_t)t * (H / 16));
+      const uint32_t c16 = (uint32_t)(H / 16);
+      for (int g = lane; g < H / 64; g += 32)
+        *reinterpret_cast<uint32_t*>(psf + sf_offset(pp, 4 * g, c16)) = __ldg(ssrc + g);
+      if (lane == 0) ps[pp] = xs[t];
+    }
+  }
+}
+
+void launch_route(const RouteArgs& a, cudaStream_t s) {
+  const int nchunks = (a.TK + kChunk - 1) / kChunk;
+  route_count_kernel<<<nchunks, kChunk, sizeof(int) * a.E, s>>>(a.ids, a.TK, a.E, a.chunk_counts,
+                                                               a.status);
+  route_scan_kernel<<<1, 1024, 0, s>>>(nchunks, a.E, a.chunk_counts, a.chunk_prefix, a.counts,
+                                       a.group_row0, a.tile_expert, a.tile_rows, a.status);
+  const size_t smem = sizeof(int) * (kChunk / 32) * a.E;
+  if (a.w4a16)
+    route_scatter_kernel<true><<<nchunks, kChunk, smem, s>>>(
+        a.ids, a.TK, a.K, a.E, a.chunk_prefix, a.group_row0, a.inv, a.perm, a.H, nullptr, nullptr,
+        nullptr, nullptr, nullptr, nullptr, static_cast<const uint4*>(a.xb),
+        static_cast<uint4*>(a.pb));
+  else
+    route_scatter_kernel<false><<<nchunks, kChunk, smem, s>>>(
+        a.ids, a.TK, a.K, a.E, a.chunk_prefix, a.group_row0, a.inv, a.perm, a.H, a.xc, a.xsf, a.xs,
+        a.pc, a.psf, a.ps, nullptr, nullptr);
+}
+
+// ============================================================== FC2-input requant
+// Megatron-LM PR #8262, "How to extend": fc2_input_scale = 1/(448*6) for the
+// per-token recipe; the FC2 input is quantized per routed row.  One warp per
+// route reads the fp32 activated row written by the FC1 epilogue.
+__global__ void __launch_bounds__(256) requant_kernel(int TK, int I, const int32_t* __restrict__ inv,
+                                                      const float* __restrict__ act,
+                                                      uint8_t* __restrict__ qc,
+                                                      uint8_t* __restrict__ qsf,
+                                                      float* __restrict__ qs) {
+  const int idx = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (idx >= TK) return;
+  const int p = inv[idx];
+  if (p < 0) return;
+  const float4* row = reinterpret_cast<const float4*>(act + (size_t)p * I);
+  float m = 0.0f;
+  for (int i = lane; i < I / 4; i += 32) {
+    const float4 v = row[i];
+    m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  }
+  m = warp_max(m);
+  uint2* crow = reinterpret_cast<uint2*>(qc + (size_t)p * (I / 2));
+  const uint32_t c16 = (uint32_t)(I / 16);
+  if (m == 0.0f) {
+    for (int b = lane; b < I / 16; b += 32) {
+      crow[b] = make_uint2(0u, 0u);
+      qsf[sf_offset(p, b, c16)] = 0;
+    }
+    if (lane == 0) qs[p] = 0.0f;
+    return;
+  }
+  const float enc = __fdiv_rn(kRecipeMax, m);
+  for (int b = lane; b < I / 16; b += 32) {
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 f = row[4 * b + i];
+      v[4 * i] = f.x;
+      v[4 * i + 1] = f.y;
+      v[4 * i + 2] = f.z;
+      v[4 * i + 3] = f.w;
+    }
+    uint2 q;
+    qsf[sf_offset(p, b, c16)] = (uint8_t)quant_block16(v, enc, q);
+    crow[b] = q;
+  }
+  if (lane == 0) qs[p] = __fmul_rn(m, kRecipeInv);
+}
+
+void launch_requant(int TK, int I, const int32_t* inv, const float* act, uint8_t* qc, uint8_t* qsf,
+                    float* qs, cudaStream_t s) {
+  const int warps = 8;
+  requant_kernel<<<(TK + warps - 1) / warps, warps * 32, 0, s>>>(TK, I, inv, act, qc, qsf, qs);
+}
+
+// ============================================================== finalize
+// Megatron-LM PR #8262, "What is added": the two-stage finalize reduces each
+// token's top-k routes in a fixed order; FlashInfer PR #5019, "Tensor and
+// numerical contract": bf16 per-route terms times fp32 scores, one final bf16
+// conversion.  fp32 accumulator from +0, k ascending, one fma per term.
+__global__ void __launch_bounds__(128) finalize_kernel(int K, int H, const int32_t* __restrict__ inv,
+                                                       const float* __restrict__ w,
+                                                       const uint4* __restrict__ route,
+                                                       uint4* __restrict__ out) {
+  const int t = blockIdx.x;
+  const int v = blockIdx.y * blockDim.x + threadIdx.x;
+  if (v >= H / 8) return;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+  for (int k = 0; k < K; ++k) {
+    const int p = inv[(size_t)t * K + k];
+    if (p < 0) continue;
+    const float wk = w[(size_t)t * K + k];
+    const uint4 r = route[(size_t)p * (H / 8) + v];
+    const uint32_t q[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[2 * i] = __fmaf_rn(wk, __uint_as_float(q[i] << 16), acc[2 * i]);
+      acc[2 * i + 1] = __fmaf_rn(wk, __uint_as_float(q[i] & 0xFFFF0000u), acc[2 * i + 1]);
+    }
+  }
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+    o[i] = *reinterpret_cast<const uint32_t*>(&b2);
+  }
+  out[(size_t)t * (H / 8) + v] = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+void launch_finalize(int T, int K, int H, const int32_t* inv, const float* w, const void* route,
+                     void* out, cudaStream_t s) {
+  const int threads = 128;
+  dim3 grid(T, (H / 8 + threads - 1) / threads);
+  finalize_kernel<<<grid, threads, 0, s>>>(K, H, inv, w, static_cast<const uint4*>(route),
+                                           static_cast<uint4*>(out));
+}
+
+}  // namespace moe
