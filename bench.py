@@ -1,0 +1,421 @@
+#!/usr/bin/env python
+"""Benchmark of the routed NVFP4 MoE expert layer on GB300.
+
+One step = per-token quantization + the W4A4 forward (routing permutation,
+FC1 grouped GEMM with fused activation, FC2-input requant, FC2 grouped GEMM,
+deterministic finalize) over one batch of T synthetic tokens, replayed from a
+CUDA graph.  Inputs are resident in HBM; L2 is flushed (a 256 MB write)
+between timed steps, outside the per-step CUDA events.
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle instead
+(bounded samples on the host cores).  Multi-GPU runs (torchrun) are replicas:
+every rank runs the same workload on its own GPU, no collective on the data
+path; value = all tokens / max-over-ranks time.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import nvfp4_token_routed_gb300 as M  # noqa: E402
+from nvfp4_token_routed_gb300 import workloads as W  # noqa: E402
+
+METRIC = "MoE-layer tokens/s and µs/layer at 1 GB300"
+KERNELS_PER_STEP = 8  # quantize, route count/scan/scatter, FC1, requant, FC2, finalize
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=W.SWIGLU_E64.name, choices=list(W.ALL))
+    p.add_argument("--T", type=int, default=0, help="override the workload's token count")
+    p.add_argument("--no-graph", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for f in ("gemm_w4a4.cu", "ptx.cuh", "internal.h"):
+        with open(os.path.join(ROOT, "nvfp4_token_routed_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(workload):
+    """DRAM bytes per FC1 launch from the committed ncu summary, if it still
+    describes the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "fc1_gemm_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("kernel_hash") != kernel_hash():
+        return None
+    return d.get("per_launch_bytes", {}).get(workload)
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def make_inputs(wl, device):
+    big = wl.E * (wl.N1 + wl.I) * wl.H > 2e9
+    gen_dev = device if big else "cpu"
+    x = W.make_x(wl, device=gen_dev)
+    w1, w2 = W.make_weights(wl, device=gen_dev)
+    ids, wts = W.make_routing(wl, device=gen_dev)
+    return x, w1, w2, ids, wts
+
+
+def algorithmic_fc1_bytes(wl, ids):
+    """Algorithmic DRAM bytes of one FC1 launch: each touched expert's FC1 codes
+    and scales once (9/16 byte per weight), the permuted token codes and scales,
+    the fp32 activated rows and the per-row scales."""
+    idsn = ids.cpu().numpy().ravel()
+    valid = idsn[(idsn >= 0) & (idsn < wl.E)]
+    U = int(np.unique(valid).size)
+    R = int(valid.size)
+    return U * wl.N1 * wl.H * 9 / 16 + R * wl.H * 9 / 16 + 4 * R * wl.I + 4 * R, U, R
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample_runner(wl, x, w1, w2, ids, wts):
+    """Build a function that runs the oracle (quantize + W4A4 forward) on the
+    first n tokens of the workload, with only the experts those tokens use."""
+    from oracle import oracle as O
+
+    idsn = ids.cpu().numpy().astype(np.int32)
+    wtn = wts.cpu().numpy().astype(np.float32)
+    xs = W.bf16_bits(x.cpu())
+    cache = {}
+
+    def run(start, n):
+        sl = slice(start, start + n)
+        Wt, remap, Eu = prepared_for(sl)
+        sub_ids = np.where(idsn[sl] >= 0, remap[np.clip(idsn[sl], 0, None)], -1).astype(np.int32)
+        t0 = time.perf_counter()
+        c, f, s = O.quantize_tokens(xs[sl])
+        O.forward_w4a4(Wt, c, f, s, sub_ids, wtn[sl], Eu, wl.H, wl.I, wl.act)
+        return time.perf_counter() - t0
+
+    full = wl.E * (wl.N1 + wl.I) * wl.H <= 1e9   # small enough to prepare every expert once
+
+    def prepared_for(sl):
+        if full:
+            if "all" not in cache:
+                cache["all"] = O.Weights(W.bf16_bits(w1.cpu()), W.bf16_bits(w2.cpu()))
+            return cache["all"], np.arange(wl.E, dtype=np.int32), wl.E
+        used = np.unique(idsn[sl][idsn[sl] >= 0])
+        key = tuple(used.tolist())
+        if key not in cache:
+            cache.clear()
+            idx = torch.as_tensor(used, dtype=torch.long, device=w1.device)
+            cache[key] = O.Weights(W.bf16_bits(w1.index_select(0, idx).cpu()),
+                                   W.bf16_bits(w2.index_select(0, idx).cpu()))
+        remap = np.full(wl.E, -1, np.int32)
+        remap[used] = np.arange(used.size, dtype=np.int32)
+        return cache[key], remap, used.size
+
+    return run, O.num_threads()
+
+
+def cpu_baseline(wl, x, w1, w2, ids, wts, seconds):
+    run, cores = oracle_sample_runner(wl, x, w1, w2, ids, wts)
+    # the sample: a prefix of the batch's tokens, all their routes; grown until
+    # it holds about `seconds` of oracle work
+    n = 1
+    t1 = run(0, 1)
+    n = int(max(1, min(wl.T, seconds / max(t1, 1e-6))))
+    t = run(0, n) if n > 1 else t1
+    return {"value": n / t, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {n} of {wl.T} tokens of {wl.name} (all their routes; only the "
+                      f"experts they use), quantize + W4A4 forward, {t:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    wl = W.ALL[args.workload]
+    if args.T:
+        wl = wl.with_T(args.T)
+    if rank != 0:
+        return
+    x, w1, w2, ids, wts = make_inputs(wl, "cpu")
+    run, cores = oracle_sample_runner(wl, x, w1, w2, ids, wts)
+    t1 = run(0, 1)
+    budget = 150.0  # seconds for warmup + timed steps
+    n = 1
+    per_step = t1
+    steps = args.steps
+    # each step is a bounded sample: one token (all its routes) at a time, cycling
+    times = []
+    for i in range(args.warmup):
+        run(i % wl.T, 1)
+    for i in range(steps):
+        times.append(run(i % wl.T, n))
+        if sum(times) > budget:
+            break
+    mean = sum(times) / len(times)
+    value = n / mean
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": len(times), "warmup": args.warmup,
+            "ms_per_step": mean * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
+                       "K": wl.K, "act": wl.act},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{n} token per step (all its routes), cycling over the "
+                                       f"{wl.T} tokens; {len(times)} steps run of {steps} asked "
+                                       f"(150 s budget)"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_ours(args, rank, world, local_rank):
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = W.ALL[args.workload]
+    if args.T:
+        wl = wl.with_T(args.T)
+    x, w1, w2, ids, wts = make_inputs(wl, dev)
+    x_d, ids_d, wts_d = x.to(dev), ids.to(dev), wts.to(dev)
+    w = M.prepare_weights(w1.to(dev), w2.to(dev), wl.act)
+    T, H, K = wl.T, wl.H, wl.K
+    codes = torch.empty(T, H // 2, dtype=torch.uint8, device=dev)
+    sf = torch.empty(T, H // 16, dtype=torch.uint8, device=dev)
+    scale = torch.empty(T, dtype=torch.float32, device=dev)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    ws = M.workspace(w, T, K, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    # stage markers: [0] forward start, [1] after routing, [2] after FC1, ...
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    with torch.cuda.stream(stream):
+        for e in marks:
+            e.record()
+    torch.cuda.synchronize()
+    M.moe_nvfp4_profile_events(marks)
+
+    def step():
+        M.moe_nvfp4_quantize_tokens(x_d, codes, sf, scale, stream)
+        M.moe_nvfp4_forward(w.dims, w, codes, sf, scale, ids_d, wts_d, out, ws, stream)
+
+    with torch.cuda.stream(stream):
+        step()  # first call runs the device check outside capture
+    torch.cuda.synchronize()
+    assert M.moe_nvfp4_read_status(ws, stream) == 0
+
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        torch.cuda.synchronize()
+
+    def run_step():
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            flush.zero_()
+            run_step()
+    torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    fc1_ms = []
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    t_wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            run_step()
+            ends[i].record(stream)
+            ends[i].synchronize()
+            fc1_ms.append(marks[1].elapsed_time(marks[2]))
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    M.moe_nvfp4_profile_events([])
+
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    value = world * T * args.steps / (total_ms / 1e3)
+
+    # ---- end to end through the public API with host buffers
+    x_h = x.cpu().pin_memory()
+    ids_h = ids.cpu().pin_memory()
+    wts_h = wts.cpu().pin_memory()
+    out_h = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+    x_e = torch.empty_like(x_d)
+    ids_e = torch.empty_like(ids_d)
+    wts_e = torch.empty_like(wts_d)
+    e2e_steps = min(args.steps, 500)
+
+    def e2e_step():
+        x_e.copy_(x_h, non_blocking=True)
+        ids_e.copy_(ids_h, non_blocking=True)
+        wts_e.copy_(wts_h, non_blocking=True)
+        M.moe_nvfp4_quantize_tokens(x_e, codes, sf, scale, stream)
+        M.moe_nvfp4_forward(w.dims, w, codes, sf, scale, ids_e, wts_e, out, ws, stream)
+        out_h.copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+    torch.cuda.synchronize()
+    e_s = torch.cuda.Event(enable_timing=True)
+    e_e = torch.cuda.Event(enable_timing=True)
+    e2e_ms = 0.0
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            flush.zero_()
+            e_s.record(stream)
+            e2e_step()
+            e_e.record(stream)
+            e_e.synchronize()
+            e2e_ms += e_s.elapsed_time(e_e)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_value = world * T * e2e_steps / (e2e_ms / 1e3)
+    h2d = x_h.numel() * 2 + ids_h.numel() * 4 + wts_h.numel() * 4
+    d2h = out_h.numel() * 2
+
+    if rank != 0:
+        return
+    fc1_bytes, U, R = algorithmic_fc1_bytes(wl, ids)
+    fc1_mean = statistics.fmean(fc1_ms)
+    hbm, src = peaks()
+    achieved = fc1_bytes / (fc1_mean * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "us_per_layer": ms_per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "nvfp4", "data": "synthetic (seeded N(0,1)-family inputs)",
+        "config": {"workload": wl.name, "T": T, "H": H, "I": wl.I, "E": wl.E, "K": K,
+                   "act": wl.act, "routes": R, "experts_touched": U,
+                   "l2": "flushed (256 MB write) between timed steps",
+                   "graph": graph is not None, "parallelism": f"replicas x{world}"},
+        "roofline": {"kernel": "fc1 grouped GEMM (gemm_w4a4_kernel<SwiGLU|ReLU2>)",
+                     "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "peak_source": src,
+                     "traffic": traffic_for(wl.name), "algorithmic_bytes": fc1_bytes,
+                     "kernel_us": fc1_mean * 1e3},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "clocks": clocks,
+        "wall_s": t_wall,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, x, w1, w2, ids, wts, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        torch.distributed.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo")
+    run_ours(args, rank, world, local_rank)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -158,7 +158,14 @@ cudaEvent_t g_prof[kMaxProfileEvents];
 int g_nprof = 0;
 
 void mark(int i, cudaStream_t s) {
-  if (i < g_nprof && g_prof[i]) cudaEventRecord(g_prof[i], s);
+  if (i >= g_nprof || !g_prof[i]) return;
+  // inside stream capture the record must become an event-record node of the graph
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(s, &cs);
+  if (cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(g_prof[i], s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(g_prof[i], s);
 }
 
 template <typename T>
