@@ -186,6 +186,32 @@ moe_status moe_nvfp4_forward_w4a16(const moe_dims* d, const moe_nvfp4_weights* w
  * helper; not capturable. */
 moe_status moe_nvfp4_read_status(const void* ws, moe_stream_t stream);
 
+/* Allocation-free W4A4 forward.  (The source pages have no counterpart: this
+ * entry point exists for callers of this library.)  It is moe_nvfp4_forward
+ * with the workspace taken from a scratch array that the library keeps in
+ * device memory, so the caller passes only its inputs and outputs.  It is for
+ * callers that may not allocate device memory themselves -- a plugin inside a
+ * framework that owns all allocations, code running under a locked or budgeted
+ * allocator, an embedded runtime with memory fixed at start-up.
+ *   - The scratch is one array of 64 MiB per device, reserved on every device
+ *     that loads the library and held until the process exits.  A (d, T, K)
+ *     whose workspace (moe_nvfp4_workspace_bytes(d, T, K, 0)) exceeds 64 MiB
+ *     is rejected with MOE_ERR_WORKSPACE_TOO_SMALL before anything runs.
+ *   - The first call on each device looks up the array's device address (with
+ *     that device current); make that first call outside any stream capture.
+ *   - Nothing is allocated or freed, by the library or any routine it calls.
+ *   - All calls on a device share the one array.  The forward clears the
+ *     status words it needs zeroed; the rest is written before it is read, so
+ *     the previous call's leftovers do no harm.  Calls whose execution overlaps
+ *     on the GPU (different streams, no ordering between them) race on the
+ *     array and give wrong results: order them on one stream or with events.
+ *   - Device-reported status (bad ids) is not readable for this variant.
+ * Arguments and outputs as moe_nvfp4_forward, without ws / ws_bytes. */
+moe_status moe_nvfp4_forward_noalloc(const moe_dims* d, const moe_nvfp4_weights* w, int32_t T,
+                                     int32_t K, const uint8_t* codes, const uint8_t* sf,
+                                     const float* scale, const int32_t* topk_ids,
+                                     const float* topk_w, void* out_bf16, moe_stream_t stream);
+
 /* Profiling hook: register `n` cudaEvent_t handles (host pointer to an array of
  * event handles; n == 0 or events == NULL unregisters).  While registered,
  * every forward records events[0] before its first stage and events[i] after

@@ -78,10 +78,13 @@ def lib():
         L.moe_nvfp4_forward_w4a16.argtypes = [C.POINTER(moe_dims), C.POINTER(moe_nvfp4_weights),
                                               i32, i32, vp, vp, vp, vp, vp, sz, vp]
         L.moe_nvfp4_read_status.argtypes = [vp, vp]
+        L.moe_nvfp4_forward_noalloc.argtypes = [C.POINTER(moe_dims), C.POINTER(moe_nvfp4_weights),
+                                                i32, i32, vp, vp, vp, vp, vp, vp, vp]
         L.moe_nvfp4_profile_events.argtypes = [C.POINTER(C.c_void_p), i32]
         for f in ["moe_nvfp4_weight_sizes", "moe_nvfp4_prepare_weights",
                   "moe_nvfp4_quantize_tokens", "moe_nvfp4_workspace_layout", "moe_nvfp4_forward",
-                  "moe_nvfp4_forward_w4a16", "moe_nvfp4_read_status", "moe_nvfp4_profile_events"]:
+                  "moe_nvfp4_forward_w4a16", "moe_nvfp4_read_status", "moe_nvfp4_profile_events",
+                  "moe_nvfp4_forward_noalloc"]:
             getattr(L, f).restype = C.c_int
         _lib = L
     return _lib
@@ -171,6 +174,17 @@ def moe_nvfp4_forward_w4a16(d, w, x_bf16, topk_ids, topk_w, out, ws, stream=None
                                          _ptr(topk_ids), _ptr(topk_w), _ptr(out), _ptr(ws),
                                          ws.numel() * ws.element_size(), _stream(stream)),
            "moe_nvfp4_forward_w4a16")
+
+
+def moe_nvfp4_forward_noalloc(d, w, codes, sf, scale, topk_ids, topk_w, out, stream=None):
+    """The W4A4 forward on the library's own 64 MiB device scratch array, for
+    callers that cannot allocate device memory (see include/moe_nvfp4.h)."""
+    _need_cuda(codes, sf, scale, topk_ids, topk_w, out)
+    T, K = topk_ids.shape
+    _check(lib().moe_nvfp4_forward_noalloc(C.byref(d), C.byref(w.c), T, K, _ptr(codes), _ptr(sf),
+                                           _ptr(scale), _ptr(topk_ids), _ptr(topk_w), _ptr(out),
+                                           _stream(stream)),
+           "moe_nvfp4_forward_noalloc")
 
 
 def moe_nvfp4_read_status(ws, stream=None):
