@@ -32,7 +32,7 @@ import nvfp4_token_routed_gb300 as M  # noqa: E402
 from nvfp4_token_routed_gb300 import workloads as W  # noqa: E402
 
 METRIC = "MoE-layer tokens/s and µs/layer at 1 GB300"
-KERNELS_PER_STEP = 8  # quantize, route count/scan/scatter, FC1, requant, FC2, finalize
+KERNELS_PER_STEP = 9  # quantize, route count/scan/scatter/gather, FC1, requant, FC2, finalize
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -44,6 +44,7 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=W.SWIGLU_E64.name, choices=list(W.ALL))
     p.add_argument("--T", type=int, default=0, help="override the workload's token count")
+    p.add_argument("--E", type=int, default=0, help="override the expert count (profiling cases)")
     p.add_argument("--no-graph", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -247,6 +248,8 @@ def run_ours(args, rank, world, local_rank):
     wl = W.ALL[args.workload]
     if args.T:
         wl = wl.with_T(args.T)
+    if args.E:
+        wl = wl.with_E(args.E)
     x, w1, w2, ids, wts = make_inputs(wl, dev)
     x_d, ids_d, wts_d = x.to(dev), ids.to(dev), wts.to(dev)
     w = M.prepare_weights(w1.to(dev), w2.to(dev), wl.act)
@@ -259,14 +262,6 @@ def run_ours(args, rank, world, local_rank):
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
-    # stage markers: [0] forward start, [1] after routing, [2] after FC1, ...
-    marks = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-    with torch.cuda.stream(stream):
-        for e in marks:
-            e.record()
-    torch.cuda.synchronize()
-    M.moe_nvfp4_profile_events(marks)
-
     def step():
         M.moe_nvfp4_quantize_tokens(x_d, codes, sf, scale, stream)
         M.moe_nvfp4_forward(w.dims, w, codes, sf, scale, ids_d, wts_d, out, ws, stream)
@@ -276,28 +271,32 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     assert M.moe_nvfp4_read_status(ws, stream) == 0
 
-    graph = None
-    if not args.no_graph:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
+    def capture():
+        if args.no_graph:
+            return None
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
             step()
         torch.cuda.synchronize()
+        return g
 
-    def run_step():
-        if graph is not None:
-            graph.replay()
+    graph = capture()
+
+    def run_step(g):
+        if g is not None:
+            g.replay()
         else:
             step()
 
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
             flush.zero_()
-            run_step()
+            run_step(graph)
     torch.cuda.synchronize()
 
+    # ---- the timed region: K steps, each bracketed by events on the launching stream
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    fc1_ms = []
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if world > 1:
         torch.distributed.barrier()
@@ -310,15 +309,36 @@ def run_ours(args, rank, world, local_rank):
         for i in range(args.steps):
             flush.zero_()
             starts[i].record(stream)
-            run_step()
+            run_step(graph)
             ends[i].record(stream)
-            ends[i].synchronize()
-            fc1_ms.append(marks[1].elapsed_time(marks[2]))
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop() if sampler else None
+
+    # ---- per-kernel times: the same K steps again with stage markers recorded by
+    # the library between its kernels ([1] after routing, [2] after FC1, ...).
+    # Markers stop kernels from overlapping their launch with the previous
+    # kernel, so they get a pass of their own.
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    with torch.cuda.stream(stream):
+        for e in marks:
+            e.record()
+    torch.cuda.synchronize()
+    M.moe_nvfp4_profile_events(marks)
+    graph_marked = capture()
+    M.moe_nvfp4_profile_events([])
+    M.moe_nvfp4_profile_events(marks)
+    fc1_ms, fc2_ms = [], []
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.zero_()
+            run_step(graph_marked)
+            marks[5].synchronize()
+            fc1_ms.append(marks[1].elapsed_time(marks[2]))
+            fc2_ms.append(marks[3].elapsed_time(marks[4]))
+    torch.cuda.synchronize()
     M.moe_nvfp4_profile_events([])
 
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
@@ -390,7 +410,9 @@ def run_ours(args, rank, world, local_rank):
                      "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "peak_source": src,
                      "traffic": traffic_for(wl.name), "algorithmic_bytes": fc1_bytes,
-                     "kernel_us": fc1_mean * 1e3},
+                     "kernel_us": fc1_mean * 1e3, "fc2_kernel_us": statistics.fmean(fc2_ms) * 1e3,
+                     "timing": "CUDA events recorded by the library around the FC1 launch, "
+                               "over a second pass of the same K steps"},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": KERNELS_PER_STEP * args.steps,

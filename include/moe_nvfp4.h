@@ -66,10 +66,10 @@ typedef struct {
  * kept separate, never folded into scales).  All device pointers, 16-byte
  * aligned (alphas 4-byte).  Stored layouts:
  *   fc1_codes [E][N1][H/2]  K-contiguous rows.  For SwiGLU the stored row order
- *                           interleaves 128-row blocks: stored rows
- *                           [256f, 256f+128) are gate rows [128f, 128f+128) and
- *                           stored rows [256f+128, 256f+256) are up rows
- *                           I+[128f, 128f+128).  Squared ReLU keeps row order.
+ *                           interleaves 64-row blocks: stored rows
+ *                           [128f, 128f+64) are gate rows [64f, 64f+64) and
+ *                           stored rows [128f+64, 128f+128) are up rows
+ *                           I+[64f, 64f+64).  Squared ReLU keeps row order.
  *   fc1_sf    [E][N1*H/16]  swizzled: byte of (stored row r, scale column j) is
  *                           ((r/128)*(H/64) + j/4)*512 + (r%32)*16 + ((r/32)%4)*4 + j%4
  *   fc1_alpha [E]           1 / w_scale, w_scale = 2688 / amax(expert FC1)
@@ -88,13 +88,17 @@ typedef struct {
  * workspace base; a region that the variant does not use has size 0. */
 typedef struct {
   size_t total;
-  int64_t rows_cap;      /* padded permuted rows reserved (multiple of 128) */
-  size_t status;         /* int32[16]: [0] error bits, [1] token tiles, [2] padded rows */
+  int64_t rows_cap;      /* padded permuted rows reserved (multiple of 128);
+                            each expert's group starts at a multiple of 128 */
+  size_t status;         /* int32[16]: [0] error bits, [1] token tiles, [2] padded rows,
+                            [3] rows of the largest token tile */
   size_t counts;         /* int32[E] routes per expert                     */
   size_t group_row0;     /* int32[E] first permuted row of each expert     */
-  size_t tile_expert;    /* int32[rows_cap/128]                            */
-  size_t tile_rows;      /* int32[rows_cap/128] valid rows of each tile    */
-  size_t chunk_counts;   /* int32[ceil(T*K/256)][E]                        */
+  size_t tiles;          /* int32[rows_cap/128][4] per token tile: expert, the
+                            expert's first tile, its tile count, its routes */
+  size_t chunk_counts;   /* int32[ceil(T*K/256)][E+1]: routes per expert in
+                            each 256-route chunk, then 1 if the chunk held an
+                            id outside [-1, E)                              */
   size_t chunk_prefix;   /* int32[ceil(T*K/256)][E]                        */
   size_t inv;            /* int32[T*K] permuted row of route t*K+k, or -1   */
   size_t perm;           /* int32[rows_cap] route id t*K+k of a valid row   */
@@ -182,7 +186,7 @@ moe_status moe_nvfp4_forward_w4a16(const moe_dims* d, const moe_nvfp4_weights* w
 
 /* Device-reported status of the last forward that used `ws`: synchronises
  * `stream`, then returns MOE_ERR_BAD_EXPERT_ID, MOE_ERR_DEVICE_TIMEOUT or
- * MOE_OK.  The flags are cleared at the start of every forward.  Debug/test
+ * MOE_OK.  The flags are rewritten by every forward.  Debug/test
  * helper; not capturable. */
 moe_status moe_nvfp4_read_status(const void* ws, moe_stream_t stream);
 

@@ -41,8 +41,8 @@ class moe_nvfp4_weights(C.Structure):
                 ("fc2_codes", C.c_void_p), ("fc2_sf", C.c_void_p), ("fc2_alpha", C.c_void_p)]
 
 
-_LAYOUT_FIELDS = ["total", "rows_cap", "status", "counts", "group_row0", "tile_expert",
-                  "tile_rows", "chunk_counts", "chunk_prefix", "inv", "perm", "xq_codes", "xq_sf",
+_LAYOUT_FIELDS = ["total", "rows_cap", "status", "counts", "group_row0", "tiles",
+                  "chunk_counts", "chunk_prefix", "inv", "perm", "xq_codes", "xq_sf",
                   "xq_scale", "act", "fc2q_codes", "fc2q_sf", "fc2q_scale", "x_perm", "act_bf16",
                   "route"]
 

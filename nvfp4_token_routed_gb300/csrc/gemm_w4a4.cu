@@ -8,15 +8,27 @@
 // FC1 epilogue writes the fp32 activated row and a row-parallel pass quantizes it.
 //
 // Structure (swap-AB: weights are the M=128 operand, tokens the N operand, so a
-// decode-sized group of 1..128 tokens does not waste a 128-row MMA):
-//   * persistent CTAs, one per SM; work item = (token tile, 256-row weight tile)
-//   * warp 0: TMA producer -- weight tile halves (2 x 128 rows x 128 B, 128-byte
-//     swizzle), token tile (16-row boxes), scale atoms via bulk copies
+// decode-sized group of a few tokens does not waste a 128-row MMA):
+//   * persistent CTAs, one per SM; work item = (token tile of <= 128 rows of one
+//     expert, 128-row weight tile of that expert), items strided over CTAs
+//   * warp 0: TMA producer -- weight tile (128 rows x 128 B, 128-byte swizzle),
+//     token tile (16-row boxes), block-scale atoms via bulk copies
+//   * warps 6-9: scale staging -- move each stage's E4M3 scale atoms from shared
+//     memory into that stage's TMEM scale slot with tcgen05.st, in the layout the
+//     block-scaled MMA reads (row r of a 128-row atom at lane r%32, column r/32,
+//     replicated in all four lane quadrants)
 //   * warp 1: TMEM allocator and single-thread MMA issuer:
-//     tcgen05.cp of the scale atoms into TMEM, then
-//     tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X (K = 64 per instruction)
+//     tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X, K = 64 per
+//     instruction, N = the tile's token count rounded up to 16
 //   * warps 2-5: epilogue, one TMEM lane (= one weight row) per thread
-//   * 4-stage shared-memory ring guarded by mbarriers; every wait is bounded.
+//   * the shared-memory stage ring is sized at run time from the largest token
+//     tile of the launch (5 stages at 128 tokens, 9 at 16); the two accumulator
+//     buffers let the epilogue of one tile overlap the MMAs of the next.
+//   * every mbarrier wait is bounded; on timeout the CTA records an error flag,
+//     drains its own copies and MMAs, frees TMEM and returns.
+// SwiGLU: the stored FC1 rows interleave 64-row blocks [gate | up], so TMEM
+// lanes 0-63 hold gate rows and 64-127 the matching up rows; the up warps pass
+// their values to the gate warps through shared memory.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -29,33 +41,50 @@
 namespace moe {
 
 namespace w4a4 {
-constexpr int kStages = 4;
-constexpr int kBK = 256;                        // K elements per stage
-constexpr int kRowBytes = kBK / 2;              // packed FP4 bytes per row per stage
-constexpr int kAHalfBytes = 128 * kRowBytes;    // 16 KB
-constexpr int kABytes = 2 * kAHalfBytes;        // 32 KB
-constexpr int kBBytes = kTileRows * kRowBytes;  // 16 KB
-constexpr int kAtom = 512;                      // 128 rows x 4 scale columns
-constexpr int kSfaBytes = 2 * 4 * kAtom;        // two row halves x 4 K-atoms
-constexpr int kSfbBytes = 4 * kAtom;
-constexpr int kOffB = kABytes;
-constexpr int kOffSfa = kOffB + kBBytes;
-constexpr int kOffSfb = kOffSfa + kSfaBytes;
-constexpr int kStageBytes = kOffSfb + kSfbBytes;  // 55296, a multiple of 1024
-constexpr int kBarOff = kStages * kStageBytes;
-constexpr int kSmemBytes = kBarOff + 256 + 1024;  // + barriers + alignment slack
+constexpr int kBK = 256;                    // K elements per stage
+constexpr int kRowBytes = kBK / 2;          // packed FP4 bytes per row per stage
+constexpr int kABytes = 128 * kRowBytes;    // 16 KB weight tile per stage
+constexpr int kAtom = 512;                  // 128 rows x 4 scale columns
+constexpr int kSfaBytes = 4 * kAtom;        // 4 K-atoms of the 128-row weight tile
+constexpr int kMaxStages = 12;
 constexpr int kTmemCols = 512;
-constexpr int kAccCols = 256;            // two 128-column accumulators (row halves)
-constexpr int kSfColsPerStage = 48;      // SFA 2 x 4 atoms x 4 cols + SFB 4 atoms x 4 cols
-constexpr int kThreads = 192;
-static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
-static_assert(kAccCols + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
+constexpr int kXchgFloats = 2 * 64 * 33;    // SwiGLU exchange: 2 buffers x 64 rows x 32 (+1 pad)
+constexpr int kXchgBytes = (kXchgFloats * 4 + 1023) / 1024 * 1024;
+constexpr int kBarBytes = 2048;             // barriers + flags, then 256 staged row scales
+constexpr int kSmemBytes = 227 * 1024;      // dynamic shared memory of every launch
+constexpr int kStageBudget = kSmemBytes - 1024 - kBarBytes - kXchgBytes;
+constexpr int kThreads = 320;               // 10 warps
+// barrier indices
+constexpr int kBarFull = 0;
+constexpr int kBarEmpty = kMaxStages;
+constexpr int kBarSfReady = 2 * kMaxStages;
+constexpr int kBarAccFull = 3 * kMaxStages;       // 2 of them
+constexpr int kBarAccEmpty = 3 * kMaxStages + 2;  // 2 of them
+constexpr int kBarDrain = 3 * kMaxStages + 4;
+constexpr int kNumBars = kBarDrain + 1;
+static_assert(8 * kNumBars + 16 <= 1024, "barrier area");
 }  // namespace w4a4
 
-struct Smem {
-  uint8_t* base;
-  __device__ uint32_t bar(int i) const { return smem_u32(base + w4a4::kBarOff + 8 * i); }
+struct Ring {
+  uint8_t* base;  // 1024-aligned
+  __device__ uint32_t bar(int i) const { return smem_u32(base + 8 * i); }
 };
+
+// A work item: token tile tt (rows valid rows of expert e) x weight tile mt.
+// Items are numbered expert by expert, and within an expert weight-tile-major,
+// so the token tiles that share a weight tile run on neighbouring CTAs at the
+// same time and the weight tile comes from HBM once (then L2).  Loaded one item
+// ahead of use.
+struct TileInfo {
+  int e, tt, mt, rows;
+};
+__device__ __forceinline__ TileInfo tile_info(const GemmArgs& a, int item, int n_items) {
+  if (item >= n_items) return TileInfo{0, 0, 0, 0};
+  const int4 t = a.tiles[item / a.m_tiles];  // {expert, first tile, tiles, routes}
+  const int local = item - a.m_tiles * t.y;
+  const int j = local % t.z;
+  return TileInfo{t.x, t.y + j, local / t.z, min(kTileRows, t.w - kTileRows * j)};
+}
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                               int32_t* status) {
@@ -72,6 +101,10 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
   }
 }
 
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(w4a4::kThreads, 1)
     gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -80,27 +113,29 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const Smem S{smem};
-  // barrier indices: full[s] = s, empty[s] = kStages + s, acc_full, acc_empty, drain
-  const int kFull = 0, kEmpty = kStages, kAccFull = 2 * kStages, kAccEmpty = 2 * kStages + 1,
-            kDrain = 2 * kStages + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 8 * (2 * kStages + 3));
+  const Ring R{smem};
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 8 * kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  const int n_tiles = a.status[kStatusTiles];
-  const int n_items = n_tiles * a.m_tiles;
-  if ((int)blockIdx.x >= n_items) return;
+  volatile int* epi_stop = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  float* s_scale = reinterpret_cast<float*>(smem + 1024);  // row scales of the current tile (128)
+  float* xchg = reinterpret_cast<float*>(smem + kBarBytes);
+  uint8_t* stages = smem + kBarBytes + kXchgBytes;  // 1024-aligned
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // prologue that reads nothing the previous kernel writes: barriers, TMEM
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(S.bar(kFull + s), 1);
-      mbar_init(S.bar(kEmpty + s), 1);
+    for (int s = 0; s < kMaxStages; ++s) {
+      mbar_init(R.bar(kBarFull + s), 1);
+      mbar_init(R.bar(kBarEmpty + s), 1);
+      mbar_init(R.bar(kBarSfReady + s), 4);
     }
-    mbar_init(S.bar(kAccFull), 1);
-    mbar_init(S.bar(kAccEmpty), 128);
-    mbar_init(S.bar(kDrain), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(R.bar(kBarAccFull + b), 1);
+      mbar_init(R.bar(kBarAccEmpty + b), 128);
+    }
+    mbar_init(R.bar(kBarDrain), 1);
     *abort_flag = 0;
+    *epi_stop = 0;
     fence_barrier_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
@@ -113,169 +148,244 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();
+  pdl_trigger();
+
+  const int n_tiles = a.status[kStatusTiles];
+  const int n_items = n_tiles * a.m_tiles;
+
+  // ---- geometry from the largest token tile (<= 128 rows) of this launch
+  const int max_n16 = (a.status[kStatusMaxRows] + 15) & ~15;
+  const int b_bytes = max_n16 * kRowBytes;                // multiple of 2048
+  const int stage_bytes = kABytes + kSfaBytes + b_bytes + 4 * kAtom;  // multiple of 1024
+  const int off_sfa = kABytes, off_b = kABytes + kSfaBytes, off_sfb = off_b + b_bytes;
+  const int acc_stride = (max_n16 + 31) & ~31;            // TMEM columns per accumulator
+  const int slot_cols = 32;                               // scale columns per stage (A 16, B 16)
+  const int sf_base = 2 * acc_stride;                     // two accumulator buffers
+  int n_stages = kStageBudget / stage_bytes;
+  if (n_stages > kMaxStages) n_stages = kMaxStages;
+  while (n_stages > 2 && sf_base + n_stages * slot_cols > kTmemCols) --n_stages;
 
   const int kblocks = a.K / kBK;
-  const int atoms = a.K / 64;            // scale atoms per 128-row block
+  const int atoms = a.K / 64;                          // scale atoms per 128-row block
   const size_t plane = (size_t)a.w_rows * (a.K / 16);  // weight scale bytes per expert
 
-  if (warp == 0) {
+  if ((int)blockIdx.x >= n_items) {
+    // no work for this CTA: fall through to the teardown
+  } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int last_par[kStages];
+      int last_par[kMaxStages];
 #pragma unroll
-      for (int s = 0; s < kStages; ++s) last_par[s] = -1;
+      for (int s = 0; s < kMaxStages; ++s) last_par[s] = -1;
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
-      uint32_t stage = 0, phase = 0;
+      int stage = 0;
+      uint32_t phase = 0;
       bool ok = true;
+      TileInfo cur = tile_info(a, blockIdx.x, n_items);
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const int tt = item / a.m_tiles, mt = item % a.m_tiles;
-        const int e = a.tile_expert[tt];
-        const int rows = a.tile_rows[tt];
-        const int n16 = (rows + 15) & ~15;
-        const int a_row = e * a.w_rows + mt * 256;
-        const int b_row = tt * kTileRows;
-        const uint8_t* sfa0 = a.sfa + (size_t)e * plane + (size_t)(2 * mt) * atoms * kAtom;
-        const uint8_t* sfb0 = a.sfb + (size_t)tt * atoms * kAtom;
-        const uint32_t tx = kABytes + kSfaBytes + kSfbBytes + n16 * kRowBytes;
+        const TileInfo nxt = tile_info(a, item + gridDim.x, n_items);
+        const int n16 = (cur.rows + 15) & ~15;
+        const int a_row = cur.e * a.w_rows + cur.mt * 128;
+        const int b_row = cur.tt * kTileRows;
+        const uint8_t* sfa0 = a.sfa + (size_t)cur.e * plane + (size_t)cur.mt * atoms * kAtom;
+        const uint8_t* sfb0 = a.sfb + (size_t)cur.tt * atoms * kAtom;
+        const uint32_t tx = kABytes + kSfaBytes + n16 * kRowBytes + 4 * kAtom;
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!wait_or_abort(S.bar(kEmpty + stage), phase ^ 1, abort_flag, a.status)) {
+          if (!wait_or_abort(R.bar(kBarEmpty + stage), phase ^ 1, abort_flag, a.status)) {
             ok = false;
             break;
           }
-          uint8_t* sb = smem + stage * kStageBytes;
-          const uint32_t full = S.bar(kFull + stage);
+          uint8_t* sb = stages + stage * stage_bytes;
+          const uint32_t full = R.bar(kBarFull + stage);
           mbar_expect_tx(full, tx);
           tma_load_2d_hint(smem_u32(sb), &tmA, full, kb * kRowBytes, a_row, pol_w);
-          tma_load_2d_hint(smem_u32(sb + kAHalfBytes), &tmA, full, kb * kRowBytes, a_row + 128,
-                           pol_w);
           for (int c = 0; c < n16 / 16; ++c)
-            tma_load_2d_hint(smem_u32(sb + kOffB + c * 16 * kRowBytes), &tmB, full, kb * kRowBytes,
-                             b_row + 16 * c, pol_x);
-          bulk_load(smem_u32(sb + kOffSfa), sfa0 + (size_t)(kb * 4) * kAtom, 4 * kAtom, full);
-          bulk_load(smem_u32(sb + kOffSfa + 4 * kAtom), sfa0 + (size_t)(atoms + kb * 4) * kAtom,
-                    4 * kAtom, full);
-          bulk_load(smem_u32(sb + kOffSfb), sfb0 + (size_t)(kb * 4) * kAtom, 4 * kAtom, full);
+            tma_load_2d_hint(smem_u32(sb + off_b + c * 16 * kRowBytes), &tmB, full,
+                             kb * kRowBytes, b_row + 16 * c, pol_x);
+          bulk_load(smem_u32(sb + off_sfa), sfa0 + (size_t)(kb * 4) * kAtom, 4 * kAtom, full);
+          bulk_load(smem_u32(sb + off_sfb), sfb0 + (size_t)(kb * 4) * kAtom, 4 * kAtom, full);
           last_par[stage] = (int)phase;
-          if (++stage == kStages) {
+          if (++stage == n_stages) {
             stage = 0;
             phase ^= 1;
           }
         }
+        cur = nxt;
       }
-      if (!ok) {
+      if (!ok || *abort_flag) {
         // let every copy still in flight land before the CTA's shared memory goes away
-        for (int s = 0; s < kStages; ++s)
-          if (last_par[s] >= 0) mbar_wait(S.bar(kFull + s), (uint32_t)last_par[s]);
+        for (int s = 0; s < kMaxStages; ++s)
+          if (last_par[s] >= 0) mbar_wait(R.bar(kBarFull + s), (uint32_t)last_par[s]);
       }
+    }
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ scale staging
+    // Atom bytes [16l, 16l+16) hold rows l, l+32, l+64, l+96 (4 scales each);
+    // lane l of every quadrant gets them in 4 consecutive columns.
+    const uint32_t lane_q = (uint32_t)((warp & 3) * 32) << 16;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+      bool ok = true;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!wait_or_abort(R.bar(kBarFull + stage), phase, abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sb = smem_u32(stages + stage * stage_bytes);
+        const uint32_t col0 = tmem + lane_q + sf_base + stage * slot_cols;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          tmem_st4(col0 + 4 * ks, lds128(sb + off_sfa + ks * kAtom + lane * 16));
+          tmem_st4(col0 + 16 + 4 * ks, lds128(sb + off_sfb + ks * kAtom + lane * 16));
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(R.bar(kBarSfReady + stage));
+        if (++stage == n_stages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      uint32_t stage = 0, phase = 0, acc_phase = 0;
+      int stage = 0, local = 0;
+      uint32_t phase = 0;
       bool ok = true, issued = false;
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const int tt = item / a.m_tiles;
-        const int rows = a.tile_rows[tt];
-        const int n16 = (rows + 15) & ~15;
+      TileInfo cur = tile_info(a, blockIdx.x, n_items);
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++local) {
+        const TileInfo nxt = tile_info(a, item + gridDim.x, n_items);
+        const int n16 = (cur.rows + 15) & ~15;
         const uint32_t idesc = idesc_mxf4nvf4(128, n16);
-        if (!wait_or_abort(S.bar(kAccEmpty), acc_phase ^ 1, abort_flag, a.status)) {
+        const int buf = local & 1;
+        const uint32_t acc_par = ((uint32_t)(local >> 1) & 1u) ^ 1u;
+        if (!wait_or_abort(R.bar(kBarAccEmpty + buf), acc_par, abort_flag, a.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const uint32_t acc = tmem + buf * acc_stride;
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!wait_or_abort(S.bar(kFull + stage), phase, abort_flag, a.status)) {
+          // scales staged (which implies the stage's copies landed); the full
+          // barrier is re-checked so this thread observes the TMA writes itself
+          if (!wait_or_abort(R.bar(kBarSfReady + stage), phase, abort_flag, a.status) ||
+              !wait_or_abort(R.bar(kBarFull + stage), phase, abort_flag, a.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint8_t* sb = smem + stage * kStageBytes;
-          const uint32_t sf_col = tmem + kAccCols + stage * kSfColsPerStage;
-#pragma unroll
-          for (int i = 0; i < 8; ++i)  // SFA: half i/4, K-atom i%4 -> columns 4*i
-            tc_cp_sf_atom(sf_col + 4 * i, smem_desc(smem_u32(sb + kOffSfa + i * kAtom), 0, 128, 0));
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            tc_cp_sf_atom(sf_col + 32 + 4 * i,
-                          smem_desc(smem_u32(sb + kOffSfb + i * kAtom), 0, 128, 0));
+          const uint8_t* sb = stages + stage * stage_bytes;
+          const uint32_t col0 = tmem + sf_base + stage * slot_cols;
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bdesc = smem_desc(smem_u32(sb + kOffB + ks * 32), 16, 1024, 2);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const uint64_t adesc =
-                  smem_desc(smem_u32(sb + h * kAHalfBytes + ks * 32), 16, 1024, 2);
-              mma_mxf4nvf4(tmem + h * 128, adesc, bdesc, idesc, sf_col + 16 * h + 4 * ks,
-                           sf_col + 32 + 4 * ks, (kb | ks) != 0 ? 1u : 0u);
-            }
+            const uint64_t adesc = smem_desc(smem_u32(sb + ks * 32), 16, 1024, 2);
+            const uint64_t bdesc = smem_desc(smem_u32(sb + off_b + ks * 32), 16, 1024, 2);
+            mma_mxf4nvf4(acc, adesc, bdesc, idesc, col0 + 4 * ks, col0 + 16 + 4 * ks,
+                         (kb | ks) != 0 ? 1u : 0u);
           }
           issued = true;
-          tc_commit(S.bar(kEmpty + stage));
-          if (++stage == kStages) {
+          tc_commit(R.bar(kBarEmpty + stage));
+          if (++stage == n_stages) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        tc_commit(S.bar(kAccFull));
-        acc_phase ^= 1;
+        tc_commit(R.bar(kBarAccFull + buf));
+        cur = nxt;
       }
-      if (!ok && issued) {
+      if ((!ok || *abort_flag) && issued) {
         // drain the tensor-core work issued so far before TMEM is released
-        tc_commit(S.bar(kDrain));
-        mbar_wait(S.bar(kDrain), 0);
+        tc_commit(R.bar(kBarDrain));
+        mbar_wait(R.bar(kBarDrain), 0);
       }
     }
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                  // TMEM lane quadrant of this warp
-    const int r = q * 32 + lane;             // row within a 128-row half
+    const int r = q * 32 + lane;             // weight row within the 128-row tile
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-    uint32_t acc_phase = 0;
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-      const int tt = item / a.m_tiles, mt = item % a.m_tiles;
-      const int e = a.tile_expert[tt];
-      const int rows = a.tile_rows[tt];
+    int local = 0;
+    int xb = 0;  // exchange buffer of the next SwiGLU chunk; alternates across items too
+    TileInfo cur = tile_info(a, blockIdx.x, n_items);
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++local) {
+      const TileInfo nxt = tile_info(a, item + gridDim.x, n_items);
+      const int mt = cur.mt;
+      const int rows = cur.rows;
       const int n16 = (rows + 15) & ~15;
-      const int row0 = tt * kTileRows;
-      if (!wait_or_abort(S.bar(kAccFull), acc_phase, abort_flag, a.status)) break;
+      const int row0 = cur.tt * kTileRows;
+      const int buf = local & 1;
+      const uint32_t acc_par = (uint32_t)(local >> 1) & 1u;
+      const float alpha = a.alpha[cur.e];
+      // the tile's per-row scales, loaded before the wait so the latency overlaps it
+      const float s_r = r < n16 ? a.row_scale[(size_t)row0 + r] : 0.0f;
+      // all four epilogue warps take the same stop decision, so none is left
+      // waiting alone at a named barrier; the first barrier also ends every
+      // read of the previous tile's staged scales
+      if (!wait_or_abort(R.bar(kBarAccFull + buf), acc_par, abort_flag, a.status)) *epi_stop = 1;
+      named_bar_sync(1, 128);
+      s_scale[r] = s_r;
+      const bool stop = *epi_stop != 0;
+      named_bar_sync(1, 128);
+      if (stop) break;
       tc_fence_after();
-      const float alpha = a.alpha[e];
-      for (int c0 = 0; c0 < n16; c0 += 16) {
-        float g[16], u[16];
-        tmem_ld16(tmem + lane_addr + c0, g);
-        tmem_ld16(tmem + lane_addr + 128 + c0, u);
-        tmem_wait_ld();
+      const uint32_t acc = tmem + lane_addr + buf * acc_stride;
+      if constexpr (MODE == kFc1Swiglu) {
+        // lanes 0-63: gate rows of features mt*64 + r; lanes 64-127: the matching up rows
+        const bool gate = q < 2;
+        const int f = mt * 64 + (r & 63);
+        for (int c0 = 0; c0 < n16; c0 += 32, xb ^= 1) {
+          float v[32];
+          tmem_ld16(acc + c0, *reinterpret_cast<float(*)[16]>(v));
+          if (c0 + 16 < n16) tmem_ld16(acc + c0 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+          tmem_wait_ld();
+          float* xrow = xchg + xb * (64 * 33) + (r & 63) * 33;
+          const int ncol = min(32, n16 - c0);
+          if (!gate) {
+            for (int j = 0; j < ncol; ++j)
+              xrow[j] = __fmul_rn(__fmul_rn(v[j], alpha), s_scale[c0 + j]);
+          }
+          named_bar_sync(1, 128);
+          if (gate) {
+            for (int j = 0; j < ncol; ++j) {
+              const int col = c0 + j;
+              if (col >= rows) break;
+              const size_t p = (size_t)row0 + col;
+              const float yg = __fmul_rn(__fmul_rn(v[j], alpha), s_scale[col]);
+              const float yu = xrow[j];
+              a.act_out[p * a.I + f] = __fmul_rn(__fdiv_rn(yg, __fadd_rn(1.0f, expf(-yg))), yu);
+            }
+          }
+        }
+      } else {
+        for (int c0 = 0; c0 < n16; c0 += 16) {
+          float v[16];
+          tmem_ld16(acc + c0, v);
+          tmem_wait_ld();
 #pragma unroll 4
-        for (int j = 0; j < 16; ++j) {
-          const int col = c0 + j;
-          if (col >= rows) break;
-          const size_t p = (size_t)row0 + col;
-          const float s = a.row_scale[p];
-          if constexpr (MODE == kFc1Swiglu) {
-            const float yg = __fmul_rn(__fmul_rn(g[j], alpha), s);
-            const float yu = __fmul_rn(__fmul_rn(u[j], alpha), s);
-            const float act = __fmul_rn(__fdiv_rn(yg, __fadd_rn(1.0f, expf(-yg))), yu);
-            a.act_out[p * a.I + mt * 128 + r] = act;
-          } else if constexpr (MODE == kFc1Relu2) {
-            const float y0 = fmaxf(__fmul_rn(__fmul_rn(g[j], alpha), s), 0.0f);
-            const float y1 = fmaxf(__fmul_rn(__fmul_rn(u[j], alpha), s), 0.0f);
-            float* dst = a.act_out + p * a.I + mt * 256 + r;
-            dst[0] = __fmul_rn(y0, y0);
-            dst[128] = __fmul_rn(y1, y1);
-          } else {
-            const float z0 = __fmul_rn(__fmul_rn(g[j], alpha), s);
-            const float z1 = __fmul_rn(__fmul_rn(u[j], alpha), s);
-            uint16_t* dst = a.route_out + p * a.H + mt * 256 + r;
-            dst[0] = __bfloat16_as_ushort(__float2bfloat16_rn(z0));
-            dst[128] = __bfloat16_as_ushort(__float2bfloat16_rn(z1));
+          for (int j = 0; j < 16; ++j) {
+            const int col = c0 + j;
+            if (col >= rows) break;
+            const size_t p = (size_t)row0 + col;
+            const float y = __fmul_rn(__fmul_rn(v[j], alpha), s_scale[col]);
+            if constexpr (MODE == kFc1Relu2) {
+              const float t = fmaxf(y, 0.0f);
+              a.act_out[p * a.I + mt * 128 + r] = __fmul_rn(t, t);
+            } else {
+              a.route_out[p * a.H + mt * 128 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+            }
           }
         }
       }
       tc_fence_before();
-      mbar_arrive(S.bar(kAccEmpty));
-      acc_phase ^= 1;
+      mbar_arrive(R.bar(kBarAccEmpty + buf));
+      cur = nxt;
     }
   }
 
@@ -290,7 +400,7 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
 template <int MODE>
 static cudaError_t launch_mode(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
                                int grid, cudaStream_t s) {
-  static bool configured = false;  // per process; the attribute is per function
+  static bool configured = false;  // the attribute is per function
   if (!configured) {
     cudaError_t err = cudaFuncSetAttribute(gemm_w4a4_kernel<MODE>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -298,8 +408,8 @@ static cudaError_t launch_mode(const CUtensorMap& tmA, const CUtensorMap& tmB, c
     if (err != cudaSuccess) return err;
     configured = true;
   }
-  gemm_w4a4_kernel<MODE><<<grid, w4a4::kThreads, w4a4::kSmemBytes, s>>>(tmA, tmB, a);
-  return cudaGetLastError();
+  return launch_pdl(gemm_w4a4_kernel<MODE>, dim3(grid), dim3(w4a4::kThreads),
+                    (size_t)w4a4::kSmemBytes, s, tmA, tmB, a);
 }
 
 cudaError_t launch_gemm_w4a4(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,

@@ -5,6 +5,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 namespace moe {
 
@@ -16,9 +17,11 @@ constexpr int kTileRows = 128;
 constexpr int kStatusFlags = 0;   // error bits, see below
 constexpr int kStatusTiles = 1;   // number of token tiles after the scan
 constexpr int kStatusRows = 2;    // padded rows in use after the scan
+constexpr int kStatusMaxRows = 3; // largest token tile (rows) after the scan
 constexpr int kStatusWords = 16;
 
 constexpr int kFlagBadExpertId = 1;   // an id outside [-1, E) was seen (slot ignored)
+// The routing scan rewrites every status word each forward (no separate reset).
 constexpr int kFlagWaitTimeout = 2;   // a bounded in-kernel wait gave up
 
 struct RouteArgs {
@@ -30,8 +33,7 @@ struct RouteArgs {
   int32_t* chunk_prefix;
   int32_t* counts;
   int32_t* group_row0;
-  int32_t* tile_expert;
-  int32_t* tile_rows;
+  int4* tiles;  // per token tile: {expert, expert's first tile, expert's tiles, expert's routes}
   int32_t* inv;
   int32_t* perm;
   // W4A4 gather
@@ -53,20 +55,38 @@ enum GemmMode { kFc1Relu2 = 0, kFc1Swiglu = 1, kFc2 = 2 };
 struct GemmArgs {
   int mode;            // GemmMode
   int K;               // reduction length (H for FC1, I for FC2)
-  int m_tiles;         // 256-row weight tiles per expert
+  int m_tiles;         // 128-row weight tiles per expert
   int w_rows;          // weight rows per expert (N1 for FC1, H for FC2)
   const uint8_t* sfa;  // weight scales, swizzled, [E][w_rows * K/16]
   const uint8_t* sfb;  // token scales, swizzled over permuted rows
   const float* alpha;  // [E]
   const float* row_scale;  // per permuted row: s_t (FC1) or s2 (FC2)
-  const int32_t* tile_expert;
-  const int32_t* tile_rows;
+  const int4* tiles;   // per token tile: {expert, first tile, tiles, routes} of its expert
   int32_t* status;
   float* act_out;      // FC1: [rows][I] fp32
   int I;
   uint16_t* route_out; // FC2: [rows][H] bf16
   int H;
 };
+
+// Launch with programmatic stream serialization: the kernel may start while the
+// previous kernel of the stream finishes; it calls pdl_wait() before reading
+// anything that kernel wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 void launch_quantize_tokens(int T, int H, const void* x, uint8_t* codes, uint8_t* sf, float* scale,
                             cudaStream_t s);

@@ -88,9 +88,8 @@ void compute_layout(const moe_dims* d, int32_t T, int32_t K, int32_t w4a16, moe_
   L->status = take(sizeof(int32_t) * kStatusWords);
   L->counts = take(sizeof(int32_t) * E);
   L->group_row0 = take(sizeof(int32_t) * E);
-  L->tile_expert = take(sizeof(int32_t) * (tiles ? tiles : 1));
-  L->tile_rows = take(sizeof(int32_t) * (tiles ? tiles : 1));
-  L->chunk_counts = take(sizeof(int32_t) * nchunks * E);
+  L->tiles = take(sizeof(int32_t) * 4 * (tiles ? tiles : 1));
+  L->chunk_counts = take(sizeof(int32_t) * nchunks * (E + 1));
   L->chunk_prefix = take(sizeof(int32_t) * nchunks * E);
   L->inv = take(sizeof(int32_t) * TK);
   L->perm = take(sizeof(int32_t) * rows);
@@ -287,8 +286,7 @@ static RouteArgs route_args(const moe_dims* d, int32_t T, int32_t K, const int32
   r.chunk_prefix = at<int32_t>(ws, L.chunk_prefix);
   r.counts = at<int32_t>(ws, L.counts);
   r.group_row0 = at<int32_t>(ws, L.group_row0);
-  r.tile_expert = at<int32_t>(ws, L.tile_expert);
-  r.tile_rows = at<int32_t>(ws, L.tile_rows);
+  r.tiles = at<int4>(ws, L.tiles);
   r.inv = at<int32_t>(ws, L.inv);
   r.perm = at<int32_t>(ws, L.perm);
   return r;
@@ -315,9 +313,6 @@ moe_status moe_nvfp4_forward(const moe_dims* d, const moe_nvfp4_weights* w, int3
       !make_tmap_bytes(&tmB2, at<uint8_t>(ws, L.fc2q_codes), I / 2, L.rows_cap, 16))
     return MOE_ERR_CUDA;
 
-  cudaError_t err = cudaMemsetAsync(at<int32_t>(ws, L.status), 0, sizeof(int32_t) * kStatusWords, s);
-  if (err != cudaSuccess) return MOE_ERR_CUDA;
-
   mark(0, s);
   RouteArgs r = route_args(d, T, K, topk_ids, ws, L, 0);
   r.xc = codes;
@@ -333,20 +328,19 @@ moe_status moe_nvfp4_forward(const moe_dims* d, const moe_nvfp4_weights* w, int3
   GemmArgs g{};
   g.mode = d->act == MOE_ACT_SWIGLU ? kFc1Swiglu : kFc1Relu2;
   g.K = H;
-  g.m_tiles = N1 / 256;
+  g.m_tiles = N1 / 128;
   g.w_rows = N1;
   g.sfa = w->fc1_sf;
   g.sfb = at<uint8_t>(ws, L.xq_sf);
   g.alpha = w->fc1_alpha;
   g.row_scale = at<float>(ws, L.xq_scale);
-  g.tile_expert = at<int32_t>(ws, L.tile_expert);
-  g.tile_rows = at<int32_t>(ws, L.tile_rows);
+  g.tiles = at<int4>(ws, L.tiles);
   g.status = at<int32_t>(ws, L.status);
   g.act_out = at<float>(ws, L.act);
   g.I = I;
   g.H = H;
   int grid = (int)std::min<int64_t>(sms, tiles_cap * g.m_tiles);
-  if ((err = launch_gemm_w4a4(tmA1, tmB1, g, grid, s)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gemm_w4a4(tmA1, tmB1, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
   mark(2, s);
 
   launch_requant(T * K, I, at<int32_t>(ws, L.inv), at<float>(ws, L.act),
@@ -357,7 +351,7 @@ moe_status moe_nvfp4_forward(const moe_dims* d, const moe_nvfp4_weights* w, int3
   GemmArgs g2 = g;
   g2.mode = kFc2;
   g2.K = I;
-  g2.m_tiles = H / 256;
+  g2.m_tiles = H / 128;
   g2.w_rows = H;
   g2.sfa = w->fc2_sf;
   g2.sfb = at<uint8_t>(ws, L.fc2q_sf);
@@ -366,7 +360,7 @@ moe_status moe_nvfp4_forward(const moe_dims* d, const moe_nvfp4_weights* w, int3
   g2.act_out = nullptr;
   g2.route_out = at<uint16_t>(ws, L.route);
   grid = (int)std::min<int64_t>(sms, tiles_cap * g2.m_tiles);
-  if ((err = launch_gemm_w4a4(tmA2, tmB2, g2, grid, s)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gemm_w4a4(tmA2, tmB2, g2, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
   mark(4, s);
 
   launch_finalize(T, K, H, at<int32_t>(ws, L.inv), topk_w, at<uint16_t>(ws, L.route), out_bf16, s);

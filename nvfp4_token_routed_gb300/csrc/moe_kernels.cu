@@ -21,6 +21,8 @@ __global__ void __launch_bounds__(256) quantize_tokens_kernel(int T, int H,
                                                               uint8_t* __restrict__ codes,
                                                               uint8_t* __restrict__ sf,
                                                               float* __restrict__ scale) {
+  pdl_wait();
+  pdl_trigger();
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -53,8 +55,8 @@ void launch_quantize_tokens(int T, int H, const void* x, uint8_t* codes, uint8_t
                             cudaStream_t s) {
   const int warps = 8;
   const int blocks = (T + warps - 1) / warps;
-  quantize_tokens_kernel<<<blocks, warps * 32, 0, s>>>(T, H, static_cast<const uint4*>(x), codes,
-                                                       sf, scale);
+  launch_pdl(quantize_tokens_kernel, dim3(blocks), dim3(warps * 32), 0, s, T, H,
+             static_cast<const uint4*>(x), codes, sf, scale);
 }
 
 // ============================================================== weight preparation
@@ -83,7 +85,7 @@ __global__ void __launch_bounds__(256) expert_amax_kernel(const uint4* __restric
 }
 
 // Stage 2: one warp per stored row.  For SwiGLU the stored FC1 row order
-// interleaves 128-row blocks [gate f0..f0+127 | up f0..f0+127], so one 256-row
+// interleaves 64-row blocks [gate f0..f0+63 | up f0..f0+63], so one 128-row
 // GEMM tile holds matching gate and up rows; canonical order is [gate; up].
 __global__ void __launch_bounds__(256) quantize_weights_kernel(
     const uint4* __restrict__ w, int E, int N, int D, int swiglu_I,
@@ -96,8 +98,8 @@ __global__ void __launch_bounds__(256) quantize_weights_kernel(
   const int ir = (int)(gw % N);
   int cr = ir;
   if (swiglu_I > 0) {
-    const int b = ir >> 7;
-    cr = (b & 1) * swiglu_I + (b >> 1) * 128 + (ir & 127);
+    const int b = ir >> 6;
+    cr = (b & 1) * swiglu_I + (b >> 1) * 64 + (ir & 63);
   }
   const float amax = __uint_as_float(amax_bits[e]);
   const uint4* row = w + ((size_t)e * N + cr) * (D / 8);
@@ -148,44 +150,56 @@ void launch_prepare_fc(int E, int N, int D, int swiglu_I, const void* w, uint8_t
 // ============================================================== routing permutation
 // Stable counting sort of the (token, slot) routes by expert: per-chunk
 // histograms, a per-expert scan over chunks plus an exclusive scan of the
-// 128-row-padded group sizes, then a stable scatter that also gathers the
-// quantized rows into expert-contiguous order.
+// 128-row-padded group sizes, a stable scatter of the route ids, then a gather
+// of the token rows into expert-contiguous order.
 constexpr int kChunk = 256;
 
 __global__ void __launch_bounds__(kChunk) route_count_kernel(const int32_t* __restrict__ ids,
                                                              int TK, int E,
-                                                             int32_t* __restrict__ chunk_counts,
-                                                             int32_t* __restrict__ status) {
+                                                             int32_t* __restrict__ chunk_counts) {
   extern __shared__ int s_cnt[];
+  pdl_wait();
+  pdl_trigger();
   for (int i = threadIdx.x; i < E; i += blockDim.x) s_cnt[i] = 0;
   __syncthreads();
   const int idx = blockIdx.x * kChunk + threadIdx.x;
+  int bad = 0;
   if (idx < TK) {
     const int e = ids[idx];
     if (e >= 0 && e < E)
       atomicAdd(&s_cnt[e], 1);
     else if (e != -1)
-      atomicOr(status + kStatusFlags, kFlagBadExpertId);
+      bad = 1;
   }
-  __syncthreads();
-  for (int i = threadIdx.x; i < E; i += blockDim.x) chunk_counts[(size_t)blockIdx.x * E + i] = s_cnt[i];
+  bad = __syncthreads_or(bad);
+  // row of E counts plus one flag word: the chunk held an id outside [-1, E)
+  int32_t* row = chunk_counts + (size_t)blockIdx.x * (E + 1);
+  for (int i = threadIdx.x; i < E; i += blockDim.x) row[i] = s_cnt[i];
+  if (threadIdx.x == 0) row[E] = bad;
 }
 
 __global__ void __launch_bounds__(1024) route_scan_kernel(
     int nchunks, int E, const int32_t* __restrict__ chunk_counts, int32_t* __restrict__ chunk_prefix,
-    int32_t* __restrict__ counts, int32_t* __restrict__ group_row0, int32_t* __restrict__ tile_expert,
-    int32_t* __restrict__ tile_rows, int32_t* __restrict__ status) {
+    int32_t* __restrict__ counts, int32_t* __restrict__ group_row0, int4* __restrict__ tiles,
+    int32_t* __restrict__ status) {
+  pdl_wait();
+  pdl_trigger();
   const int e = threadIdx.x;
   int total = 0;
   if (e < E) {
     for (int c = 0; c < nchunks; ++c) {
       chunk_prefix[(size_t)c * E + e] = total;
-      total += chunk_counts[(size_t)c * E + e];
+      total += chunk_counts[(size_t)c * (E + 1) + e];
     }
   }
+  int bad = 0;
+  for (int c = e; c < nchunks; c += blockDim.x) bad |= chunk_counts[(size_t)c * (E + 1) + E];
+  bad = __syncthreads_or(bad);
   const int ntiles = (total + kTileRows - 1) / kTileRows;
-  // block-wide exclusive scan of ntiles
+  // block-wide exclusive scan of ntiles, and the largest tile
   __shared__ int warp_sum[32];
+  __shared__ int max_rows;
+  if (e == 0) max_rows = 0;
   const int lane = e & 31, wid = e >> 5;
   int incl = ntiles;
 #pragma unroll
@@ -195,6 +209,7 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(
   }
   if (lane == 31) warp_sum[wid] = incl;
   __syncthreads();
+  if (total > 0) atomicMax(&max_rows, min(kTileRows, total));
   if (wid == 0) {
     int v = (lane < (int)(blockDim.x >> 5)) ? warp_sum[lane] : 0;
 #pragma unroll
@@ -209,32 +224,30 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(
   if (e < E) {
     counts[e] = total;
     group_row0[e] = base * kTileRows;
-    for (int j = 0; j < ntiles; ++j) {
-      tile_expert[base + j] = e;
-      tile_rows[base + j] = min(kTileRows, total - j * kTileRows);
-    }
+    for (int j = 0; j < ntiles; ++j) tiles[base + j] = make_int4(e, base, ntiles, total);
   }
   if (e == (int)blockDim.x - 1) {
+    status[kStatusFlags] = bad ? kFlagBadExpertId : 0;
     status[kStatusTiles] = base + ntiles;
     status[kStatusRows] = (base + ntiles) * kTileRows;
+    status[kStatusMaxRows] = max_rows;
   }
 }
 
-template <bool kW4A16>
 __global__ void __launch_bounds__(kChunk) route_scatter_kernel(
-    const int32_t* __restrict__ ids, int TK, int K, int E, const int32_t* __restrict__ chunk_prefix,
-    const int32_t* __restrict__ group_row0, int32_t* __restrict__ inv, int32_t* __restrict__ perm,
-    int H, const uint8_t* __restrict__ xc, const uint8_t* __restrict__ xsf,
-    const float* __restrict__ xs, uint8_t* __restrict__ pc, uint8_t* __restrict__ psf,
-    float* __restrict__ ps, const uint4* __restrict__ xb, uint4* __restrict__ pb) {
+    const int32_t* __restrict__ ids, int TK, int E, const int32_t* __restrict__ chunk_prefix,
+    const int32_t* __restrict__ group_row0, int32_t* __restrict__ inv, int32_t* __restrict__ perm) {
   extern __shared__ int s_wcnt[];  // [kChunk/32][E]
   constexpr int kWarps = kChunk / 32;
+  pdl_wait();
+  pdl_trigger();
   for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) s_wcnt[i] = 0;
   __syncthreads();
   const int idx = blockIdx.x * kChunk + threadIdx.x;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = idx < TK ? ids[idx] : -1;
   const bool valid = e >= 0 && e < E;
+  // stable rank: earlier lanes of this warp with the same expert, then earlier warps
   const unsigned peers = __match_any_sync(0xFFFFFFFFu, valid ? e : -1);
   const int rank = __popc(peers & ((1u << lane) - 1u));
   if (valid && rank == 0) s_wcnt[w * E + e] = __popc(peers);
@@ -247,45 +260,59 @@ __global__ void __launch_bounds__(kChunk) route_scatter_kernel(
     perm[p] = idx;
   }
   if (idx < TK) inv[idx] = p;
-  // gather: the warp copies each of its routes' token rows to their positions
-  for (int l = 0; l < 32; ++l) {
-    const int pp = __shfl_sync(0xFFFFFFFFu, p, l);
-    const int ii = __shfl_sync(0xFFFFFFFFu, idx, l);
-    if (pp < 0) continue;
-    const int t = ii / K;
-    if constexpr (kW4A16) {
-      const uint4* src = xb + (size_t)t * (H / 8);
-      uint4* dst = pb + (size_t)pp * (H / 8);
-      for (int i = lane; i < H / 8; i += 32) dst[i] = __ldg(src + i);
-    } else {
-      const uint4* src = reinterpret_cast<const uint4*>(xc + (size_t)t * (H / 2));
-      uint4* dst = reinterpret_cast<uint4*>(pc + (size_t)pp * (H / 2));
-      for (int i = lane; i < H / 32; i += 32) dst[i] = __ldg(src + i);
-      const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(xsf + (size_t)t * (H / 16));
-      const uint32_t c16 = (uint32_t)(H / 16);
-      for (int g = lane; g < H / 64; g += 32)
-        *reinterpret_cast<uint32_t*>(psf + sf_offset(pp, 4 * g, c16)) = __ldg(ssrc + g);
-      if (lane == 0) ps[pp] = xs[t];
-    }
+}
+
+// Gather: one warp per route copies its token's row to the route's permuted row.
+template <bool kW4A16>
+__global__ void __launch_bounds__(256) gather_rows_kernel(
+    int TK, int K, int H, const int32_t* __restrict__ inv, const uint8_t* __restrict__ xc,
+    const uint8_t* __restrict__ xsf, const float* __restrict__ xs, uint8_t* __restrict__ pc,
+    uint8_t* __restrict__ psf, float* __restrict__ ps, const uint4* __restrict__ xb,
+    uint4* __restrict__ pb) {
+  pdl_wait();
+  pdl_trigger();
+  const int idx = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (idx >= TK) return;
+  const int p = inv[idx];
+  if (p < 0) return;
+  const int t = idx / K;
+  if constexpr (kW4A16) {
+    const uint4* src = xb + (size_t)t * (H / 8);
+    uint4* dst = pb + (size_t)p * (H / 8);
+    for (int i = lane; i < H / 8; i += 32) dst[i] = __ldg(src + i);
+  } else {
+    const uint4* src = reinterpret_cast<const uint4*>(xc + (size_t)t * (H / 2));
+    uint4* dst = reinterpret_cast<uint4*>(pc + (size_t)p * (H / 2));
+    for (int i = lane; i < H / 32; i += 32) dst[i] = __ldg(src + i);
+    const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(xsf + (size_t)t * (H / 16));
+    const uint32_t c16 = (uint32_t)(H / 16);
+    for (int g = lane; g < H / 64; g += 32)
+      *reinterpret_cast<uint32_t*>(psf + sf_offset(p, 4 * g, c16)) = __ldg(ssrc + g);
+    if (lane == 0) ps[p] = xs[t];
   }
 }
 
 void launch_route(const RouteArgs& a, cudaStream_t s) {
   const int nchunks = (a.TK + kChunk - 1) / kChunk;
-  route_count_kernel<<<nchunks, kChunk, sizeof(int) * a.E, s>>>(a.ids, a.TK, a.E, a.chunk_counts,
-                                                               a.status);
-  route_scan_kernel<<<1, 1024, 0, s>>>(nchunks, a.E, a.chunk_counts, a.chunk_prefix, a.counts,
-                                       a.group_row0, a.tile_expert, a.tile_rows, a.status);
+  launch_pdl(route_count_kernel, dim3(nchunks), dim3(kChunk), sizeof(int) * a.E, s, a.ids, a.TK,
+             a.E, a.chunk_counts);
+  launch_pdl(route_scan_kernel, dim3(1), dim3(1024), 0, s, nchunks, a.E,
+             (const int32_t*)a.chunk_counts, a.chunk_prefix, a.counts, a.group_row0, a.tiles,
+             a.status);
   const size_t smem = sizeof(int) * (kChunk / 32) * a.E;
+  launch_pdl(route_scatter_kernel, dim3(nchunks), dim3(kChunk), smem, s, a.ids, a.TK, a.E,
+             (const int32_t*)a.chunk_prefix, (const int32_t*)a.group_row0, a.inv, a.perm);
+  const int gblocks = (a.TK + 7) / 8;
   if (a.w4a16)
-    route_scatter_kernel<true><<<nchunks, kChunk, smem, s>>>(
-        a.ids, a.TK, a.K, a.E, a.chunk_prefix, a.group_row0, a.inv, a.perm, a.H, nullptr, nullptr,
-        nullptr, nullptr, nullptr, nullptr, static_cast<const uint4*>(a.xb),
-        static_cast<uint4*>(a.pb));
+    launch_pdl(gather_rows_kernel<true>, dim3(gblocks), dim3(256), 0, s, a.TK, a.K, a.H,
+               (const int32_t*)a.inv, (const uint8_t*)nullptr, (const uint8_t*)nullptr,
+               (const float*)nullptr, (uint8_t*)nullptr, (uint8_t*)nullptr, (float*)nullptr,
+               static_cast<const uint4*>(a.xb), static_cast<uint4*>(a.pb));
   else
-    route_scatter_kernel<false><<<nchunks, kChunk, smem, s>>>(
-        a.ids, a.TK, a.K, a.E, a.chunk_prefix, a.group_row0, a.inv, a.perm, a.H, a.xc, a.xsf, a.xs,
-        a.pc, a.psf, a.ps, nullptr, nullptr);
+    launch_pdl(gather_rows_kernel<false>, dim3(gblocks), dim3(256), 0, s, a.TK, a.K, a.H,
+               (const int32_t*)a.inv, a.xc, a.xsf, a.xs, a.pc, a.psf, a.ps,
+               (const uint4*)nullptr, (uint4*)nullptr);
 }
 
 // ============================================================== FC2-input requant
@@ -297,6 +324,8 @@ __global__ void __launch_bounds__(256) requant_kernel(int TK, int I, const int32
                                                       uint8_t* __restrict__ qc,
                                                       uint8_t* __restrict__ qsf,
                                                       float* __restrict__ qs) {
+  pdl_wait();
+  pdl_trigger();
   const int idx = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (idx >= TK) return;
@@ -340,7 +369,8 @@ __global__ void __launch_bounds__(256) requant_kernel(int TK, int I, const int32
 void launch_requant(int TK, int I, const int32_t* inv, const float* act, uint8_t* qc, uint8_t* qsf,
                     float* qs, cudaStream_t s) {
   const int warps = 8;
-  requant_kernel<<<(TK + warps - 1) / warps, warps * 32, 0, s>>>(TK, I, inv, act, qc, qsf, qs);
+  launch_pdl(requant_kernel, dim3((TK + warps - 1) / warps), dim3(warps * 32), 0, s, TK, I, inv,
+             act, qc, qsf, qs);
 }
 
 // ============================================================== finalize
@@ -352,22 +382,38 @@ __global__ void __launch_bounds__(128) finalize_kernel(int K, int H, const int32
                                                        const float* __restrict__ w,
                                                        const uint4* __restrict__ route,
                                                        uint4* __restrict__ out) {
+  __shared__ int s_p[32];
+  __shared__ float s_w[32];
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x;
+  if (threadIdx.x < K) {
+    s_p[threadIdx.x] = inv[(size_t)t * K + threadIdx.x];
+    s_w[threadIdx.x] = w[(size_t)t * K + threadIdx.x];
+  }
+  __syncthreads();
   const int v = blockIdx.y * blockDim.x + threadIdx.x;
   if (v >= H / 8) return;
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-  for (int k = 0; k < K; ++k) {
-    const int p = inv[(size_t)t * K + k];
-    if (p < 0) continue;
-    const float wk = w[(size_t)t * K + k];
-    const uint4 r = route[(size_t)p * (H / 8) + v];
-    const uint32_t q[4] = {r.x, r.y, r.z, r.w};
+  for (int k0 = 0; k0 < K; k0 += 8) {
+    uint4 r[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      acc[2 * i] = __fmaf_rn(wk, __uint_as_float(q[i] << 16), acc[2 * i]);
-      acc[2 * i + 1] = __fmaf_rn(wk, __uint_as_float(q[i] & 0xFFFF0000u), acc[2 * i + 1]);
+    for (int j = 0; j < 8; ++j) {  // issue the loads of 8 routes before using any
+      const int p = k0 + j < K ? s_p[k0 + j] : -1;
+      r[j] = p >= 0 ? route[(size_t)p * (H / 8) + v] : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (k0 + j >= K || s_p[k0 + j] < 0) continue;
+      const float wk = s_w[k0 + j];
+      const uint32_t q[4] = {r[j].x, r[j].y, r[j].z, r[j].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = __fmaf_rn(wk, __uint_as_float(q[i] << 16), acc[2 * i]);
+        acc[2 * i + 1] = __fmaf_rn(wk, __uint_as_float(q[i] & 0xFFFF0000u), acc[2 * i + 1]);
+      }
     }
   }
   uint32_t o[4];
@@ -383,8 +429,8 @@ void launch_finalize(int T, int K, int H, const int32_t* inv, const float* w, co
                      void* out, cudaStream_t s) {
   const int threads = 128;
   dim3 grid(T, (H / 8 + threads - 1) / threads);
-  finalize_kernel<<<grid, threads, 0, s>>>(K, H, inv, w, static_cast<const uint4*>(route),
-                                           static_cast<uint4*>(out));
+  launch_pdl(finalize_kernel, grid, dim3(threads), 0, s, K, H, inv, w,
+             static_cast<const uint4*>(route), static_cast<uint4*>(out));
 }
 
 }  // namespace moe

@@ -59,8 +59,8 @@ extern "C" moe_status moe_nvfp4_forward_noalloc(const moe_dims* d, const moe_nvf
   void* scratch = nullptr;
   moe_status st = scratch_for_current_device(&scratch);
   if (st != MOE_OK) return st;
-  // The forward clears the scratch's status words itself before its first
-  // kernel; every other scratch region is written before it is read, so
+  // The forward rewrites the scratch's status words itself (in its routing
+  // step); every other scratch region is written before it is read, so
   // whatever an earlier call left in the array does not matter.
   return moe_nvfp4_forward(d, w, T, K, codes, sf, scale, topk_ids, topk_w, out_bf16, scratch,
                            kNoAllocScratchBytes, stream);

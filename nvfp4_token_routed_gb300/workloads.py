@@ -39,6 +39,12 @@ class Workload:
         d["name"] = f"{self.name.split('@')[0]}@T{T}"
         return Workload(**d)
 
+    def with_E(self, E):
+        d = dict(self.__dict__)
+        d["E"] = E
+        d["name"] = f"{self.name}@E{E}"
+        return Workload(**d)
+
 
 # The five workload shapes (tiny squared-ReLU; SwiGLU E64; mid-scale Zipf; DeepSeek-like
 # H7168/I2048/E256; the pages' benchmark shape H7168/I3072/E384 on one GPU).

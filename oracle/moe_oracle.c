@@ -197,12 +197,13 @@ static float quantize_row_per_token(const float* v, int64_t D, uint8_t* codes, u
  * scales [T][H/16], per-token fp32 scales [T]. */
 void orc_quantize_tokens(int64_t T, int64_t H, const uint16_t* x, uint8_t* codes, uint8_t* sf,
                          float* s) {
-    float* row = (float*)malloc(sizeof(float) * (size_t)H);
+#pragma omp parallel for schedule(static)
     for (int64_t t = 0; t < T; ++t) {
+        float* row = (float*)malloc(sizeof(float) * (size_t)H);
         for (int64_t h = 0; h < H; ++h) row[h] = bf16_to_f32(x[t * H + h]);
         s[t] = quantize_row_per_token(row, H, codes + t * (H / 2), sf + t * (H / 16));
+        free(row);
     }
-    free(row);
 }
 
 /* Float-input variant used for the requantized FC2 input (R6). */
@@ -215,8 +216,9 @@ float orc_quantize_row_per_token_f32(const float* v, int64_t D, uint8_t* codes, 
  * is added: per-expert FP32 alphas; How to extend: alpha = 1 / w_scale). */
 void orc_prepare_fc(int64_t E, int64_t N, int64_t D, const uint16_t* w, uint8_t* codes,
                     uint8_t* sf, float* alpha) {
-    float* row = (float*)malloc(sizeof(float) * (size_t)D);
+#pragma omp parallel for schedule(dynamic, 1)
     for (int64_t e = 0; e < E; ++e) {
+        float* row = (float*)malloc(sizeof(float) * (size_t)D);
         const uint16_t* we = w + e * N * D;
         float amax = 0.0f;
         for (int64_t i = 0; i < N * D; ++i) amax = fmaxf(amax, fabsf(bf16_to_f32(we[i])));
@@ -226,6 +228,7 @@ void orc_prepare_fc(int64_t E, int64_t N, int64_t D, const uint16_t* w, uint8_t*
             memset(ce, 0, (size_t)(N * D / 2));
             memset(se, 0, (size_t)(N * D / 16));
             alpha[e] = 0.0f;
+            free(row);
             continue;
         }
         float w_scale = 2688.0f / amax;
@@ -234,8 +237,8 @@ void orc_prepare_fc(int64_t E, int64_t N, int64_t D, const uint16_t* w, uint8_t*
             for (int64_t d = 0; d < D; ++d) row[d] = bf16_to_f32(we[n * D + d]);
             orc_quantize_row(row, D, w_scale, ce + n * (D / 2), se + n * (D / 16));
         }
+        free(row);
     }
-    free(row);
 }
 
 /* Byte offset of block scale (row r, scale column j) in the 128x4-swizzled

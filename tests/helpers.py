@@ -10,6 +10,9 @@ from oracle import oracle as O
 from nvfp4_token_routed_gb300 import workloads as W
 
 
+TILE_ROWS = 128  # each expert group of the permuted buffers starts at a multiple of this
+
+
 def sf_offsets(rows, c16):
     """Byte offsets of (row, scale column) in a 128x4-swizzled plane (vectorised)."""
     r = np.asarray(rows, np.int64)[:, None]
@@ -24,13 +27,13 @@ def unswizzle(plane, rows, c16):
 
 
 def stored_fc1_rows(N1, I, act):
-    """Canonical FC1 row held at each stored row (stored order interleaves 128-row
+    """Canonical FC1 row held at each stored row (stored order interleaves 64-row
     [gate | up] blocks for SwiGLU; identity for squared ReLU)."""
     ir = np.arange(N1)
     if act != "swiglu":
         return ir
-    b = ir // 128
-    return (b % 2) * I + (b // 2) * 128 + ir % 128
+    b = ir // 64
+    return (b % 2) * I + (b // 2) * 64 + ir % 64
 
 
 def signed_step(codes_a, codes_b):

@@ -13,7 +13,7 @@ import nvfp4_token_routed_gb300 as M
 from nvfp4_token_routed_gb300 import workloads as W
 from oracle import oracle as O
 
-from helpers import (OracleRun, bf16_np, rel_l2, signed_step, stored_fc1_rows, to_np_u16,
+from helpers import (TILE_ROWS, OracleRun, bf16_np, rel_l2, signed_step, stored_fc1_rows, to_np_u16,
                      unpack_codes, unswizzle)
 
 pytestmark = pytest.mark.gpu
@@ -107,10 +107,11 @@ def test_routing_permutation_bit_exact(name):
     counts = g.view("counts", torch.int32, (E,))
     assert np.array_equal(counts, o.res["counts"])
     row0 = g.view("group_row0", torch.int32, (E,))
-    tiles = np.ceil(counts / 128).astype(np.int64)
-    assert np.array_equal(row0, 128 * np.concatenate([[0], np.cumsum(tiles)[:-1]]))
+    tiles = np.ceil(counts / TILE_ROWS).astype(np.int64)
+    assert np.array_equal(row0, TILE_ROWS * np.concatenate([[0], np.cumsum(tiles)[:-1]]))
     status = g.view("status", torch.int32, (16,))
     assert status[1] == tiles.sum()
+    assert status[3] == min(TILE_ROWS, counts.max())
     rmap = _rows_map(g, o)
     perm = g.view("perm", torch.int32, (g.L["rows_cap"],))
     assert np.array_equal(perm[rmap], o.res["perm"])
