@@ -46,6 +46,7 @@ def parse():
     p.add_argument("--T", type=int, default=0, help="override the workload's token count")
     p.add_argument("--E", type=int, default=0, help="override the expert count (profiling cases)")
     p.add_argument("--no-graph", action="store_true")
+    p.add_argument("--w4a16", action="store_true", help="time the BF16-activation variant")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     return p.parse_args()
@@ -136,15 +137,19 @@ def make_inputs(wl, device):
     return x, w1, w2, ids, wts
 
 
-def algorithmic_fc1_bytes(wl, ids):
+def algorithmic_fc1_bytes(wl, ids, w4a16=False):
     """Algorithmic DRAM bytes of one FC1 launch: each touched expert's FC1 codes
-    and scales once (9/16 byte per weight), the permuted token codes and scales,
-    the fp32 activated rows and the per-row scales."""
+    and scales once (9/16 byte per weight); W4A4: the permuted token codes and
+    scales, the fp32 activated rows and the per-row scales; W4A16: the permuted
+    bf16 token rows and the bf16 activated rows."""
     idsn = ids.cpu().numpy().ravel()
     valid = idsn[(idsn >= 0) & (idsn < wl.E)]
     U = int(np.unique(valid).size)
     R = int(valid.size)
-    return U * wl.N1 * wl.H * 9 / 16 + R * wl.H * 9 / 16 + 4 * R * wl.I + 4 * R, U, R
+    weights = U * wl.N1 * wl.H * 9 / 16
+    if w4a16:
+        return weights + 2 * R * wl.H + 2 * R * wl.I, U, R
+    return weights + R * wl.H * 9 / 16 + 4 * R * wl.I + 4 * R, U, R
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -258,11 +263,14 @@ def run_ours(args, rank, world, local_rank):
     sf = torch.empty(T, H // 16, dtype=torch.uint8, device=dev)
     scale = torch.empty(T, dtype=torch.float32, device=dev)
     out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
-    ws = M.workspace(w, T, K, device=dev)
+    ws = M.workspace(w, T, K, w4a16=args.w4a16, device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
     def step():
+        if args.w4a16:
+            M.moe_nvfp4_forward_w4a16(w.dims, w, x_d, ids_d, wts_d, out, ws, stream)
+            return
         M.moe_nvfp4_quantize_tokens(x_d, codes, sf, scale, stream)
         M.moe_nvfp4_forward(w.dims, w, codes, sf, scale, ids_d, wts_d, out, ws, stream)
 
@@ -364,8 +372,11 @@ def run_ours(args, rank, world, local_rank):
         x_e.copy_(x_h, non_blocking=True)
         ids_e.copy_(ids_h, non_blocking=True)
         wts_e.copy_(wts_h, non_blocking=True)
-        M.moe_nvfp4_quantize_tokens(x_e, codes, sf, scale, stream)
-        M.moe_nvfp4_forward(w.dims, w, codes, sf, scale, ids_e, wts_e, out, ws, stream)
+        if args.w4a16:
+            M.moe_nvfp4_forward_w4a16(w.dims, w, x_e, ids_e, wts_e, out, ws, stream)
+        else:
+            M.moe_nvfp4_quantize_tokens(x_e, codes, sf, scale, stream)
+            M.moe_nvfp4_forward(w.dims, w, codes, sf, scale, ids_e, wts_e, out, ws, stream)
         out_h.copy_(out, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -393,7 +404,7 @@ def run_ours(args, rank, world, local_rank):
 
     if rank != 0:
         return
-    fc1_bytes, U, R = algorithmic_fc1_bytes(wl, ids)
+    fc1_bytes, U, R = algorithmic_fc1_bytes(wl, ids, args.w4a16)
     fc1_mean = statistics.fmean(fc1_ms)
     hbm, src = peaks()
     achieved = fc1_bytes / (fc1_mean * 1e-3) / 1e9
@@ -401,12 +412,14 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "us_per_layer": ms_per_step * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "nvfp4", "data": "synthetic (seeded N(0,1)-family inputs)",
-        "config": {"workload": wl.name, "T": T, "H": H, "I": wl.I, "E": wl.E, "K": K,
+        "vs_baseline": None, "dtype": "bf16 x nvfp4" if args.w4a16 else "nvfp4",
+        "data": "synthetic (seeded N(0,1)-family inputs)",
+        "config": {"workload": wl.name + ("+w4a16" if args.w4a16 else ""), "T": T, "H": H, "I": wl.I, "E": wl.E, "K": K,
                    "act": wl.act, "routes": R, "experts_touched": U,
                    "l2": "flushed (256 MB write) between timed steps",
                    "graph": graph is not None, "parallelism": f"replicas x{world}"},
-        "roofline": {"kernel": "fc1 grouped GEMM (gemm_w4a4_kernel<SwiGLU|ReLU2>)",
+        "roofline": {"kernel": ("fc1 grouped GEMM (gemm_w4a16_kernel<SwiGLU|ReLU2>)" if args.w4a16
+                                else "fc1 grouped GEMM (gemm_w4a4_kernel<SwiGLU|ReLU2>)"),
                      "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "peak_source": src,
                      "traffic": traffic_for(wl.name), "algorithmic_bytes": fc1_bytes,
@@ -415,11 +428,11 @@ def run_ours(args, rank, world, local_rank):
                                "over a second pass of the same K steps"},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "gpu_launches": (KERNELS_PER_STEP - (2 if args.w4a16 else 0)) * args.steps,
         "clocks": clocks,
         "wall_s": t_wall,
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and not args.w4a16:
         line["cpu_baseline"] = cpu_baseline(wl, x, w1, w2, ids, wts, args.cpu_seconds)
     print(json.dumps(line), flush=True)
 

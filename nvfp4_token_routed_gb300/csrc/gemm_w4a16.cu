@@ -1,0 +1,495 @@
+// gemm_w4a16.cu -- BF16-activation x NVFP4-weight grouped GEMMs (FC1 with fused
+// activation and bf16 handoff, FC2) on tcgen05 tensor cores.
+//
+// Megatron-LM PR #8262, "How to extend" (BF16 x NVFP4, 'weight_only'): bf16
+// hidden states meet the same prepared NVFP4 weights and alphas, no activation
+// quantization.  FlashInfer PR #5019, "Tensor and numerical contract": decode
+// E2M1 x E4M3 to BF16, accumulate in FP32, then apply the expert alpha; FC1's
+// activation comes before a BF16 handoff; FC2 applies alpha before BF16 output.
+//
+// Structure (swap-AB as in the W4A4 kernel; weights are the M=128 operand and
+// are decoded on chip, never written back to global or shared memory):
+//   * warp 0: TMA producer -- packed E2M1 weight slots (128 rows x 128 B = 256 K
+//     elements, 128-byte swizzle, so each row is read in 128-byte runs) with
+//     their E4M3 scale atoms (bulk copy), and bf16 token stages (two 64-element
+//     K chunks, 128-byte swizzle, 16-row boxes) -- two token stages per slot
+//   * warps 6-13: decode -- two warps per TMEM lane quadrant; thread r of
+//     quadrant q owns weight row 32q+r: for each 128-K half of a packed slot it
+//     reads 32 packed bytes and their scales from shared memory, forms 64 exact
+//     bf16 values (E2M1 -> f16x2, times the f16 scale, widened to bf16) and
+//     writes them into a TMEM A slot (lane = row, 2 K elements per column); the
+//     packed slot is released as soon as both halves are decoded
+//   * warp 1: TMEM allocator and single-thread MMA issuer:
+//     tcgen05.mma.kind::f16 with A from TMEM and B from shared memory, K = 16
+//     per instruction, N = the tile's token count rounded up to 16
+//   * warps 2-5: epilogue (alpha, activation, bf16 rounding), one TMEM lane per
+//     thread; SwiGLU pairs gate and up rows through shared memory as in W4A4
+//   * three rings: packed-weight slots (4-6), token stages (up to 12) and TMEM
+//     slots of decoded weights (4-6); each item's accumulator is split into
+//     even / odd K-step partial sums; 1-2 items in flight; every wait bounded.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "gemm_common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace w4a16 {
+constexpr int kRawK = 256;                  // K elements per packed-weight slot
+constexpr int kRawBytes = 128 * kRawK / 2;  // 16 KB: 128 rows x 128 B (128-byte swizzle)
+constexpr int kAtom = 512;
+constexpr int kSfaBytes = 4 * kAtom;        // 4 K-atoms (4 scale columns each)
+constexpr int kRawSlotBytes = kRawBytes + kSfaBytes;
+constexpr int kBK = 128;                    // K elements per token stage / decoded TMEM slot
+constexpr int kChunkRowBytes = 128;         // 64 bf16 per row per K chunk
+constexpr int kACols = kBK / 2;             // TMEM columns of one decoded A slot
+constexpr int kMaxRaw = 6;                  // packed-weight slots (released after decode)
+constexpr int kMaxStages = 12;              // token stages (released by the MMAs)
+constexpr int kMaxASlots = 6;               // TMEM slots of decoded weights
+constexpr int kMaxAcc = 2;
+constexpr int kTmemCols = 512;
+constexpr int kXchgFloats = 2 * 64 * 33;
+constexpr int kXchgBytes = (kXchgFloats * 4 + 1023) / 1024 * 1024;
+constexpr int kBarBytes = 2048;
+constexpr int kSmemBytes = 227 * 1024;
+constexpr int kRingBudget = kSmemBytes - 1024 - kBarBytes - kXchgBytes;
+constexpr int kThreads = 448;               // 14 warps
+constexpr int kDecodeWarps = 8;             // warps 6-13, two per TMEM lane quadrant
+constexpr int kBarRawFull = 0;
+constexpr int kBarRawEmpty = kBarRawFull + kMaxRaw;
+constexpr int kBarFull = kBarRawEmpty + kMaxRaw;          // token stages
+constexpr int kBarEmpty = kBarFull + kMaxStages;
+constexpr int kBarAReady = kBarEmpty + kMaxStages;        // per TMEM A slot
+constexpr int kBarAFree = kBarAReady + kMaxASlots;
+constexpr int kBarAccFull = kBarAFree + kMaxASlots;
+constexpr int kBarAccEmpty = kBarAccFull + kMaxAcc;
+constexpr int kBarItemFull = kBarAccEmpty + kMaxAcc;
+constexpr int kBarItemEmpty = kBarItemFull + kItemSlots;
+constexpr int kBarDrain = kBarItemEmpty + kItemSlots;
+constexpr int kNumBars = kBarDrain + 1;
+constexpr int kFlagsOff = 8 * kNumBars;
+constexpr int kRingOff = 768;
+static_assert(kFlagsOff + 16 <= kRingOff && kRingOff + 16 * kItemSlots <= 1024, "flag area");
+}  // namespace w4a16
+
+template <int MODE>
+__global__ void __launch_bounds__(w4a16::kThreads, 1)
+    gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const GemmArgs a) {
+  using namespace w4a16;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const Ring R{smem};
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kFlagsOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* epi_stop = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  const ItemQueue Q{reinterpret_cast<int4*>(smem + kRingOff), R.bar(kBarItemFull),
+                    R.bar(kBarItemEmpty)};
+  float* xchg = reinterpret_cast<float*>(smem + kBarBytes);
+  uint8_t* rings = smem + kBarBytes + kXchgBytes;     // 1024-aligned
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kMaxRaw; ++s) {
+      mbar_init(R.bar(kBarRawFull + s), 1);
+      mbar_init(R.bar(kBarRawEmpty + s), kDecodeWarps);
+    }
+    for (int s = 0; s < kMaxStages; ++s) {
+      mbar_init(R.bar(kBarFull + s), 1);
+      mbar_init(R.bar(kBarEmpty + s), 1);
+    }
+    for (int j = 0; j < kMaxASlots; ++j) {
+      mbar_init(R.bar(kBarAReady + j), kDecodeWarps);
+      mbar_init(R.bar(kBarAFree + j), 1);
+    }
+    for (int b = 0; b < kMaxAcc; ++b) {
+      mbar_init(R.bar(kBarAccFull + b), 1);
+      mbar_init(R.bar(kBarAccEmpty + b), 128);
+    }
+    for (int s = 0; s < kItemSlots; ++s) {
+      mbar_init(R.bar(kBarItemFull + s), 1);
+      mbar_init(R.bar(kBarItemEmpty + s), 1 + kDecodeWarps + 4);
+    }
+    mbar_init(R.bar(kBarDrain), 1);
+    *abort_flag = 0;
+    *epi_stop = 0;
+    fence_barrier_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();
+  pdl_trigger();
+
+  const int n_items = a.status[kStatusTiles] * a.m_tiles;
+  const int max_n16 = (a.status[kStatusMaxRows] + 15) & ~15;
+  const int chunk_bytes = max_n16 * kChunkRowBytes;        // one K chunk of the token tile
+  const int stage_bytes = 2 * chunk_bytes;                 // token stage: 128 K, multiple of 1024
+  // Each item accumulates into two partial sums (even and odd K steps, so
+  // consecutive MMAs do not wait on one another), added in a fixed order in the
+  // epilogue.  The split never depends on the batch, so results stay bitwise
+  // batch invariant.  nbuf items are in flight (one when tiles exceed 64 tokens).
+  const int acc_cols = (max_n16 + 31) & ~31;
+  const int nacc = 2;
+  const int acc_stride = nacc * acc_cols;                  // TMEM columns per item
+  const int nbuf = max_n16 <= 64 ? 2 : 1;                  // accumulator buffers
+  const int a_base = nbuf * acc_stride;                    // decoded A slots follow the accumulators
+  int n_aslots = (kTmemCols - a_base) / kACols;
+  if (n_aslots > kMaxASlots) n_aslots = kMaxASlots;
+  const int n_raw = max_n16 <= 64 ? kMaxRaw : 4;
+  uint8_t* raw_ring = rings;
+  uint8_t* stage_ring = rings + n_raw * kRawSlotBytes;     // multiple of 1024 past rings
+  int n_stages = (kRingBudget - n_raw * kRawSlotBytes) / stage_bytes;
+  if (n_stages > kMaxStages) n_stages = kMaxStages;
+
+  const int kraw = a.K / kRawK;                        // packed-weight slots per item
+  const int atoms = a.K / 64;
+  const size_t plane = (size_t)a.w_rows * (a.K / 16);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int last_raw[kMaxRaw], last_stg[kMaxStages];
+#pragma unroll
+      for (int s = 0; s < kMaxRaw; ++s) last_raw[s] = -1;
+#pragma unroll
+      for (int s = 0; s < kMaxStages; ++s) last_stg[s] = -1;
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      int rs = 0, stage = 0;
+      uint32_t rphase = 0, phase = 0;
+      QueuePos qp;
+      bool ok = true;
+      // Items are claimed two ahead and their table entries loaded one ahead;
+      // the raw values are only used an item later, so neither the atomic's nor
+      // the load's latency stalls the copy stream.
+      int item = blockIdx.x;
+      TileInfo cur = tile_info(a, item, n_items);        // rows == 0 past the end
+      int next = (int)gridDim.x + (item < n_items ? atomicAdd(a.item_counter, 1) : n_items);
+      int4 next_raw = tile_raw(a, next, n_items);
+      int claim = next < n_items ? atomicAdd(a.item_counter, 1) : n_items;  // raw counter value
+      while (ok) {
+        if (!queue_push(Q, qp, cur, abort_flag, a.status) || cur.rows == 0) break;
+        const int next2 = (int)gridDim.x + claim;         // claimed one item ago
+        const int4 next2_raw = tile_raw(a, next2, n_items);
+        claim = next2 < n_items ? atomicAdd(a.item_counter, 1) : n_items;
+        const TileInfo nxt = tile_decode(a, next, n_items, next_raw);  // loaded one item ago
+        const int n16 = (cur.rows + 15) & ~15;
+        const int a_row = cur.e * a.w_rows + cur.mt * 128;
+        const int b_row = cur.tt * kTileRows;
+        const uint8_t* sfa0 = a.sfa + (size_t)cur.e * plane + (size_t)cur.mt * atoms * kAtom;
+        for (int kr = 0; kr < kraw && ok; ++kr) {
+          // one packed-weight slot (256 K) ...
+          if (!wait_or_abort(R.bar(kBarRawEmpty + rs), rphase ^ 1, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* rb = raw_ring + rs * kRawSlotBytes;
+          const uint32_t rfull = R.bar(kBarRawFull + rs);
+          mbar_expect_tx(rfull, kRawSlotBytes);
+          tma_load_2d_hint(smem_u32(rb), &tmA, rfull, kr * (kRawK / 2), a_row, pol_w);
+          bulk_load(smem_u32(rb + kRawBytes), sfa0 + (size_t)(kr * 4) * kAtom, kSfaBytes, rfull);
+          last_raw[rs] = (int)rphase;
+          if (++rs == n_raw) {
+            rs = 0;
+            rphase ^= 1;
+          }
+          // ... and the two token stages (128 K each) that go with it
+          for (int h = 0; h < 2; ++h) {
+            if (!wait_or_abort(R.bar(kBarEmpty + stage), phase ^ 1, abort_flag, a.status)) {
+              ok = false;
+              break;
+            }
+            uint8_t* sb = stage_ring + stage * stage_bytes;
+            const uint32_t full = R.bar(kBarFull + stage);
+            mbar_expect_tx(full, 2 * n16 * kChunkRowBytes);
+            for (int kc = 0; kc < 2; ++kc)
+              for (int c = 0; c < n16 / 16; ++c)
+                tma_load_2d_hint(smem_u32(sb + kc * chunk_bytes + c * 16 * kChunkRowBytes), &tmB,
+                                 full, (kr * 4 + h * 2 + kc) * kChunkRowBytes, b_row + 16 * c,
+                                 pol_x);
+            last_stg[stage] = (int)phase;
+            if (++stage == n_stages) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+        }
+        cur = nxt;
+        next = next2;
+        next_raw = next2_raw;
+      }
+      if (!ok || *abort_flag) {
+        for (int s = 0; s < kMaxRaw; ++s)
+          if (last_raw[s] >= 0) mbar_wait(R.bar(kBarRawFull + s), (uint32_t)last_raw[s]);
+        for (int s = 0; s < kMaxStages; ++s)
+          if (last_stg[s] >= 0) mbar_wait(R.bar(kBarFull + s), (uint32_t)last_stg[s]);
+      }
+    }
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ decode into TMEM
+    // (warps 6..13) Packed row m: 128 B per slot, 16-byte chunk c stored at
+    // chunk c ^ (m & 7) (128-byte swizzle).  Half h of the slot (K 128h..128h+127)
+    // is chunks 4h..4h+3 and goes to one TMEM A slot; each warp of a quadrant
+    // pair decodes two of those four chunks.
+    const int q = warp & 3;
+    const int wpair = (warp - 6) >> 2;
+    const int m = q * 32 + lane;                 // weight row of this thread
+    const uint32_t lane_q = (uint32_t)(q * 32) << 16;
+    const uint32_t swz = (uint32_t)(m & 7);
+    int rs = 0, slot = 0;
+    uint32_t rphase = 0, aphase = 0;
+    QueuePos qp;
+    bool ok = true;
+    while (ok) {
+      const TileInfo cur = queue_pop_warp(Q, qp, abort_flag, a.status);
+      if (cur.rows == 0) break;
+      for (int kr = 0; kr < kraw && ok; ++kr) {
+        if (!wait_or_abort(R.bar(kBarRawFull + rs), rphase, abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t rb = smem_u32(raw_ring + rs * kRawSlotBytes);
+        for (int h = 0; h < 2; ++h) {
+          // the TMEM slot's previous MMAs are done
+          if (!wait_or_abort(R.bar(kBarAFree + slot), aphase ^ 1, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // row m's 8 block scales of this half: atoms 2h and 2h+1
+          const uint32_t s03 = lds32(rb + kRawBytes + (2 * h) * kAtom + (m & 31) * 16 + (m >> 5) * 4);
+          const uint32_t s47 =
+              lds32(rb + kRawBytes + (2 * h + 1) * kAtom + (m & 31) * 16 + (m >> 5) * 4);
+          const uint32_t acol = tmem + lane_q + a_base + slot * kACols;
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {       // 32 elements per 16-byte chunk
+            const int c = 2 * wpair + cc;        // chunk within the half
+            const uint4 raw = lds128(rb + m * 128 + (((uint32_t)(4 * h + c) ^ swz) << 4));
+            const uint32_t sw = c < 2 ? s03 : s47;
+            const uint32_t sc0 = e4m3_to_f16x2_bcast(sw >> (16 * (c & 1)));
+            const uint32_t sc1 = e4m3_to_f16x2_bcast(sw >> (16 * (c & 1) + 8));
+            uint32_t o[16];
+            decode8_bf16(raw.x, sc0, o);
+            decode8_bf16(raw.y, sc0, o + 4);
+            decode8_bf16(raw.z, sc1, o + 8);
+            decode8_bf16(raw.w, sc1, o + 12);
+            tmem_st16(acol + 16 * c, o);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(R.bar(kBarAReady + slot));
+          if (++slot == n_aslots) {
+            slot = 0;
+            aphase ^= 1;
+          }
+        }
+        // this warp has read its part of the packed slot
+        __syncwarp();
+        if (lane == 0) mbar_arrive(R.bar(kBarRawEmpty + rs));
+        if (++rs == n_raw) {
+          rs = 0;
+          rphase ^= 1;
+        }
+      }
+      ok = __all_sync(0xFFFFFFFFu, ok);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0, slot = 0, local = 0;
+      uint32_t phase = 0, aphase = 0;
+      QueuePos qp;
+      bool ok = true, issued = false;
+      const int kblocks = a.K / kBK;
+      while (ok) {
+        const TileInfo cur = queue_pop_thread(Q, qp, abort_flag, a.status);
+        if (cur.rows == 0) break;
+        const int n16 = (cur.rows + 15) & ~15;
+        const uint32_t idesc = idesc_bf16(128, n16);
+        const int buf = local % nbuf;
+        const uint32_t acc_par = ((uint32_t)(local / nbuf) & 1u) ^ 1u;
+        if (!wait_or_abort(R.bar(kBarAccEmpty + buf), acc_par, abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t acc = tmem + buf * acc_stride;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!wait_or_abort(R.bar(kBarAReady + slot), aphase, abort_flag, a.status) ||
+              !wait_or_abort(R.bar(kBarFull + stage), phase, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint8_t* sb = stage_ring + stage * stage_bytes;
+          const uint32_t acol = tmem + a_base + slot * kACols;
+#pragma unroll
+          for (int ks = 0; ks < kBK / 16; ++ks) {
+            const uint64_t bdesc = smem_desc(
+                smem_u32(sb + (ks >> 2) * chunk_bytes + (ks & 3) * 32), 16, 1024, 2);
+            const int part = nacc == 2 ? (ks & 1) : 0;
+            const uint32_t first = (kb == 0 && ks < nacc) ? 1u : 0u;
+            mma_bf16_ts(acc + part * acc_cols, acol + 8 * ks, bdesc, idesc, first ? 0u : 1u);
+          }
+          issued = true;
+          tc_commit(R.bar(kBarEmpty + stage));
+          tc_commit(R.bar(kBarAFree + slot));
+          if (++stage == n_stages) {
+            stage = 0;
+            phase ^= 1;
+          }
+          if (++slot == n_aslots) {
+            slot = 0;
+            aphase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit(R.bar(kBarAccFull + buf));
+        ++local;
+      }
+      if ((!ok || *abort_flag) && issued) {
+        tc_commit(R.bar(kBarDrain));
+        mbar_wait(R.bar(kBarDrain), 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+    int local = 0;
+    int xb = 0;
+    QueuePos qp;
+    while (true) {
+      const TileInfo cur = queue_pop_warp(Q, qp, abort_flag, a.status);
+      const int mt = cur.mt;
+      const int rows = cur.rows;
+      const int n16 = (rows + 15) & ~15;
+      const int row0 = cur.tt * kTileRows;
+      const int buf = local % nbuf;
+      const uint32_t acc_par = (uint32_t)(local / nbuf) & 1u;
+      const float alpha = rows ? a.alpha[cur.e] : 0.0f;
+      if (rows == 0 || !wait_or_abort(R.bar(kBarAccFull + buf), acc_par, abort_flag, a.status))
+        *epi_stop = 1;
+      named_bar_sync(1, 128);
+      const bool stop = *epi_stop != 0;
+      named_bar_sync(1, 128);
+      if (stop) break;
+      tc_fence_after();
+      const uint32_t acc = tmem + lane_addr + buf * acc_stride;
+      if constexpr (MODE == kFc1Swiglu) {
+        const bool gate = q < 2;
+        const int f = mt * 64 + (r & 63);
+        for (int c0 = 0; c0 < n16; c0 += 32, xb ^= 1) {
+          float v[32];
+          tmem_ld16(acc + c0, *reinterpret_cast<float(*)[16]>(v));
+          if (c0 + 16 < n16) tmem_ld16(acc + c0 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+          if (nacc == 2) {
+            float w[32];
+            tmem_ld16(acc + acc_cols + c0, *reinterpret_cast<float(*)[16]>(w));
+            if (c0 + 16 < n16)
+              tmem_ld16(acc + acc_cols + c0 + 16, *reinterpret_cast<float(*)[16]>(w + 16));
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __fadd_rn(v[j], w[j]);
+          }
+          tmem_wait_ld();
+          float* xrow = xchg + xb * (64 * 33) + (r & 63) * 33;
+          const int ncol = min(32, n16 - c0);
+          if (!gate) {
+            for (int j = 0; j < ncol; ++j) xrow[j] = __fmul_rn(v[j], alpha);
+          }
+          named_bar_sync(1, 128);
+          if (gate) {
+            for (int j = 0; j < ncol; ++j) {
+              const int col = c0 + j;
+              if (col >= rows) break;
+              const size_t p = (size_t)row0 + col;
+              const float yg = __fmul_rn(v[j], alpha);
+              const float act = __fmul_rn(__fdiv_rn(yg, __fadd_rn(1.0f, expf(-yg))), xrow[j]);
+              a.route_out[p * a.I + f] = __bfloat16_as_ushort(__float2bfloat16_rn(act));
+            }
+          }
+        }
+      } else {
+        for (int c0 = 0; c0 < n16; c0 += 16) {
+          float v[16];
+          tmem_ld16(acc + c0, v);
+          if (nacc == 2) {
+            float w[16];
+            tmem_ld16(acc + acc_cols + c0, w);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = __fadd_rn(v[j], w[j]);
+          }
+          tmem_wait_ld();
+#pragma unroll 4
+          for (int j = 0; j < 16; ++j) {
+            const int col = c0 + j;
+            if (col >= rows) break;
+            const size_t p = (size_t)row0 + col;
+            const float y = __fmul_rn(v[j], alpha);
+            if constexpr (MODE == kFc1Relu2) {
+              const float t = fmaxf(y, 0.0f);
+              a.route_out[p * a.I + mt * 128 + r] =
+                  __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(t, t)));
+            } else {
+              a.route_out[p * a.H + mt * 128 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(R.bar(kBarAccEmpty + buf));
+      ++local;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int MODE>
+static cudaError_t launch_w4a16_mode(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                     const GemmArgs& a, int grid, cudaStream_t s) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t err = cudaFuncSetAttribute(gemm_w4a16_kernel<MODE>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           w4a16::kSmemBytes);
+    if (err != cudaSuccess) return err;
+    configured = true;
+  }
+  return launch_pdl(gemm_w4a16_kernel<MODE>, dim3(grid), dim3(w4a16::kThreads),
+                    (size_t)w4a16::kSmemBytes, s, tmA, tmB, a);
+}
+
+cudaError_t launch_gemm_w4a16(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+                              int grid, cudaStream_t s) {
+  switch (a.mode) {
+    case kFc1Relu2: return launch_w4a16_mode<kFc1Relu2>(tmA, tmB, a, grid, s);
+    case kFc1Swiglu: return launch_w4a16_mode<kFc1Swiglu>(tmA, tmB, a, grid, s);
+    default: return launch_w4a16_mode<kFc2>(tmA, tmB, a, grid, s);
+  }
+}
+
+}  // namespace moe

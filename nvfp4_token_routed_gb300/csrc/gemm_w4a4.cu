@@ -10,7 +10,9 @@
 // Structure (swap-AB: weights are the M=128 operand, tokens the N operand, so a
 // decode-sized group of a few tokens does not waste a 128-row MMA):
 //   * persistent CTAs, one per SM; work item = (token tile of <= 128 rows of one
-//     expert, 128-row weight tile of that expert), items strided over CTAs
+//     expert, 128-row weight tile of that expert); each CTA starts with item
+//     blockIdx.x and then claims items from a global counter, and its roles
+//     receive them through a shared-memory ring
 //   * warp 0: TMA producer -- weight tile (128 rows x 128 B, 128-byte swizzle),
 //     token tile (16-row boxes), block-scale atoms via bulk copies
 //   * warps 6-9: scale staging -- move each stage's E4M3 scale atoms from shared
@@ -22,8 +24,9 @@
 //     instruction, N = the tile's token count rounded up to 16
 //   * warps 2-5: epilogue, one TMEM lane (= one weight row) per thread
 //   * the shared-memory stage ring is sized at run time from the largest token
-//     tile of the launch (5 stages at 128 tokens, 9 at 16); the two accumulator
-//     buffers let the epilogue of one tile overlap the MMAs of the next.
+//     tile of the launch (5 stages at 128 tokens, 9 at 16); two accumulator
+//     buffers (four when no tile exceeds 64 tokens) let the epilogue of one tile
+//     overlap the MMAs of the next ones.
 //   * every mbarrier wait is bounded; on timeout the CTA records an error flag,
 //     drains its own copies and MMAs, frees TMEM and returns.
 // SwiGLU: the stored FC1 rows interleave 64-row blocks [gate | up], so TMEM
@@ -35,6 +38,7 @@
 
 #include <cstdint>
 
+#include "gemm_common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -47,10 +51,11 @@ constexpr int kABytes = 128 * kRowBytes;    // 16 KB weight tile per stage
 constexpr int kAtom = 512;                  // 128 rows x 4 scale columns
 constexpr int kSfaBytes = 4 * kAtom;        // 4 K-atoms of the 128-row weight tile
 constexpr int kMaxStages = 12;
+constexpr int kMaxAcc = 4;                  // accumulator buffers (4 when tiles <= 64 tokens)
 constexpr int kTmemCols = 512;
 constexpr int kXchgFloats = 2 * 64 * 33;    // SwiGLU exchange: 2 buffers x 64 rows x 32 (+1 pad)
 constexpr int kXchgBytes = (kXchgFloats * 4 + 1023) / 1024 * 1024;
-constexpr int kBarBytes = 2048;             // barriers + flags, then 256 staged row scales
+constexpr int kBarBytes = 2048;             // barriers, flags, item ring; then 128 row scales
 constexpr int kSmemBytes = 227 * 1024;      // dynamic shared memory of every launch
 constexpr int kStageBudget = kSmemBytes - 1024 - kBarBytes - kXchgBytes;
 constexpr int kThreads = 320;               // 10 warps
@@ -58,52 +63,16 @@ constexpr int kThreads = 320;               // 10 warps
 constexpr int kBarFull = 0;
 constexpr int kBarEmpty = kMaxStages;
 constexpr int kBarSfReady = 2 * kMaxStages;
-constexpr int kBarAccFull = 3 * kMaxStages;       // 2 of them
-constexpr int kBarAccEmpty = 3 * kMaxStages + 2;  // 2 of them
-constexpr int kBarDrain = 3 * kMaxStages + 4;
+constexpr int kBarAccFull = 3 * kMaxStages;
+constexpr int kBarAccEmpty = kBarAccFull + kMaxAcc;
+constexpr int kBarItemFull = kBarAccEmpty + kMaxAcc;
+constexpr int kBarItemEmpty = kBarItemFull + kItemSlots;
+constexpr int kBarDrain = kBarItemEmpty + kItemSlots;
 constexpr int kNumBars = kBarDrain + 1;
-static_assert(8 * kNumBars + 16 <= 1024, "barrier area");
+constexpr int kFlagsOff = 8 * kNumBars;     // tmem slot, abort flag, epilogue stop flag
+constexpr int kRingOff = 768;               // kItemSlots int4
+static_assert(kFlagsOff + 16 <= kRingOff && kRingOff + 16 * kItemSlots <= 1024, "flag area");
 }  // namespace w4a4
-
-struct Ring {
-  uint8_t* base;  // 1024-aligned
-  __device__ uint32_t bar(int i) const { return smem_u32(base + 8 * i); }
-};
-
-// A work item: token tile tt (rows valid rows of expert e) x weight tile mt.
-// Items are numbered expert by expert, and within an expert weight-tile-major,
-// so the token tiles that share a weight tile run on neighbouring CTAs at the
-// same time and the weight tile comes from HBM once (then L2).  Loaded one item
-// ahead of use.
-struct TileInfo {
-  int e, tt, mt, rows;
-};
-__device__ __forceinline__ TileInfo tile_info(const GemmArgs& a, int item, int n_items) {
-  if (item >= n_items) return TileInfo{0, 0, 0, 0};
-  const int4 t = a.tiles[item / a.m_tiles];  // {expert, first tile, tiles, routes}
-  const int local = item - a.m_tiles * t.y;
-  const int j = local % t.z;
-  return TileInfo{t.x, t.y + j, local / t.z, min(kTileRows, t.w - kTileRows * j)};
-}
-
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                              int32_t* status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
-      *abort_flag = 1;
-      atomicOr(status + kStatusFlags, kFlagWaitTimeout);
-      return false;
-    }
-  }
-}
-
-__device__ __forceinline__ void named_bar_sync(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
 
 template <int MODE>
 __global__ void __launch_bounds__(w4a4::kThreads, 1)
@@ -114,9 +83,11 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const Ring R{smem};
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 8 * kNumBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kFlagsOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* epi_stop = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  const ItemQueue Q{reinterpret_cast<int4*>(smem + kRingOff), R.bar(kBarItemFull),
+                    R.bar(kBarItemEmpty)};
   float* s_scale = reinterpret_cast<float*>(smem + 1024);  // row scales of the current tile (128)
   float* xchg = reinterpret_cast<float*>(smem + kBarBytes);
   uint8_t* stages = smem + kBarBytes + kXchgBytes;  // 1024-aligned
@@ -129,9 +100,13 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
       mbar_init(R.bar(kBarEmpty + s), 1);
       mbar_init(R.bar(kBarSfReady + s), 4);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kMaxAcc; ++b) {
       mbar_init(R.bar(kBarAccFull + b), 1);
       mbar_init(R.bar(kBarAccEmpty + b), 128);
+    }
+    for (int s = 0; s < kItemSlots; ++s) {
+      mbar_init(R.bar(kBarItemFull + s), 1);
+      mbar_init(R.bar(kBarItemEmpty + s), 1 + 4 + 4);  // MMA, staging warps, epilogue warps
     }
     mbar_init(R.bar(kBarDrain), 1);
     *abort_flag = 0;
@@ -151,8 +126,7 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
   pdl_wait();
   pdl_trigger();
 
-  const int n_tiles = a.status[kStatusTiles];
-  const int n_items = n_tiles * a.m_tiles;
+  const int n_items = a.status[kStatusTiles] * a.m_tiles;
 
   // ---- geometry from the largest token tile (<= 128 rows) of this launch
   const int max_n16 = (a.status[kStatusMaxRows] + 15) & ~15;
@@ -160,8 +134,9 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
   const int stage_bytes = kABytes + kSfaBytes + b_bytes + 4 * kAtom;  // multiple of 1024
   const int off_sfa = kABytes, off_b = kABytes + kSfaBytes, off_sfb = off_b + b_bytes;
   const int acc_stride = (max_n16 + 31) & ~31;            // TMEM columns per accumulator
+  const int nbuf = max_n16 <= 64 ? 4 : 2;                 // accumulator buffers
   const int slot_cols = 32;                               // scale columns per stage (A 16, B 16)
-  const int sf_base = 2 * acc_stride;                     // two accumulator buffers
+  const int sf_base = nbuf * acc_stride;
   int n_stages = kStageBudget / stage_bytes;
   if (n_stages > kMaxStages) n_stages = kMaxStages;
   while (n_stages > 2 && sf_base + n_stages * slot_cols > kTmemCols) --n_stages;
@@ -170,9 +145,7 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
   const int atoms = a.K / 64;                          // scale atoms per 128-row block
   const size_t plane = (size_t)a.w_rows * (a.K / 16);  // weight scale bytes per expert
 
-  if ((int)blockIdx.x >= n_items) {
-    // no work for this CTA: fall through to the teardown
-  } else if (warp == 0) {
+  if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int last_par[kMaxStages];
@@ -182,10 +155,23 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
       const uint64_t pol_x = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
+      QueuePos qp;
       bool ok = true;
-      TileInfo cur = tile_info(a, blockIdx.x, n_items);
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const TileInfo nxt = tile_info(a, item + gridDim.x, n_items);
+      // Items are claimed two ahead and their table entries loaded one ahead;
+      // the raw values are only used an item later, so neither the atomic's nor
+      // the load's latency stalls the copy stream.
+      int item = blockIdx.x;
+      TileInfo cur = tile_info(a, item, n_items);        // rows == 0 past the end
+      int next = (int)gridDim.x + (item < n_items ? atomicAdd(a.item_counter, 1) : n_items);
+      int4 next_raw = tile_raw(a, next, n_items);
+      int claim = next < n_items ? atomicAdd(a.item_counter, 1) : n_items;  // raw counter value
+      while (ok) {
+        if (!queue_push(Q, qp, cur, abort_flag, a.status) || cur.rows == 0) break;
+        const int next2 = (int)gridDim.x + claim;         // claimed one item ago
+        const int4 next2_raw = tile_raw(a, next2, n_items);
+        claim = next2 < n_items ? atomicAdd(a.item_counter, 1) : n_items;
+        const TileInfo nxt = tile_decode(a, next, n_items, next_raw);  // loaded one item ago
+        // claim the next item now so the atomic's latency hides behind this one
         const int n16 = (cur.rows + 15) & ~15;
         const int a_row = cur.e * a.w_rows + cur.mt * 128;
         const int b_row = cur.tt * kTileRows;
@@ -213,6 +199,8 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
           }
         }
         cur = nxt;
+        next = next2;
+        next_raw = next2_raw;
       }
       if (!ok || *abort_flag) {
         // let every copy still in flight land before the CTA's shared memory goes away
@@ -227,8 +215,11 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
     const uint32_t lane_q = (uint32_t)((warp & 3) * 32) << 16;
     int stage = 0;
     uint32_t phase = 0;
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-      bool ok = true;
+    QueuePos qp;
+    bool ok = true;
+    while (ok) {
+      const TileInfo cur = queue_pop_warp(Q, qp, abort_flag, a.status);
+      if (cur.rows == 0) break;
       for (int kb = 0; kb < kblocks; ++kb) {
         if (!wait_or_abort(R.bar(kBarFull + stage), phase, abort_flag, a.status)) {
           ok = false;
@@ -250,21 +241,22 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
           phase ^= 1;
         }
       }
-      if (!ok) break;
+      ok = __all_sync(0xFFFFFFFFu, ok);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       int stage = 0, local = 0;
       uint32_t phase = 0;
+      QueuePos qp;
       bool ok = true, issued = false;
-      TileInfo cur = tile_info(a, blockIdx.x, n_items);
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++local) {
-        const TileInfo nxt = tile_info(a, item + gridDim.x, n_items);
+      while (ok) {
+        const TileInfo cur = queue_pop_thread(Q, qp, abort_flag, a.status);
+        if (cur.rows == 0) break;
         const int n16 = (cur.rows + 15) & ~15;
         const uint32_t idesc = idesc_mxf4nvf4(128, n16);
-        const int buf = local & 1;
-        const uint32_t acc_par = ((uint32_t)(local >> 1) & 1u) ^ 1u;
+        const int buf = local % nbuf;
+        const uint32_t acc_par = ((uint32_t)(local / nbuf) & 1u) ^ 1u;
         if (!wait_or_abort(R.bar(kBarAccEmpty + buf), acc_par, abort_flag, a.status)) {
           ok = false;
           break;
@@ -298,7 +290,7 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
         }
         if (!ok) break;
         tc_commit(R.bar(kBarAccFull + buf));
-        cur = nxt;
+        ++local;
       }
       if ((!ok || *abort_flag) && issued) {
         // drain the tensor-core work issued so far before TMEM is released
@@ -313,22 +305,23 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
     int local = 0;
     int xb = 0;  // exchange buffer of the next SwiGLU chunk; alternates across items too
-    TileInfo cur = tile_info(a, blockIdx.x, n_items);
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++local) {
-      const TileInfo nxt = tile_info(a, item + gridDim.x, n_items);
+    QueuePos qp;
+    while (true) {
+      const TileInfo cur = queue_pop_warp(Q, qp, abort_flag, a.status);
       const int mt = cur.mt;
       const int rows = cur.rows;
       const int n16 = (rows + 15) & ~15;
       const int row0 = cur.tt * kTileRows;
-      const int buf = local & 1;
-      const uint32_t acc_par = (uint32_t)(local >> 1) & 1u;
-      const float alpha = a.alpha[cur.e];
+      const int buf = local % nbuf;
+      const uint32_t acc_par = (uint32_t)(local / nbuf) & 1u;
+      const float alpha = rows ? a.alpha[cur.e] : 0.0f;
       // the tile's per-row scales, loaded before the wait so the latency overlaps it
       const float s_r = r < n16 ? a.row_scale[(size_t)row0 + r] : 0.0f;
       // all four epilogue warps take the same stop decision, so none is left
       // waiting alone at a named barrier; the first barrier also ends every
       // read of the previous tile's staged scales
-      if (!wait_or_abort(R.bar(kBarAccFull + buf), acc_par, abort_flag, a.status)) *epi_stop = 1;
+      if (rows == 0 || !wait_or_abort(R.bar(kBarAccFull + buf), acc_par, abort_flag, a.status))
+        *epi_stop = 1;
       named_bar_sync(1, 128);
       s_scale[r] = s_r;
       const bool stop = *epi_stop != 0;
@@ -385,7 +378,7 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(R.bar(kBarAccEmpty + buf));
-      cur = nxt;
+      ++local;
     }
   }
 

@@ -18,6 +18,7 @@ constexpr int kStatusFlags = 0;   // error bits, see below
 constexpr int kStatusTiles = 1;   // number of token tiles after the scan
 constexpr int kStatusRows = 2;    // padded rows in use after the scan
 constexpr int kStatusMaxRows = 3; // largest token tile (rows) after the scan
+constexpr int kStatusItemCtr = 4; // two work-item counters (FC1, FC2), zeroed by the scan
 constexpr int kStatusWords = 16;
 
 constexpr int kFlagBadExpertId = 1;   // an id outside [-1, E) was seen (slot ignored)
@@ -63,6 +64,7 @@ struct GemmArgs {
   const float* row_scale;  // per permuted row: s_t (FC1) or s2 (FC2)
   const int4* tiles;   // per token tile: {expert, first tile, tiles, routes} of its expert
   int32_t* status;
+  int32_t* item_counter;  // work items claimed beyond the first gridDim.x (zeroed by the scan)
   float* act_out;      // FC1: [rows][I] fp32
   int I;
   uint16_t* route_out; // FC2: [rows][H] bf16
@@ -99,5 +101,10 @@ void launch_finalize(int T, int K, int H, const int32_t* inv, const float* w, co
                      void* out, cudaStream_t s);
 cudaError_t launch_gemm_w4a4(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
                              int grid, cudaStream_t s);
+// W4A16: tmA over packed weights (128-byte boxes, 128-byte swizzle), tmB over bf16
+// token rows (128-byte boxes, 128-byte swizzle); route_out receives the bf16
+// activated rows (FC1, row stride I) or the bf16 route rows (FC2, stride H).
+cudaError_t launch_gemm_w4a16(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+                              int grid, cudaStream_t s);
 
 }  // namespace moe

@@ -124,17 +124,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2-D byte tensor [rows][row_bytes] (row stride = row_bytes), box of
-// box_rows x 128 bytes with the 128-byte swizzle.
+// box_rows x box_bytes with the 128-byte (box_bytes 128) or 64-byte (64) swizzle.
 bool make_tmap_bytes(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows,
-                     uint32_t box_rows) {
+                     uint32_t box_rows, uint32_t box_bytes = 128) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {row_bytes, rows};
   cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t box[2] = {box_bytes, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
-                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  box_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -298,11 +299,12 @@ moe_status moe_nvfp4_forward(const moe_dims* d, const moe_nvfp4_weights* w, int3
                              void* ws, size_t ws_bytes, moe_stream_t stream) {
   moe_ws_layout L;
   int sms = 0;
+  if (T > 0 && (!codes || !sf || !scale)) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!aligned(codes, 16) || !aligned(sf, 16) || !aligned(scale, 4)))
+    return MOE_ERR_MISALIGNED;
   moe_status st =
       forward_common(d, w, T, K, topk_ids, topk_w, out_bf16, ws, ws_bytes, 0, &L, &sms);
   if (st != MOE_OK || T == 0) return st;
-  if (!codes || !sf || !scale) return MOE_ERR_INVALID_ARG;
-  if (!aligned(codes, 16) || !aligned(sf, 16) || !aligned(scale, 4)) return MOE_ERR_MISALIGNED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int H = d->H, I = d->I, N1 = (int)n1_of(d);
 
@@ -336,6 +338,7 @@ moe_status moe_nvfp4_forward(const moe_dims* d, const moe_nvfp4_weights* w, int3
   g.row_scale = at<float>(ws, L.xq_scale);
   g.tiles = at<int4>(ws, L.tiles);
   g.status = at<int32_t>(ws, L.status);
+  g.item_counter = g.status + kStatusItemCtr;
   g.act_out = at<float>(ws, L.act);
   g.I = I;
   g.H = H;
@@ -358,6 +361,7 @@ moe_status moe_nvfp4_forward(const moe_dims* d, const moe_nvfp4_weights* w, int3
   g2.alpha = w->fc2_alpha;
   g2.row_scale = at<float>(ws, L.fc2q_scale);
   g2.act_out = nullptr;
+  g2.item_counter = g.status + kStatusItemCtr + 1;
   g2.route_out = at<uint16_t>(ws, L.route);
   grid = (int)std::min<int64_t>(sms, tiles_cap * g2.m_tiles);
   if (launch_gemm_w4a4(tmA2, tmB2, g2, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -374,13 +378,63 @@ moe_status moe_nvfp4_forward_w4a16(const moe_dims* d, const moe_nvfp4_weights* w
                                    size_t ws_bytes, moe_stream_t stream) {
   moe_ws_layout L;
   int sms = 0;
+  if (T > 0 && !x_bf16) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && !aligned(x_bf16, 16)) return MOE_ERR_MISALIGNED;
   moe_status st =
       forward_common(d, w, T, K, topk_ids, topk_w, out_bf16, ws, ws_bytes, 1, &L, &sms);
   if (st != MOE_OK || T == 0) return st;
-  if (!x_bf16) return MOE_ERR_INVALID_ARG;
-  if (!aligned(x_bf16, 16)) return MOE_ERR_MISALIGNED;
-  (void)stream;
-  return MOE_ERR_UNSUPPORTED_SHAPE;  // filled in by the W4A16 kernels
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int H = d->H, I = d->I, N1 = (int)n1_of(d);
+
+  CUtensorMap tmA1, tmB1, tmA2, tmB2;
+  if (!make_tmap_bytes(&tmA1, w->fc1_codes, H / 2, (uint64_t)d->E * N1, 128) ||
+      !make_tmap_bytes(&tmB1, at<uint8_t>(ws, L.x_perm), 2 * (uint64_t)H, L.rows_cap, 16) ||
+      !make_tmap_bytes(&tmA2, w->fc2_codes, I / 2, (uint64_t)d->E * H, 128) ||
+      !make_tmap_bytes(&tmB2, at<uint8_t>(ws, L.act_bf16), 2 * (uint64_t)I, L.rows_cap, 16))
+    return MOE_ERR_CUDA;
+
+  mark(0, s);
+  RouteArgs r = route_args(d, T, K, topk_ids, ws, L, 1);
+  r.xb = x_bf16;
+  r.pb = at<uint8_t>(ws, L.x_perm);
+  launch_route(r, s);
+  mark(1, s);
+
+  const int64_t tiles_cap = L.rows_cap / kTileRows;
+  GemmArgs g{};
+  g.mode = d->act == MOE_ACT_SWIGLU ? kFc1Swiglu : kFc1Relu2;
+  g.K = H;
+  g.m_tiles = N1 / 128;
+  g.w_rows = N1;
+  g.sfa = w->fc1_sf;
+  g.alpha = w->fc1_alpha;
+  g.tiles = at<int4>(ws, L.tiles);
+  g.status = at<int32_t>(ws, L.status);
+  g.item_counter = g.status + kStatusItemCtr;
+  g.route_out = at<uint16_t>(ws, L.act_bf16);
+  g.I = I;
+  g.H = H;
+  int grid = (int)std::min<int64_t>(sms, tiles_cap * g.m_tiles);
+  if (launch_gemm_w4a16(tmA1, tmB1, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
+  mark(2, s);
+  mark(3, s);
+
+  GemmArgs g2 = g;
+  g2.mode = kFc2;
+  g2.K = I;
+  g2.m_tiles = H / 128;
+  g2.w_rows = H;
+  g2.sfa = w->fc2_sf;
+  g2.alpha = w->fc2_alpha;
+  g2.item_counter = g.status + kStatusItemCtr + 1;
+  g2.route_out = at<uint16_t>(ws, L.route);
+  grid = (int)std::min<int64_t>(sms, tiles_cap * g2.m_tiles);
+  if (launch_gemm_w4a16(tmA2, tmB2, g2, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
+  mark(4, s);
+
+  launch_finalize(T, K, H, at<int32_t>(ws, L.inv), topk_w, at<uint16_t>(ws, L.route), out_bf16, s);
+  mark(5, s);
+  return cuda_status(cudaGetLastError());
 }
 
 moe_status moe_nvfp4_profile_events(void* const* events, int32_t n) {

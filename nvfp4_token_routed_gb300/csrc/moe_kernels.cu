@@ -231,6 +231,8 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(
     status[kStatusTiles] = base + ntiles;
     status[kStatusRows] = (base + ntiles) * kTileRows;
     status[kStatusMaxRows] = max_rows;
+    status[kStatusItemCtr] = 0;
+    status[kStatusItemCtr + 1] = 0;
   }
 }
 

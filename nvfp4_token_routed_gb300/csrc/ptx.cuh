@@ -190,6 +190,17 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T, bf16 inputs (A: lane = row, 2 K elements
+// per 32-bit column, lower half first).
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Copy one 512-byte scale-factor atom (32 rows x 16 bytes) from shared memory to
 // 4 TMEM columns of lanes 0..31, replicated to the four 32-lane quadrants.
 __device__ __forceinline__ void tc_cp_sf_atom(uint32_t taddr, uint64_t sdesc) {
@@ -216,6 +227,21 @@ __device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint4& v) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
                "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
+}
+// Store 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0],"
+      " {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t saddr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(saddr));
+  return v;
 }
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -248,6 +274,39 @@ __device__ __forceinline__ uint32_t cvt_e4m3(float v) {
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(out) : "f"(v), "f"(v));
   return out & 0xFFu;
 }
+// E4M3 byte -> f16x2 holding that value in both halves (exact).
+__device__ __forceinline__ uint32_t e4m3_to_f16x2_bcast(uint32_t b) {
+  uint32_t out;
+  const uint16_t pair = (uint16_t)((b & 0xFFu) | ((b & 0xFFu) << 8));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(out) : "h"(pair));
+  return out;
+}
+
+// 8 E2M1 codes (one 32-bit word, element 0 in the low nibble) times a block
+// scale given as f16x2 -> 4 bf16x2 words (element 0 in the low half).  Every
+// E2M1 x E4M3 product has at most 5 significant bits and lies in [2^-10, 2688],
+// so the f16 multiply and the f16 -> f32 -> bf16 conversions are exact.
+__device__ __forceinline__ void decode8_bf16(uint32_t w, uint32_t scale_f16x2, uint32_t* o) {
+  uint32_t h[4];
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t p;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(p) : "r"(h[i]), "r"(scale_f16x2));
+    float lo, hi;
+    asm("{\n .reg .b16 l, u;\n mov.b32 {l, u}, %2;\n cvt.f32.f16 %0, l;\n cvt.f32.f16 %1, u;\n}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(p));
+    uint32_t b;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(b) : "f"(hi), "f"(lo));
+    o[i] = b;
+  }
+}
+
 // E4M3 byte -> fp32, exact (bias 7, subnormal step 2^-9).
 __device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
   const uint32_t e = (b >> 3) & 15u, m = b & 7u;

@@ -201,3 +201,24 @@ def test_prepare_refreshes_in_place():
     oc, osf, oa = O.prepare_fc(to_np_u16(w1b))
     assert np.array_equal(w.fc1_alpha.cpu().numpy(), oa)
     assert np.array_equal(w.fc1_codes.cpu().numpy(), oc)
+
+
+def test_w4a16_batch_invariance(e64):
+    wl, w, x, ids, wts = e64
+    full = M.forward_w4a16(w, x, ids, wts)
+    g = torch.Generator().manual_seed(W.BASE_SEED + 7)
+    for T in (1, 7, 128):
+        sel = torch.randperm(wl.T, generator=g)[:T].to(DEV)
+        out = M.forward_w4a16(w, x[sel].contiguous(), ids[sel].contiguous(), wts[sel].contiguous())
+        assert torch.equal(out.view(torch.int16), full[sel].view(torch.int16)), T
+    # inside a 1024-token batch of 100x larger tokens routed to the same experts
+    tgt = slice(0, 7)
+    alone = M.forward_w4a16(w, x[tgt].contiguous(), ids[tgt].contiguous(), wts[tgt].contiguous())
+    gd = torch.Generator(device=DEV).manual_seed(W.BASE_SEED + 8)
+    big = (torch.randn(1017, wl.H, generator=gd, device=DEV) * 100.0).to(torch.bfloat16)
+    rep = torch.arange(1017, device=DEV) % 7
+    xb = torch.cat([x[tgt], big]).contiguous()
+    ib = torch.cat([ids[tgt], ids[tgt][rep]]).contiguous()
+    wb = torch.cat([wts[tgt], wts[tgt][rep]]).contiguous()
+    out = M.forward_w4a16(w, xb, ib, wb)
+    assert torch.equal(out[:7].view(torch.int16), alone.view(torch.int16))

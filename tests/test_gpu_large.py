@@ -87,3 +87,39 @@ def test_full_size_workload(name):
     del x, w1, w2, w, ws, out, codes, sf, scale
     gc.collect()
     torch.cuda.empty_cache()
+
+
+LARGE16 = {
+    "e384_T1024_w4a16": W.PAGES_E384.with_T(1024),
+    "dsv3_T128_w4a16": W.DSV3_LIKE.with_T(128),
+}
+
+
+@pytest.mark.parametrize("name", list(LARGE16))
+def test_full_size_workload_w4a16(name):
+    wl = LARGE16[name]
+    x = W.make_x(wl, device=DEV)
+    w1, w2 = W.make_weights(wl, device=DEV)
+    ids, wts = W.make_routing(wl, device=DEV)
+    w = M.prepare_weights(w1, w2, wl.act)
+    ws = M.workspace(w, wl.T, wl.K, w4a16=True)
+    out = M.forward_w4a16(w, x, ids, wts, ws=ws)
+    torch.cuda.synchronize()
+    assert M.moe_nvfp4_read_status(ws) == 0
+    idsn = ids.cpu().numpy()
+    g = np.random.default_rng(11)
+    sample = np.sort(g.choice(wl.T, size=min(4, wl.T), replace=False))
+    s_ids = idsn[sample]
+    used = np.unique(s_ids[s_ids >= 0])
+    idx = torch.as_tensor(used, device=DEV)
+    Wt = O.Weights(to_np_u16(w1.index_select(0, idx)), to_np_u16(w2.index_select(0, idx)))
+    remap = np.full(wl.E, -1, np.int32)
+    remap[used] = np.arange(used.size, dtype=np.int32)
+    sub = np.where(s_ids >= 0, remap[np.clip(s_ids, 0, None)], -1).astype(np.int32)
+    xs = to_np_u16(x)[sample]
+    res = O.forward_w4a16(Wt, xs, sub, wts.cpu().numpy()[sample], used.size, wl.H, wl.I, wl.act)
+    got = out[torch.as_tensor(sample, device=DEV)].cpu().view(torch.int16).numpy().view(np.uint16)
+    assert rel_l2(bf16_np(got), bf16_np(res["out"])) <= 1e-2
+    del x, w1, w2, w, ws, out
+    gc.collect()
+    torch.cuda.empty_cache()

@@ -164,3 +164,62 @@ def test_route_rows_and_output_rel_l2(name):
     assert rel_l2(bf16_np(route), bf16_np(o.res["route"])) <= 1e-2
     out = g.out.cpu().view(torch.int16).numpy().view(np.uint16)
     assert rel_l2(bf16_np(out), bf16_np(o.res["out"])) <= 1e-2
+
+
+# ----------------------------------------------------------------------------- W4A16
+
+class GpuRun16:
+    def __init__(self, wl, x, w1, w2, ids, wts):
+        dev = "cuda"
+        self.wl = wl
+        self.w = M.prepare_weights(w1.to(dev), w2.to(dev), wl.act)
+        self.ws = M.workspace(self.w, wl.T, wl.K, w4a16=True)
+        self.L = M.moe_nvfp4_workspace_layout(self.w.dims, wl.T, wl.K, w4a16=True)
+        self.out = M.forward_w4a16(self.w, x.to(dev), ids.to(dev), wts.to(dev), ws=self.ws)
+        torch.cuda.synchronize()
+        self.status = M.moe_nvfp4_read_status(self.ws)
+
+    def view(self, name, dtype, shape):
+        return M.ws_view(self.ws, self.L, name, dtype, shape).cpu().numpy()
+
+
+_cache16 = {}
+
+
+def _run16(name):
+    if name not in _cache16:
+        wl = CASES[name]
+        x, w1, w2, ids, wts = _inputs(wl)
+        _cache16[name] = (wl, GpuRun16(wl, x, w1, w2, ids, wts),
+                          OracleRun(wl, x, w1, w2, ids, wts, w4a16=True), x)
+    return _cache16[name]
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_w4a16_permuted_rows_and_routing(name):
+    wl, g, o, x = _run16(name)
+    assert g.status == 0
+    counts = g.view("counts", torch.int32, (wl.E,))
+    assert np.array_equal(counts, o.res["counts"])
+    rmap = _rows_map(g, o)
+    perm = g.view("perm", torch.int32, (g.L["rows_cap"],))
+    assert np.array_equal(perm[rmap], o.res["perm"])
+    xp = g.view("x_perm", torch.int16, (g.L["rows_cap"], wl.H))[rmap].view(np.uint16)
+    assert np.array_equal(xp, to_np_u16(x)[o.res["perm"] // wl.K])
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_w4a16_handoff_route_rows_and_output(name):
+    wl, g, o, x = _run16(name)
+    rmap = _rows_map(g, o)
+    act = g.view("act_bf16", torch.int16, (g.L["rows_cap"], wl.I))[rmap].view(np.uint16)
+    a_g, a_o = bf16_np(act), bf16_np(o.res["act"])
+    assert rel_l2(a_g, a_o) <= 4e-3
+    # bf16 rounding of an fp32-accumulated vs an fp64 value: one bf16 step apart
+    # at most, except where cancellation leaves a value near zero (at most 0.1%)
+    step = np.abs(a_g.view(np.int32) - a_o.view(np.int32)) >> 16
+    assert (step > 1).mean() <= 1e-3
+    route = g.view("route", torch.int16, (g.L["rows_cap"], wl.H))[rmap].view(np.uint16)
+    assert rel_l2(bf16_np(route), bf16_np(o.res["route"])) <= 1e-2
+    out = g.out.cpu().view(torch.int16).numpy().view(np.uint16)
+    assert rel_l2(bf16_np(out), bf16_np(o.res["out"])) <= 1e-2
