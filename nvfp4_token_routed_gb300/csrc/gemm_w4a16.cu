@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
   }
+  __syncwarp();  // thread 0's set-up branch rejoins its warp before the barrier
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
@@ -460,6 +461,10 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
     }
   }
 
+  // Lane 0 of warps 0 and 1 ran its role alone; the warp reconverges before
+  // the CTA barrier (bar.sync is a per-warp, aligned barrier), so TMEM is
+  // released only after every role has finished.
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

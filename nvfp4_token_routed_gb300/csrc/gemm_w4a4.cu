@@ -14,7 +14,9 @@
 //     blockIdx.x and then claims items from a global counter, and its roles
 //     receive them through a shared-memory ring
 //   * warp 0: TMA producer -- weight tile (128 rows x 128 B, 128-byte swizzle),
-//     token tile (16-row boxes), block-scale atoms via bulk copies
+//     token tile (one to three boxes of 128/64/32/16 rows), block-scale atoms
+//     via bulk copies.  Every copy costs the single issuing thread a few hundred
+//     cycles, so a stage is issued in as few copies as its shape allows.
 //   * warps 6-9: scale staging -- move each stage's E4M3 scale atoms from shared
 //     memory into that stage's TMEM scale slot with tcgen05.st, in the layout the
 //     block-scaled MMA reads (row r of a 128-row atom at lane r%32, column r/32,
@@ -29,9 +31,12 @@
 //     overlap the MMAs of the next ones.
 //   * every mbarrier wait is bounded; on timeout the CTA records an error flag,
 //     drains its own copies and MMAs, frees TMEM and returns.
+//   * the epilogue stages each chunk of up to 32 tokens in shared memory as
+//     [token][feature] rows and one thread writes them with TMA tensor stores,
+//     so global writes are whole 16-byte sectors however few tokens a tile has
 // SwiGLU: the stored FC1 rows interleave 64-row blocks [gate | up], so TMEM
-// lanes 0-63 hold gate rows and 64-127 the matching up rows; the up warps pass
-// their values to the gate warps through shared memory.
+// lanes 0-63 hold gate rows and 64-127 the matching up rows; both halves are
+// staged in shared memory and all four epilogue warps apply silu(gate) * up.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -53,11 +58,14 @@ constexpr int kSfaBytes = 4 * kAtom;        // 4 K-atoms of the 128-row weight t
 constexpr int kMaxStages = 12;
 constexpr int kMaxAcc = 4;                  // accumulator buffers (4 when tiles <= 64 tokens)
 constexpr int kTmemCols = 512;
-constexpr int kXchgFloats = 2 * 64 * 33;    // SwiGLU exchange: 2 buffers x 64 rows x 32 (+1 pad)
-constexpr int kXchgBytes = (kXchgFloats * 4 + 1023) / 1024 * 1024;
+// Epilogue output staging: two buffers, each one chunk of up to 32 tokens x the
+// tile's output features (fp32 x 128, or SwiGLU gate + up fp32 x 64 each, or
+// bf16 x 128), written to global memory by TMA stores of 16-row boxes.
+constexpr int kEpiBufBytes = 16384;
+constexpr int kEpiBytes = 2 * kEpiBufBytes;
 constexpr int kBarBytes = 2048;             // barriers, flags, item ring; then 128 row scales
 constexpr int kSmemBytes = 227 * 1024;      // dynamic shared memory of every launch
-constexpr int kStageBudget = kSmemBytes - 1024 - kBarBytes - kXchgBytes;
+constexpr int kStageBudget = kSmemBytes - 1024 - kBarBytes - kEpiBytes;
 constexpr int kThreads = 320;               // 10 warps
 // barrier indices
 constexpr int kBarFull = 0;
@@ -76,8 +84,8 @@ static_assert(kFlagsOff + 16 <= kRingOff && kRingOff + 16 * kItemSlots <= 1024, 
 
 template <int MODE>
 __global__ void __launch_bounds__(w4a4::kThreads, 1)
-    gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const GemmArgs a) {
+    gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ TokenMaps tmB,
+                     const __grid_constant__ CUtensorMap tmO, const GemmArgs a) {
   using namespace w4a4;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -89,8 +97,8 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
   const ItemQueue Q{reinterpret_cast<int4*>(smem + kRingOff), R.bar(kBarItemFull),
                     R.bar(kBarItemEmpty)};
   float* s_scale = reinterpret_cast<float*>(smem + 1024);  // row scales of the current tile (128)
-  float* xchg = reinterpret_cast<float*>(smem + kBarBytes);
-  uint8_t* stages = smem + kBarBytes + kXchgBytes;  // 1024-aligned
+  uint8_t* epi_buf = smem + kBarBytes;               // kEpiBytes, 1024-aligned
+  uint8_t* stages = smem + kBarBytes + kEpiBytes;     // 1024-aligned
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // prologue that reads nothing the previous kernel writes: barriers, TMEM
@@ -113,8 +121,10 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
     *epi_stop = 0;
     fence_barrier_init();
     prefetch_tmap(&tmA);
-    prefetch_tmap(&tmB);
+    for (int i = 0; i < 4; ++i) prefetch_tmap(&tmB.box[i]);
+    prefetch_tmap(&tmO);
   }
+  __syncwarp();  // thread 0's set-up branch rejoins its warp before the barrier
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
@@ -187,9 +197,14 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
           const uint32_t full = R.bar(kBarFull + stage);
           mbar_expect_tx(full, tx);
           tma_load_2d_hint(smem_u32(sb), &tmA, full, kb * kRowBytes, a_row, pol_w);
-          for (int c = 0; c < n16 / 16; ++c)
-            tma_load_2d_hint(smem_u32(sb + off_b + c * 16 * kRowBytes), &tmB, full,
-                             kb * kRowBytes, b_row + 16 * c, pol_x);
+          for (int r0 = 0; r0 < n16;) {
+            // largest box that still fits the rows left: n16 in 1-3 copies
+            const int rem = n16 - r0;
+            const int lg = rem >= 128 ? 3 : rem >= 64 ? 2 : rem >= 32 ? 1 : 0;
+            tma_load_2d_hint(smem_u32(sb + off_b + r0 * kRowBytes), &tmB.box[lg], full,
+                             kb * kRowBytes, b_row + r0, pol_x);
+            r0 += 16 << lg;
+          }
           bulk_load(smem_u32(sb + off_sfa), sfa0 + (size_t)(kb * 4) * kAtom, 4 * kAtom, full);
           bulk_load(smem_u32(sb + off_sfb), sfb0 + (size_t)(kb * 4) * kAtom, 4 * kAtom, full);
           last_par[stage] = (int)phase;
@@ -300,14 +315,22 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // Per item: one TMEM lane (weight row r) per thread; 32-token chunks are
+    // scaled, activated and written to a shared-memory staging buffer laid out
+    // [token][feature], which one thread stores with TMA (16-row boxes).  The
+    // next item and its per-token scales are fetched while this one runs.
     const int q = warp & 3;                  // TMEM lane quadrant of this warp
     const int r = q * 32 + lane;             // weight row within the 128-row tile
+    const int et = threadIdx.x - 64;         // epilogue thread 0..127
+    const bool issuer = et == 0;
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
     int local = 0;
-    int xb = 0;  // exchange buffer of the next SwiGLU chunk; alternates across items too
+    int eb = 0;                              // staging buffer of the next chunk
     QueuePos qp;
+    TileInfo cur = queue_pop_warp(Q, qp, abort_flag, a.status);
+    float s_r = 0.0f;
+    if (cur.rows && r < ((cur.rows + 15) & ~15)) s_r = a.row_scale[(size_t)cur.tt * kTileRows + r];
     while (true) {
-      const TileInfo cur = queue_pop_warp(Q, qp, abort_flag, a.status);
       const int mt = cur.mt;
       const int rows = cur.rows;
       const int n16 = (rows + 15) & ~15;
@@ -315,8 +338,6 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
       const int buf = local % nbuf;
       const uint32_t acc_par = (uint32_t)(local / nbuf) & 1u;
       const float alpha = rows ? a.alpha[cur.e] : 0.0f;
-      // the tile's per-row scales, loaded before the wait so the latency overlaps it
-      const float s_r = r < n16 ? a.row_scale[(size_t)row0 + r] : 0.0f;
       // all four epilogue warps take the same stop decision, so none is left
       // waiting alone at a named barrier; the first barrier also ends every
       // read of the previous tile's staged scales
@@ -327,61 +348,83 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
       const bool stop = *epi_stop != 0;
       named_bar_sync(1, 128);
       if (stop) break;
+      cur = queue_pop_warp(Q, qp, abort_flag, a.status);  // the next item (rows 0: end)
+      s_r = 0.0f;
+      if (cur.rows && r < ((cur.rows + 15) & ~15)) s_r = a.row_scale[(size_t)cur.tt * kTileRows + r];
       tc_fence_after();
       const uint32_t acc = tmem + lane_addr + buf * acc_stride;
-      if constexpr (MODE == kFc1Swiglu) {
-        // lanes 0-63: gate rows of features mt*64 + r; lanes 64-127: the matching up rows
-        const bool gate = q < 2;
-        const int f = mt * 64 + (r & 63);
-        for (int c0 = 0; c0 < n16; c0 += 32, xb ^= 1) {
-          float v[32];
-          tmem_ld16(acc + c0, *reinterpret_cast<float(*)[16]>(v));
-          if (c0 + 16 < n16) tmem_ld16(acc + c0 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
-          tmem_wait_ld();
-          float* xrow = xchg + xb * (64 * 33) + (r & 63) * 33;
-          const int ncol = min(32, n16 - c0);
-          if (!gate) {
-            for (int j = 0; j < ncol; ++j)
-              xrow[j] = __fmul_rn(__fmul_rn(v[j], alpha), s_scale[c0 + j]);
-          }
+      for (int c0 = 0; c0 < n16; c0 += 32) {
+        const int ncol = min(32, n16 - c0);
+        float v[32];
+        tmem_ld16(acc + c0, *reinterpret_cast<float(*)[16]>(v));
+        if (ncol > 16) tmem_ld16(acc + c0 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+        tmem_wait_ld();
+        if (c0 + 32 >= n16) {
+          // every TMEM read of this accumulator is done: the MMA may reuse it
+          tc_fence_before();
+          mbar_arrive(R.bar(kBarAccEmpty + buf));
+        }
+        // staging buffer eb is free once the store issued from it two chunks ago has read it
+        if (issuer) bulk_wait_group_read<1>();
+        named_bar_sync(1, 128);
+        uint8_t* ob = epi_buf + eb * kEpiBufBytes;
+        int out_x;                           // first output feature of the tile
+        uint32_t box_bytes;                  // bytes of one staged token row
+        if constexpr (MODE == kFc1Swiglu) {
+          // lanes 0-63: gate rows of features mt*64 + (r & 63); lanes 64-127: up rows
+          float* g = reinterpret_cast<float*>(ob);
+          float* u = g + 32 * 64;
+          float* dst = r < 64 ? g : u;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < ncol) dst[j * 64 + (r & 63)] = __fmul_rn(__fmul_rn(v[j], alpha), s_scale[c0 + j]);
           named_bar_sync(1, 128);
-          if (gate) {
-            for (int j = 0; j < ncol; ++j) {
-              const int col = c0 + j;
-              if (col >= rows) break;
-              const size_t p = (size_t)row0 + col;
-              const float yg = __fmul_rn(__fmul_rn(v[j], alpha), s_scale[col]);
-              const float yu = xrow[j];
-              a.act_out[p * a.I + f] = __fmul_rn(__fdiv_rn(yg, __fadd_rn(1.0f, expf(-yg))), yu);
-            }
+          const int f = et & 63;
+          for (int j = et >> 6; j < ncol; j += 2) {
+            const float yg = g[j * 64 + f];
+            const float yu = u[j * 64 + f];
+            g[j * 64 + f] = __fmul_rn(__fdiv_rn(yg, __fadd_rn(1.0f, expf(-yg))), yu);
           }
-        }
-      } else {
-        for (int c0 = 0; c0 < n16; c0 += 16) {
-          float v[16];
-          tmem_ld16(acc + c0, v);
-          tmem_wait_ld();
-#pragma unroll 4
-          for (int j = 0; j < 16; ++j) {
-            const int col = c0 + j;
-            if (col >= rows) break;
-            const size_t p = (size_t)row0 + col;
-            const float y = __fmul_rn(__fmul_rn(v[j], alpha), s_scale[col]);
-            if constexpr (MODE == kFc1Relu2) {
-              const float t = fmaxf(y, 0.0f);
-              a.act_out[p * a.I + mt * 128 + r] = __fmul_rn(t, t);
-            } else {
-              a.route_out[p * a.H + mt * 128 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+          out_x = mt * 64;
+          box_bytes = 64 * 4;
+        } else if constexpr (MODE == kFc1Relu2) {
+          float* o = reinterpret_cast<float*>(ob);
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < ncol) {
+              const float t = fmaxf(__fmul_rn(__fmul_rn(v[j], alpha), s_scale[c0 + j]), 0.0f);
+              o[j * 128 + r] = __fmul_rn(t, t);
             }
-          }
+          out_x = mt * 128;
+          box_bytes = 128 * 4;
+        } else {
+          uint16_t* o = reinterpret_cast<uint16_t*>(ob);
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < ncol)
+              o[j * 128 + r] = __bfloat16_as_ushort(
+                  __float2bfloat16_rn(__fmul_rn(__fmul_rn(v[j], alpha), s_scale[c0 + j])));
+          out_x = mt * 128;
+          box_bytes = 128 * 2;
         }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (issuer) {
+          for (int p = 0; p < ncol; p += 16)
+            tma_store_2d(&tmO, smem_u32(ob + p * box_bytes), out_x, row0 + c0 + p);
+          bulk_commit_group();
+        }
+        eb ^= 1;
       }
-      tc_fence_before();
-      mbar_arrive(R.bar(kBarAccEmpty + buf));
       ++local;
     }
+    if (issuer) bulk_wait_group<0>();  // every store has completed before the CTA ends
   }
 
+  // Lane 0 of warps 0 and 1 ran its role alone; the warp reconverges before
+  // the CTA barrier (bar.sync is a per-warp, aligned barrier), so TMEM is
+  // released only after every role has finished.
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -391,8 +434,8 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
 }
 
 template <int MODE>
-static cudaError_t launch_mode(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
-                               int grid, cudaStream_t s) {
+static cudaError_t launch_mode(const CUtensorMap& tmA, const TokenMaps& tmB, const CUtensorMap& tmO,
+                               const GemmArgs& a, int grid, cudaStream_t s) {
   static bool configured = false;  // the attribute is per function
   if (!configured) {
     cudaError_t err = cudaFuncSetAttribute(gemm_w4a4_kernel<MODE>,
@@ -402,15 +445,15 @@ static cudaError_t launch_mode(const CUtensorMap& tmA, const CUtensorMap& tmB, c
     configured = true;
   }
   return launch_pdl(gemm_w4a4_kernel<MODE>, dim3(grid), dim3(w4a4::kThreads),
-                    (size_t)w4a4::kSmemBytes, s, tmA, tmB, a);
+                    (size_t)w4a4::kSmemBytes, s, tmA, tmB, tmO, a);
 }
 
-cudaError_t launch_gemm_w4a4(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
-                             int grid, cudaStream_t s) {
+cudaError_t launch_gemm_w4a4(const CUtensorMap& tmA, const TokenMaps& tmB, const CUtensorMap& tmO,
+                             const GemmArgs& a, int grid, cudaStream_t s) {
   switch (a.mode) {
-    case kFc1Relu2: return launch_mode<kFc1Relu2>(tmA, tmB, a, grid, s);
-    case kFc1Swiglu: return launch_mode<kFc1Swiglu>(tmA, tmB, a, grid, s);
-    default: return launch_mode<kFc2>(tmA, tmB, a, grid, s);
+    case kFc1Relu2: return launch_mode<kFc1Relu2>(tmA, tmB, tmO, a, grid, s);
+    case kFc1Swiglu: return launch_mode<kFc1Swiglu>(tmA, tmB, tmO, a, grid, s);
+    default: return launch_mode<kFc2>(tmA, tmB, tmO, a, grid, s);
   }
 }
 

@@ -99,8 +99,17 @@ void launch_requant(int TK, int I, const int32_t* inv, const float* act, uint8_t
                     float* qs, cudaStream_t s);
 void launch_finalize(int T, int K, int H, const int32_t* inv, const float* w, const void* route,
                      void* out, cudaStream_t s);
-cudaError_t launch_gemm_w4a4(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
-                             int grid, cudaStream_t s);
+// Token-tile tensor maps of one operand: the same [rows][row_bytes] buffer with
+// boxes of 16, 32, 64 and 128 rows (128-byte swizzle), so that a tile of n rows
+// (a multiple of 16) arrives in at most three copies.
+struct TokenMaps {
+  CUtensorMap box[4];
+};
+// tmO: the output rows as TMA store target, 16-row boxes of the tile's features
+// (FC1 ReLU2: fp32 x 128 of act_out; SwiGLU: fp32 x 64 of act_out; FC2: bf16 x
+// 128 of route_out).
+cudaError_t launch_gemm_w4a4(const CUtensorMap& tmA, const TokenMaps& tmB, const CUtensorMap& tmO,
+                             const GemmArgs& a, int grid, cudaStream_t s);
 // W4A16: tmA over packed weights (128-byte boxes, 128-byte swizzle), tmB over bf16
 // token rows (128-byte boxes, 128-byte swizzle); route_out receives the bf16
 // activated rows (FC1, row stride I) or the bf16 route rows (FC2, stride H).

@@ -140,6 +140,30 @@ bool make_tmap_bytes(CUtensorMap* m, const void* base, uint64_t row_bytes, uint6
   return r == CUDA_SUCCESS;
 }
 
+// 2-D tensor of `elem_bytes`-byte elements [rows][inner], unswizzled boxes of
+// box_rows x box_inner elements (TMA store targets).
+bool make_tmap_out(CUtensorMap* m, const void* base, CUtensorMapDataType dtype, uint32_t elem_bytes,
+                   uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * elem_bytes};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// The four token-tile maps of a [rows][row_bytes] buffer (rows >= 128: the
+// buffer holds whole 128-row tiles).
+bool make_token_maps(TokenMaps* t, const void* base, uint64_t row_bytes, uint64_t rows) {
+  for (int i = 0; i < 4; ++i)
+    if (!make_tmap_bytes(&t->box[i], base, row_bytes, rows, 16u << i)) return false;
+  return true;
+}
+
 moe_status check_weights(const moe_nvfp4_weights* w) {
   if (!w || !w->fc1_codes || !w->fc1_sf || !w->fc1_alpha || !w->fc2_codes || !w->fc2_sf ||
       !w->fc2_alpha)
@@ -308,11 +332,17 @@ moe_status moe_nvfp4_forward(const moe_dims* d, const moe_nvfp4_weights* w, int3
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int H = d->H, I = d->I, N1 = (int)n1_of(d);
 
-  CUtensorMap tmA1, tmB1, tmA2, tmB2;
+  CUtensorMap tmA1, tmA2, tmO1, tmO2;
+  TokenMaps tmB1, tmB2;
+  const bool swiglu = d->act == MOE_ACT_SWIGLU;
   if (!make_tmap_bytes(&tmA1, w->fc1_codes, H / 2, (uint64_t)d->E * N1, 128) ||
-      !make_tmap_bytes(&tmB1, at<uint8_t>(ws, L.xq_codes), H / 2, L.rows_cap, 16) ||
+      !make_token_maps(&tmB1, at<uint8_t>(ws, L.xq_codes), H / 2, L.rows_cap) ||
+      !make_tmap_out(&tmO1, at<float>(ws, L.act), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, I,
+                     L.rows_cap, swiglu ? 64 : 128, 16) ||
       !make_tmap_bytes(&tmA2, w->fc2_codes, I / 2, (uint64_t)d->E * H, 128) ||
-      !make_tmap_bytes(&tmB2, at<uint8_t>(ws, L.fc2q_codes), I / 2, L.rows_cap, 16))
+      !make_token_maps(&tmB2, at<uint8_t>(ws, L.fc2q_codes), I / 2, L.rows_cap) ||
+      !make_tmap_out(&tmO2, at<uint16_t>(ws, L.route), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H,
+                     L.rows_cap, 128, 16))
     return MOE_ERR_CUDA;
 
   mark(0, s);
@@ -343,7 +373,7 @@ moe_status moe_nvfp4_forward(const moe_dims* d, const moe_nvfp4_weights* w, int3
   g.I = I;
   g.H = H;
   int grid = (int)std::min<int64_t>(sms, tiles_cap * g.m_tiles);
-  if (launch_gemm_w4a4(tmA1, tmB1, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gemm_w4a4(tmA1, tmB1, tmO1, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
   mark(2, s);
 
   launch_requant(T * K, I, at<int32_t>(ws, L.inv), at<float>(ws, L.act),
@@ -364,7 +394,7 @@ moe_status moe_nvfp4_forward(const moe_dims* d, const moe_nvfp4_weights* w, int3
   g2.item_counter = g.status + kStatusItemCtr + 1;
   g2.route_out = at<uint16_t>(ws, L.route);
   grid = (int)std::min<int64_t>(sms, tiles_cap * g2.m_tiles);
-  if (launch_gemm_w4a4(tmA2, tmB2, g2, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gemm_w4a4(tmA2, tmB2, tmO2, g2, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
   mark(4, s);
 
   launch_finalize(T, K, H, at<int32_t>(ws, L.inv), topk_w, at<uint16_t>(ws, L.route), out_bf16, s);

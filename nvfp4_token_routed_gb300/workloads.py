@@ -56,8 +56,13 @@ DSV3_LIKE = Workload("swiglu_H7168_I2048_E256_K8", 128, 7168, 2048, 256, 8, "swi
                      x_dist="normal", routing="uniform")
 PAGES_E384 = Workload("swiglu_H7168_I3072_E384_K6", 512, 7168, 3072, 384, 6, "swiglu",
                       x_dist="normal")
+# The squared-ReLU layer of the GB300 table in Megatron-LM PR #8262, "Performance":
+# H7168 / I2048 / 256 experts / plain top-8 over N(0,1) activations.
+PAGES_GB300_RELU2 = Workload("relu2_H7168_I2048_E256_K8", 128, 7168, 2048, 256, 8, "relu2",
+                             x_dist="normal")
 
-ALL = {w.name: w for w in [TINY_RELU2, SWIGLU_E64, MID_ZIPF, DSV3_LIKE, PAGES_E384]}
+ALL = {w.name: w for w in [TINY_RELU2, SWIGLU_E64, MID_ZIPF, DSV3_LIKE, PAGES_E384,
+                             PAGES_GB300_RELU2]}
 
 
 def _gen(seed, device):
