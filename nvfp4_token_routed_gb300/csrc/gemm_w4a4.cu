@@ -368,6 +368,17 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
         if (issuer) bulk_wait_group_read<1>();
         named_bar_sync(1, 128);
         uint8_t* ob = epi_buf + eb * kEpiBufBytes;
+        // the chunk's 32 token scales, read up front (the loops below then hold
+        // no shared-memory load behind a store)
+        float y[32];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float4 sc = reinterpret_cast<const float4*>(s_scale + c0)[k];
+          y[4 * k + 0] = __fmul_rn(__fmul_rn(v[4 * k + 0], alpha), sc.x);
+          y[4 * k + 1] = __fmul_rn(__fmul_rn(v[4 * k + 1], alpha), sc.y);
+          y[4 * k + 2] = __fmul_rn(__fmul_rn(v[4 * k + 2], alpha), sc.z);
+          y[4 * k + 3] = __fmul_rn(__fmul_rn(v[4 * k + 3], alpha), sc.w);
+        }
         int out_x;                           // first output feature of the tile
         uint32_t box_bytes;                  // bytes of one staged token row
         if constexpr (MODE == kFc1Swiglu) {
@@ -377,14 +388,22 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
           float* dst = r < 64 ? g : u;
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (j < ncol) dst[j * 64 + (r & 63)] = __fmul_rn(__fmul_rn(v[j], alpha), s_scale[c0 + j]);
+            if (j < ncol) dst[j * 64 + (r & 63)] = y[j];
           named_bar_sync(1, 128);
-          const int f = et & 63;
-          for (int j = et >> 6; j < ncol; j += 2) {
-            const float yg = g[j * 64 + f];
-            const float yu = u[j * 64 + f];
-            g[j * 64 + f] = __fmul_rn(__fdiv_rn(yg, __fadd_rn(1.0f, expf(-yg))), yu);
-          }
+          // thread et: feature et & 63 of tokens et/64, et/64 + 2, ...
+          const int f = et & 63, jb = et >> 6;
+          float yg[16], yu[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            if (jb + 2 * k < ncol) {
+              yg[k] = g[(jb + 2 * k) * 64 + f];
+              yu[k] = u[(jb + 2 * k) * 64 + f];
+            }
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            if (jb + 2 * k < ncol)
+              g[(jb + 2 * k) * 64 + f] =
+                  __fmul_rn(__fdiv_rn(yg[k], __fadd_rn(1.0f, expf(-yg[k]))), yu[k]);
           out_x = mt * 64;
           box_bytes = 64 * 4;
         } else if constexpr (MODE == kFc1Relu2) {
@@ -392,7 +411,7 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             if (j < ncol) {
-              const float t = fmaxf(__fmul_rn(__fmul_rn(v[j], alpha), s_scale[c0 + j]), 0.0f);
+              const float t = fmaxf(y[j], 0.0f);
               o[j * 128 + r] = __fmul_rn(t, t);
             }
           out_x = mt * 128;
@@ -401,9 +420,7 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
           uint16_t* o = reinterpret_cast<uint16_t*>(ob);
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (j < ncol)
-              o[j * 128 + r] = __bfloat16_as_ushort(
-                  __float2bfloat16_rn(__fmul_rn(__fmul_rn(v[j], alpha), s_scale[c0 + j])));
+            if (j < ncol) o[j * 128 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(y[j]));
           out_x = mt * 128;
           box_bytes = 128 * 2;
         }

@@ -53,13 +53,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// As mbar_try_wait, but a thread whose phase is still open is suspended in
+// hardware until it completes or about kSuspendNs pass, instead of spinning:
+// a spinning role warp takes issue slots from the warps that share its SM
+// sub-partition.
+constexpr uint32_t kSuspendNs = 100000;  // 0.1 ms per try
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(kSuspendNs)
+      : "memory");
+  return ok != 0;
+}
 // Wait for the phase with the given parity to complete.  Returns false after
 // kWaitLimitNs without completion (the caller records an error and unwinds).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity)) return true;
     if (globaltimer() - t0 > kWaitLimitNs) return false;
   }
 }
