@@ -54,6 +54,19 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
   }
 }
 
+// After an abort: wait (one shared time limit) for the phases this thread armed
+// on the stage `full` barriers, so that no copy still lands in shared memory
+// once the CTA is gone.  A phase another thread never armed does not complete;
+// the limit ends the wait, by which time this thread's own copies have landed.
+__device__ __forceinline__ void drain_stages(const Ring& R, int bar0, const int* last_par, int n) {
+  const uint64_t t0 = globaltimer();
+  for (int s = 0; s < n; ++s) {
+    if (last_par[s] < 0) continue;
+    while (!mbar_try_wait_sleep(R.bar(bar0 + s), (uint32_t)last_par[s]))
+      if (globaltimer() - t0 > kWaitLimitNs) return;
+  }
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }

@@ -13,10 +13,12 @@
 //     expert, 128-row weight tile of that expert); each CTA starts with item
 //     blockIdx.x and then claims items from a global counter, and its roles
 //     receive them through a shared-memory ring
-//   * warp 0: TMA producer -- weight tile (128 rows x 128 B, 128-byte swizzle),
-//     token tile (one to three boxes of 128/64/32/16 rows), block-scale atoms
-//     via bulk copies.  Every copy costs the single issuing thread a few hundred
-//     cycles, so a stage is issued in as few copies as its shape allows.
+//   * two TMA producers, each one thread, both filling every stage: warp 0
+//     claims the items and loads the weight tile (128 rows x 128 B, 128-byte
+//     swizzle) and its scale atoms; warp 10 loads the token tile (one to three
+//     boxes of 128/64/32/16 rows) and its scale atoms.  Each copy costs its
+//     issuing thread a few hundred cycles, so a stage is split between two
+//     threads and issued in as few copies as its shape allows.
 //   * warps 6-9: scale staging -- move each stage's E4M3 scale atoms from shared
 //     memory into that stage's TMEM scale slot with tcgen05.st, in the layout the
 //     block-scaled MMA reads (row r of a 128-row atom at lane r%32, column r/32,
@@ -66,7 +68,7 @@ constexpr int kEpiBytes = 2 * kEpiBufBytes;
 constexpr int kBarBytes = 2048;             // barriers, flags, item ring; then 128 row scales
 constexpr int kSmemBytes = 227 * 1024;      // dynamic shared memory of every launch
 constexpr int kStageBudget = kSmemBytes - 1024 - kBarBytes - kEpiBytes;
-constexpr int kThreads = 320;               // 10 warps
+constexpr int kThreads = 352;               // 11 warps
 // barrier indices
 constexpr int kBarFull = 0;
 constexpr int kBarEmpty = kMaxStages;
@@ -104,7 +106,7 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
   // prologue that reads nothing the previous kernel writes: barriers, TMEM
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMaxStages; ++s) {
-      mbar_init(R.bar(kBarFull + s), 1);
+      mbar_init(R.bar(kBarFull + s), 2);  // the weight and the token producer
       mbar_init(R.bar(kBarEmpty + s), 1);
       mbar_init(R.bar(kBarSfReady + s), 4);
     }
@@ -114,7 +116,7 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
     }
     for (int s = 0; s < kItemSlots; ++s) {
       mbar_init(R.bar(kBarItemFull + s), 1);
-      mbar_init(R.bar(kBarItemEmpty + s), 1 + 4 + 4);  // MMA, staging warps, epilogue warps
+      mbar_init(R.bar(kBarItemEmpty + s), 1 + 4 + 4 + 1);  // MMA, staging, epilogue, token producer
     }
     mbar_init(R.bar(kBarDrain), 1);
     *abort_flag = 0;
@@ -162,7 +164,6 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
 #pragma unroll
       for (int s = 0; s < kMaxStages; ++s) last_par[s] = -1;
       const uint64_t pol_w = policy_evict_first();
-      const uint64_t pol_x = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
       QueuePos qp;
@@ -182,12 +183,9 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
         claim = next2 < n_items ? atomicAdd(a.item_counter, 1) : n_items;
         const TileInfo nxt = tile_decode(a, next, n_items, next_raw);  // loaded one item ago
         // claim the next item now so the atomic's latency hides behind this one
-        const int n16 = (cur.rows + 15) & ~15;
         const int a_row = cur.e * a.w_rows + cur.mt * 128;
-        const int b_row = cur.tt * kTileRows;
         const uint8_t* sfa0 = a.sfa + (size_t)cur.e * plane + (size_t)cur.mt * atoms * kAtom;
-        const uint8_t* sfb0 = a.sfb + (size_t)cur.tt * atoms * kAtom;
-        const uint32_t tx = kABytes + kSfaBytes + n16 * kRowBytes + 4 * kAtom;
+        constexpr uint32_t tx = kABytes + kSfaBytes;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!wait_or_abort(R.bar(kBarEmpty + stage), phase ^ 1, abort_flag, a.status)) {
             ok = false;
@@ -197,16 +195,7 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
           const uint32_t full = R.bar(kBarFull + stage);
           mbar_expect_tx(full, tx);
           tma_load_2d_hint(smem_u32(sb), &tmA, full, kb * kRowBytes, a_row, pol_w);
-          for (int r0 = 0; r0 < n16;) {
-            // largest box that still fits the rows left: n16 in 1-3 copies
-            const int rem = n16 - r0;
-            const int lg = rem >= 128 ? 3 : rem >= 64 ? 2 : rem >= 32 ? 1 : 0;
-            tma_load_2d_hint(smem_u32(sb + off_b + r0 * kRowBytes), &tmB.box[lg], full,
-                             kb * kRowBytes, b_row + r0, pol_x);
-            r0 += 16 << lg;
-          }
           bulk_load(smem_u32(sb + off_sfa), sfa0 + (size_t)(kb * 4) * kAtom, 4 * kAtom, full);
-          bulk_load(smem_u32(sb + off_sfb), sfb0 + (size_t)(kb * 4) * kAtom, 4 * kAtom, full);
           last_par[stage] = (int)phase;
           if (++stage == n_stages) {
             stage = 0;
@@ -217,11 +206,51 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
         next = next2;
         next_raw = next2_raw;
       }
-      if (!ok || *abort_flag) {
-        // let every copy still in flight land before the CTA's shared memory goes away
-        for (int s = 0; s < kMaxStages; ++s)
-          if (last_par[s] >= 0) mbar_wait(R.bar(kBarFull + s), (uint32_t)last_par[s]);
+      if (!ok || *abort_flag) drain_stages(R, kBarFull, last_par, kMaxStages);
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ token producer
+    if (lane == 0) {
+      int last_par[kMaxStages];
+#pragma unroll
+      for (int s = 0; s < kMaxStages; ++s) last_par[s] = -1;
+      const uint64_t pol_x = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      QueuePos qp;
+      bool ok = true;
+      while (ok) {
+        const TileInfo cur = queue_pop_thread(Q, qp, abort_flag, a.status);
+        if (cur.rows == 0) break;
+        const int n16 = (cur.rows + 15) & ~15;
+        const int b_row = cur.tt * kTileRows;
+        const uint8_t* sfb0 = a.sfb + (size_t)cur.tt * atoms * kAtom;
+        const uint32_t tx = n16 * kRowBytes + 4 * kAtom;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!wait_or_abort(R.bar(kBarEmpty + stage), phase ^ 1, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sb = stages + stage * stage_bytes;
+          const uint32_t full = R.bar(kBarFull + stage);
+          mbar_expect_tx(full, tx);
+          for (int r0 = 0; r0 < n16;) {
+            // largest box that still fits the rows left: n16 in 1-3 copies
+            const int rem = n16 - r0;
+            const int lg = rem >= 128 ? 3 : rem >= 64 ? 2 : rem >= 32 ? 1 : 0;
+            tma_load_2d_hint(smem_u32(sb + off_b + r0 * kRowBytes), &tmB.box[lg], full,
+                             kb * kRowBytes, b_row + r0, pol_x);
+            r0 += 16 << lg;
+          }
+          bulk_load(smem_u32(sb + off_sfb), sfb0 + (size_t)(kb * 4) * kAtom, 4 * kAtom, full);
+          last_par[stage] = (int)phase;
+          if (++stage == n_stages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
       }
+      if (!ok || *abort_flag) drain_stages(R, kBarFull, last_par, kMaxStages);
     }
   } else if (warp >= 6) {
     // ------------------------------------------------------------ scale staging
@@ -403,7 +432,7 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
           for (int k = 0; k < 16; ++k)
             if (jb + 2 * k < ncol)
               g[(jb + 2 * k) * 64 + f] =
-                  __fmul_rn(__fdiv_rn(yg[k], __fadd_rn(1.0f, expf(-yg[k]))), yu[k]);
+                  __fmul_rn(__fdividef(yg[k], __fadd_rn(1.0f, __expf(-yg[k]))), yu[k]);
           out_x = mt * 64;
           box_bytes = 64 * 4;
         } else if constexpr (MODE == kFc1Relu2) {
