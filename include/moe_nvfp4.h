@@ -4,7 +4,8 @@
  *
  * Sources (web pages, cited by title and section):
  *   [MLM] Megatron-LM PR #8262 "per-token NVFP4 squared-ReLU and SwiGLU MoE via
- *         FlashInfer CuTe DSL" -- Background, What is added, How to extend.
+ *         FlashInfer CuTe DSL" -- Background, What is added, Why CuTe DSL, How
+ *         to extend, What is tested.
  *   [FI]  FlashInfer PR #5019 "CuTe DSL NVFP4 W4A16 MegaMoE" -- Tensor and
  *         numerical contract.
  *
@@ -21,9 +22,17 @@
  *   - bf16 is IEEE bfloat16 stored as 2 bytes; E2M1 codes are packed two per
  *     byte, element 2j in the low nibble; E4M3 scales are one byte each (the
  *     "fn" variant: bias 7, max 448, no infinities).
- *   - Shape limits of this version: 1 <= E <= 1024; H and I multiples of 256 in
- *     [256, 65536]; 1 <= K <= min(32, E) ([FI] Tensor and numerical contract,
+ *   - Shape limits of this version: 1 <= E <= 1024; H and I multiples of 64 in
+ *     [64, 65536]; 1 <= K <= min(32, E) ([FI] Tensor and numerical contract,
  *     supported scope); 0 <= T and T*K <= 2^26.
+ *   - Padding ([MLM] Why CuTe DSL: hidden sizes are padded to 256, e.g. 2688 ->
+ *     2816; What is tested: non-256-aligned shapes exercise the padding).  The
+ *     library stores and computes every hidden / intermediate dimension padded
+ *     with zeros to Hp = round_up(H, 256) and Ip = round_up(I, 256); N1p = Ip
+ *     (squared ReLU) or 2*Ip (SwiGLU, each half padded).  Zero codes and zero
+ *     block scales in the padding leave every real dot product unchanged, and
+ *     the layer output is [T][H].  When H and I are multiples of 256, Hp = H and
+ *     Ip = I.
  */
 #ifndef MOE_NVFP4_H_
 #define MOE_NVFP4_H_
@@ -52,7 +61,8 @@ typedef enum {
 typedef enum { MOE_ACT_RELU2 = 0, MOE_ACT_SWIGLU = 1 } moe_act;
 
 /* Layer shape.  N1 = I for squared ReLU, 2I for SwiGLU ([MLM] What is added:
- * SwiGLU's FC1 has twice FC2's input width; [FI]: gate-then-up FC1). */
+ * SwiGLU's FC1 has twice FC2's input width; [FI]: gate-then-up FC1).  H and I are
+ * the real (unpadded) sizes. */
 typedef struct {
   int32_t E; /* experts                 */
   int32_t H; /* hidden size             */
@@ -64,16 +74,17 @@ typedef struct {
  * block scales, per-expert FP32 alphas; [FI] Tensor and numerical contract:
  * scale plane of P = round_up(N,128)*round_up(D/16,4) bytes per expert, alpha
  * kept separate, never folded into scales).  All device pointers, 16-byte
- * aligned (alphas 4-byte).  Stored layouts:
- *   fc1_codes [E][N1][H/2]  K-contiguous rows.  For SwiGLU the stored row order
- *                           interleaves 64-row blocks: stored rows
- *                           [128f, 128f+64) are gate rows [64f, 64f+64) and
- *                           stored rows [128f+64, 128f+128) are up rows
- *                           I+[64f, 64f+64).  Squared ReLU keeps row order.
- *   fc1_sf    [E][N1*H/16]  swizzled: byte of (stored row r, scale column j) is
- *                           ((r/128)*(H/64) + j/4)*512 + (r%32)*16 + ((r/32)%4)*4 + j%4
+ * aligned (alphas 4-byte).  Stored layouts (padded sizes Hp, Ip, N1p above):
+ *   fc1_codes [E][N1p][Hp/2] K-contiguous rows.  For SwiGLU the stored row order
+ *                           interleaves 64-row blocks of the padded halves:
+ *                           stored rows [128f, 128f+64) are gate features
+ *                           [64f, 64f+64) and stored rows [128f+64, 128f+128)
+ *                           the matching up features.  Squared ReLU keeps row
+ *                           order.  Features >= I and columns >= H are zero.
+ *   fc1_sf    [E][N1p*Hp/16] swizzled: byte of (stored row r, scale column j) is
+ *                           ((r/128)*(Hp/64) + j/4)*512 + (r%32)*16 + ((r/32)%4)*4 + j%4
  *   fc1_alpha [E]           1 / w_scale, w_scale = 2688 / amax(expert FC1)
- *   fc2_codes [E][H][I/2], fc2_sf [E][H*I/16] (same swizzle), fc2_alpha [E]. */
+ *   fc2_codes [E][Hp][Ip/2], fc2_sf [E][Hp*Ip/16] (same swizzle), fc2_alpha [E]. */
 typedef struct {
   uint8_t* fc1_codes;
   uint8_t* fc1_sf;
@@ -102,16 +113,16 @@ typedef struct {
   size_t chunk_prefix;   /* int32[ceil(T*K/256)][E]                        */
   size_t inv;            /* int32[T*K] permuted row of route t*K+k, or -1   */
   size_t perm;           /* int32[rows_cap] route id t*K+k of a valid row   */
-  size_t xq_codes;       /* W4A4: u8[rows_cap][H/2] permuted token codes    */
-  size_t xq_sf;          /* W4A4: u8 swizzled over permuted rows, H/16 cols */
+  size_t xq_codes;       /* W4A4: u8[rows_cap][Hp/2] permuted token codes   */
+  size_t xq_sf;          /* W4A4: u8 swizzled over permuted rows, Hp/16 cols */
   size_t xq_scale;       /* W4A4: f32[rows_cap] per-row token scale        */
-  size_t act;            /* W4A4: f32[rows_cap][I] activated FC1 rows       */
-  size_t fc2q_codes;     /* W4A4: u8[rows_cap][I/2] requantized FC2 input   */
-  size_t fc2q_sf;        /* W4A4: u8 swizzled over permuted rows, I/16 cols */
+  size_t act;            /* W4A4: f32[rows_cap][Ip] activated FC1 rows      */
+  size_t fc2q_codes;     /* W4A4: u8[rows_cap][Ip/2] requantized FC2 input  */
+  size_t fc2q_sf;        /* W4A4: u8 swizzled over permuted rows, Ip/16 cols */
   size_t fc2q_scale;     /* W4A4: f32[rows_cap] FC2-input row scale s2      */
-  size_t x_perm;         /* W4A16: bf16[rows_cap][H] permuted token rows    */
-  size_t act_bf16;       /* W4A16: bf16[rows_cap][I] activated FC1 rows     */
-  size_t route;          /* bf16[rows_cap][H] per-route FC2 rows            */
+  size_t x_perm;         /* W4A16: bf16[rows_cap][Hp] permuted token rows   */
+  size_t act_bf16;       /* W4A16: bf16[rows_cap][Ip] activated FC1 rows    */
+  size_t route;          /* bf16[rows_cap][Hp] per-route FC2 rows           */
 } moe_ws_layout;
 
 /* ABI version of this header (bumped on any incompatible change). */
@@ -138,9 +149,9 @@ moe_status moe_nvfp4_prepare_weights(const moe_dims* d, const void* fc1_bf16,
 
 /* Stage 2, per-token activation quantization ([MLM] Background: one FP32 scale
  * per token; What is added: global scale = recipe constant 1/(448*6), no host
- * sync).  x_bf16 [T][H] -> codes [T][H/2], linear block scales sf [T][H/16],
- * scale [T] = amax_t / 2688 (0 for an all-zero row).  x, codes, sf 16-byte
- * aligned; scale 4-byte aligned.  T == 0 is a no-op. */
+ * sync).  x_bf16 [T][H] -> codes [T][Hp/2], linear block scales sf [T][Hp/16]
+ * (the columns past H are zero), scale [T] = amax_t / 2688 (0 for an all-zero
+ * row).  x, codes, sf 16-byte aligned; scale 4-byte aligned.  T == 0 is a no-op. */
 moe_status moe_nvfp4_quantize_tokens(int32_t T, int32_t H, const void* x_bf16, uint8_t* codes,
                                      uint8_t* sf, float* scale, moe_stream_t stream);
 

@@ -112,6 +112,11 @@ def _need_cuda(*ts):
             raise ValueError("tensors must be contiguous")
 
 
+def padded(n):
+    """The stored size of a hidden or intermediate dimension: n rounded up to 256."""
+    return (n + 255) // 256 * 256
+
+
 def dims(E, H, I, act):
     return moe_dims(E, H, I, ACT[act] if isinstance(act, str) else int(act))
 
@@ -210,11 +215,12 @@ class PreparedWeights:
         self.dims = dims(E, H, I, act)
         self.E, self.H, self.I, self.act = E, H, I, act
         sizes = moe_nvfp4_weight_sizes(self.dims)
-        N1 = 2 * I if act == "swiglu" else I
-        self.fc1_codes = torch.empty(E, N1, H // 2, dtype=torch.uint8, device=device)
+        Hp, Ip = padded(H), padded(I)
+        N1 = 2 * Ip if act == "swiglu" else Ip
+        self.fc1_codes = torch.empty(E, N1, Hp // 2, dtype=torch.uint8, device=device)
         self.fc1_sf = torch.empty(sizes[1], dtype=torch.uint8, device=device)
         self.fc1_alpha = torch.empty(E, dtype=torch.float32, device=device)
-        self.fc2_codes = torch.empty(E, H, I // 2, dtype=torch.uint8, device=device)
+        self.fc2_codes = torch.empty(E, Hp, Ip // 2, dtype=torch.uint8, device=device)
         self.fc2_sf = torch.empty(sizes[4], dtype=torch.uint8, device=device)
         self.fc2_alpha = torch.empty(E, dtype=torch.float32, device=device)
         assert self.fc1_codes.numel() == sizes[0] and self.fc2_codes.numel() == sizes[3]
@@ -240,8 +246,9 @@ def prepare_weights(fc1_bf16, fc2_bf16, act, out=None, stream=None):
 def quantize_tokens(x_bf16, stream=None):
     T, H = x_bf16.shape
     dev = x_bf16.device
-    codes = torch.empty(T, H // 2, dtype=torch.uint8, device=dev)
-    sf = torch.empty(T, H // 16, dtype=torch.uint8, device=dev)
+    Hp = padded(H)  # rows are zero-padded to Hp columns
+    codes = torch.empty(T, Hp // 2, dtype=torch.uint8, device=dev)
+    sf = torch.empty(T, Hp // 16, dtype=torch.uint8, device=dev)
     scale = torch.empty(T, dtype=torch.float32, device=dev)
     moe_nvfp4_quantize_tokens(x_bf16, codes, sf, scale, stream)
     return codes, sf, scale

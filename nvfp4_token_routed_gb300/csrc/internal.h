@@ -27,6 +27,7 @@ constexpr int kFlagWaitTimeout = 2;   // a bounded in-kernel wait gave up
 
 struct RouteArgs {
   int TK, K, E, H;
+  int Hp;  // H rounded up to 256: row length of the permuted token rows
   int w4a16;
   const int32_t* ids;
   int32_t* status;
@@ -90,15 +91,15 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-void launch_quantize_tokens(int T, int H, const void* x, uint8_t* codes, uint8_t* sf, float* scale,
-                            cudaStream_t s);
-void launch_prepare_fc(int E, int N, int D, int swiglu_I, const void* w, uint8_t* codes,
-                       uint8_t* sf, float* alpha, cudaStream_t s);
+void launch_quantize_tokens(int T, int H, int Hp, const void* x, uint8_t* codes, uint8_t* sf,
+                            float* scale, cudaStream_t s);
+void launch_prepare_fc(int E, int N, int D, int Np, int Dp, int swiglu_I, const void* w,
+                       uint8_t* codes, uint8_t* sf, float* alpha, cudaStream_t s);
 void launch_route(const RouteArgs& a, cudaStream_t s);
 void launch_requant(int TK, int I, const int32_t* inv, const float* act, uint8_t* qc, uint8_t* qsf,
                     float* qs, cudaStream_t s);
-void launch_finalize(int T, int K, int H, const int32_t* inv, const float* w, const void* route,
-                     void* out, cudaStream_t s);
+void launch_finalize(int T, int K, int H, int Hp, const int32_t* inv, const float* w,
+                     const void* route, void* out, cudaStream_t s);
 // Token-tile tensor maps of one operand: the same [rows][row_bytes] buffer with
 // boxes of 16, 32, 64 and 128 rows (128-byte swizzle), so that a tile of n rows
 // (a multiple of 16) arrives in at most three copies.

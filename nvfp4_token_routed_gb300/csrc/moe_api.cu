@@ -49,12 +49,16 @@ moe_status check_device(int* sms_out) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// H and I are multiples of 64 (whole 128x4 scale atoms); the library stores and
+// computes them zero-padded to multiples of 256 (one GEMM K stage).
+bool dim_ok(int32_t x) { return x >= 64 && x <= 65536 && x % 64 == 0; }
+int64_t pad256(int64_t x) { return (x + 255) / 256 * 256; }
+
 moe_status check_dims(const moe_dims* d) {
   if (!d) return MOE_ERR_INVALID_ARG;
   if (d->act != MOE_ACT_RELU2 && d->act != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
   if (d->E < 1 || d->E > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
-  if (d->H < 256 || d->H > 65536 || d->H % 256) return MOE_ERR_UNSUPPORTED_SHAPE;
-  if (d->I < 256 || d->I > 65536 || d->I % 256) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!dim_ok(d->H) || !dim_ok(d->I)) return MOE_ERR_UNSUPPORTED_SHAPE;
   return MOE_OK;
 }
 
@@ -65,14 +69,17 @@ moe_status check_tk(const moe_dims* d, int32_t T, int32_t K) {
   return MOE_OK;
 }
 
-int64_t n1_of(const moe_dims* d) { return d->act == MOE_ACT_SWIGLU ? 2LL * d->I : d->I; }
+int64_t hp_of(const moe_dims* d) { return pad256(d->H); }
+int64_t ip_of(const moe_dims* d) { return pad256(d->I); }
+// stored FC1 rows per expert: Ip, or 2 * Ip for SwiGLU (each half padded)
+int64_t n1p_of(const moe_dims* d) { return d->act == MOE_ACT_SWIGLU ? 2 * ip_of(d) : ip_of(d); }
 
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
 void compute_layout(const moe_dims* d, int32_t T, int32_t K, int32_t w4a16, moe_ws_layout* L) {
   std::memset(L, 0, sizeof(*L));
   const int64_t TK = (int64_t)T * K;
-  const int64_t E = d->E, H = d->H, I = d->I;
+  const int64_t E = d->E, H = hp_of(d), I = ip_of(d);
   const int64_t pad_groups = TK < E ? TK : E;
   int64_t rows = TK + pad_groups * (kTileRows - 1);
   rows = (rows + kTileRows - 1) / kTileRows * kTileRows;
@@ -222,7 +229,7 @@ moe_status moe_nvfp4_weight_sizes(const moe_dims* d, size_t bytes_out[6]) {
   moe_status st = check_dims(d);
   if (st != MOE_OK) return st;
   if (!bytes_out) return MOE_ERR_INVALID_ARG;
-  const size_t E = d->E, H = d->H, I = d->I, N1 = (size_t)n1_of(d);
+  const size_t E = d->E, H = (size_t)hp_of(d), I = (size_t)ip_of(d), N1 = (size_t)n1p_of(d);
   bytes_out[0] = E * N1 * (H / 2);
   bytes_out[1] = E * N1 * (H / 16);
   bytes_out[2] = E * sizeof(float);
@@ -242,24 +249,27 @@ moe_status moe_nvfp4_prepare_weights(const moe_dims* d, const void* fc1_bf16,
   if ((st = check_weights(out)) != MOE_OK) return st;
   if ((st = check_device(nullptr)) != MOE_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const int N1 = (int)n1_of(d);
-  launch_prepare_fc(d->E, N1, d->H, d->act == MOE_ACT_SWIGLU ? d->I : 0, fc1_bf16, out->fc1_codes,
-                    out->fc1_sf, out->fc1_alpha, s);
-  launch_prepare_fc(d->E, d->H, d->I, 0, fc2_bf16, out->fc2_codes, out->fc2_sf, out->fc2_alpha, s);
+  const bool swiglu = d->act == MOE_ACT_SWIGLU;
+  const int N1 = swiglu ? 2 * d->I : d->I;
+  launch_prepare_fc(d->E, N1, d->H, (int)n1p_of(d), (int)hp_of(d), swiglu ? d->I : 0, fc1_bf16,
+                    out->fc1_codes, out->fc1_sf, out->fc1_alpha, s);
+  launch_prepare_fc(d->E, d->H, d->I, (int)hp_of(d), (int)ip_of(d), 0, fc2_bf16, out->fc2_codes,
+                    out->fc2_sf, out->fc2_alpha, s);
   return cuda_status(cudaGetLastError());
 }
 
 moe_status moe_nvfp4_quantize_tokens(int32_t T, int32_t H, const void* x_bf16, uint8_t* codes,
                                      uint8_t* sf, float* scale, moe_stream_t stream) {
   if (T < 0) return MOE_ERR_INVALID_ARG;
-  if (H < 256 || H > 65536 || H % 256) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!dim_ok(H)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (T == 0) return MOE_OK;
   if (!x_bf16 || !codes || !sf || !scale) return MOE_ERR_INVALID_ARG;
   if (!aligned(x_bf16, 16) || !aligned(codes, 16) || !aligned(sf, 16) || !aligned(scale, 4))
     return MOE_ERR_MISALIGNED;
   moe_status st = check_device(nullptr);
   if (st != MOE_OK) return st;
-  launch_quantize_tokens(T, H, x_bf16, codes, sf, scale, reinterpret_cast<cudaStream_t>(stream));
+  launch_quantize_tokens(T, H, (int)pad256(H), x_bf16, codes, sf, scale,
+                         reinterpret_cast<cudaStream_t>(stream));
   return cuda_status(cudaGetLastError());
 }
 
@@ -304,6 +314,7 @@ static RouteArgs route_args(const moe_dims* d, int32_t T, int32_t K, const int32
   r.K = K;
   r.E = d->E;
   r.H = d->H;
+  r.Hp = (int)hp_of(d);
   r.w4a16 = w4a16;
   r.ids = ids;
   r.status = at<int32_t>(ws, L.status);
@@ -330,7 +341,8 @@ moe_status moe_nvfp4_forward(const moe_dims* d, const moe_nvfp4_weights* w, int3
       forward_common(d, w, T, K, topk_ids, topk_w, out_bf16, ws, ws_bytes, 0, &L, &sms);
   if (st != MOE_OK || T == 0) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const int H = d->H, I = d->I, N1 = (int)n1_of(d);
+  // padded sizes: stored weights, token rows and every workspace row
+  const int H = (int)hp_of(d), I = (int)ip_of(d), N1 = (int)n1p_of(d);
 
   CUtensorMap tmA1, tmA2, tmO1, tmO2;
   TokenMaps tmB1, tmB2;
@@ -397,7 +409,8 @@ moe_status moe_nvfp4_forward(const moe_dims* d, const moe_nvfp4_weights* w, int3
   if (launch_gemm_w4a4(tmA2, tmB2, tmO2, g2, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
   mark(4, s);
 
-  launch_finalize(T, K, H, at<int32_t>(ws, L.inv), topk_w, at<uint16_t>(ws, L.route), out_bf16, s);
+  launch_finalize(T, K, d->H, H, at<int32_t>(ws, L.inv), topk_w, at<uint16_t>(ws, L.route),
+                  out_bf16, s);
   mark(5, s);
   return cuda_status(cudaGetLastError());
 }
@@ -414,7 +427,8 @@ moe_status moe_nvfp4_forward_w4a16(const moe_dims* d, const moe_nvfp4_weights* w
       forward_common(d, w, T, K, topk_ids, topk_w, out_bf16, ws, ws_bytes, 1, &L, &sms);
   if (st != MOE_OK || T == 0) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const int H = d->H, I = d->I, N1 = (int)n1_of(d);
+  // padded sizes: stored weights, token rows and every workspace row
+  const int H = (int)hp_of(d), I = (int)ip_of(d), N1 = (int)n1p_of(d);
 
   CUtensorMap tmA1, tmB1, tmA2, tmB2;
   if (!make_tmap_bytes(&tmA1, w->fc1_codes, H / 2, (uint64_t)d->E * N1, 128) ||
@@ -462,7 +476,8 @@ moe_status moe_nvfp4_forward_w4a16(const moe_dims* d, const moe_nvfp4_weights* w
   if (launch_gemm_w4a16(tmA2, tmB2, g2, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
   mark(4, s);
 
-  launch_finalize(T, K, H, at<int32_t>(ws, L.inv), topk_w, at<uint16_t>(ws, L.route), out_bf16, s);
+  launch_finalize(T, K, d->H, H, at<int32_t>(ws, L.inv), topk_w, at<uint16_t>(ws, L.route),
+                  out_bf16, s);
   mark(5, s);
   return cuda_status(cudaGetLastError());
 }

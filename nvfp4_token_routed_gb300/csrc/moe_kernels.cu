@@ -16,7 +16,11 @@ namespace moe {
 // Megatron-LM PR #8262, "What is added": quantize_routed_nvfp4_input quantizes
 // activations per token with the recipe constant 1/(448*6) as global scale.
 // One warp per token: warp-shuffle amax, then one 16-element block per lane.
-__global__ void __launch_bounds__(256) quantize_tokens_kernel(int T, int H,
+// Rows of H values are written with Hp = round_up(H, 256) columns; the blocks
+// past H are zero (zero codes, zero scale bytes), which leaves every dot product
+// with a zero-padded weight row unchanged (Megatron-LM PR #8262, "Why CuTe DSL":
+// hidden sizes are padded to 256).
+__global__ void __launch_bounds__(256) quantize_tokens_kernel(int T, int H, int Hp,
                                                               const uint4* __restrict__ x,
                                                               uint8_t* __restrict__ codes,
                                                               uint8_t* __restrict__ sf,
@@ -30,13 +34,13 @@ __global__ void __launch_bounds__(256) quantize_tokens_kernel(int T, int H,
   float m = 0.0f;
   for (int i = lane; i < H / 8; i += 32) m = fmaxf(m, bf16x8_absmax(__ldg(row + i)));
   m = warp_max(m);
-  uint2* crow = reinterpret_cast<uint2*>(codes + (size_t)t * (H / 2));
-  uint8_t* srow = sf + (size_t)t * (H / 16);
+  uint2* crow = reinterpret_cast<uint2*>(codes + (size_t)t * (Hp / 2));
+  uint8_t* srow = sf + (size_t)t * (Hp / 16);
+  for (int b = (m == 0.0f ? 0 : H / 16) + lane; b < Hp / 16; b += 32) {
+    crow[b] = make_uint2(0u, 0u);
+    srow[b] = 0;
+  }
   if (m == 0.0f) {
-    for (int b = lane; b < H / 16; b += 32) {
-      crow[b] = make_uint2(0u, 0u);
-      srow[b] = 0;
-    }
     if (lane == 0) scale[t] = 0.0f;
     return;
   }
@@ -51,11 +55,11 @@ __global__ void __launch_bounds__(256) quantize_tokens_kernel(int T, int H,
   if (lane == 0) scale[t] = __fmul_rn(m, kRecipeInv);
 }
 
-void launch_quantize_tokens(int T, int H, const void* x, uint8_t* codes, uint8_t* sf, float* scale,
-                            cudaStream_t s) {
+void launch_quantize_tokens(int T, int H, int Hp, const void* x, uint8_t* codes, uint8_t* sf,
+                            float* scale, cudaStream_t s) {
   const int warps = 8;
   const int blocks = (T + warps - 1) / warps;
-  launch_pdl(quantize_tokens_kernel, dim3(blocks), dim3(warps * 32), 0, s, T, H,
+  launch_pdl(quantize_tokens_kernel, dim3(blocks), dim3(warps * 32), 0, s, T, H, Hp,
              static_cast<const uint4*>(x), codes, sf, scale);
 }
 
@@ -84,35 +88,38 @@ __global__ void __launch_bounds__(256) expert_amax_kernel(const uint4* __restric
   }
 }
 
-// Stage 2: one warp per stored row.  For SwiGLU the stored FC1 row order
-// interleaves 64-row blocks [gate f0..f0+63 | up f0..f0+63], so one 128-row
-// GEMM tile holds matching gate and up rows; canonical order is [gate; up].
+// Stage 2: one warp per stored row.  The source [N][D] rows are stored as
+// [Np][Dp] with zero rows and zero blocks past the source (padding to 256,
+// Megatron-LM PR #8262, "Why CuTe DSL"); SwiGLU pads each half separately.  For
+// SwiGLU the stored FC1 row order interleaves 64-row blocks [gate f0..f0+63 |
+// up f0..f0+63] of the padded halves, so one 128-row GEMM tile holds matching
+// gate and up rows; canonical order is [gate; up].
 __global__ void __launch_bounds__(256) quantize_weights_kernel(
-    const uint4* __restrict__ w, int E, int N, int D, int swiglu_I,
-    const uint32_t* __restrict__ amax_bits, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
-    uint64_t sf_expert_bytes) {
+    const uint4* __restrict__ w, int E, int N, int D, int Np, int Dp, int swiglu_I,
+    const uint32_t* __restrict__ amax_bits, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ sf, uint64_t sf_expert_bytes) {
   const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (gw >= (int64_t)E * N) return;
-  const int e = (int)(gw / N);
-  const int ir = (int)(gw % N);
-  int cr = ir;
+  if (gw >= (int64_t)E * Np) return;
+  const int e = (int)(gw / Np);
+  const int ir = (int)(gw % Np);
+  int src = ir < N ? ir : -1;  // source row of stored row ir, -1 for a padding row
   if (swiglu_I > 0) {
     const int b = ir >> 6;
-    cr = (b & 1) * swiglu_I + (b >> 1) * 64 + (ir & 63);
+    const int half = b & 1, f = (b >> 1) * 64 + (ir & 63);
+    src = f < swiglu_I ? half * swiglu_I + f : -1;
   }
   const float amax = __uint_as_float(amax_bits[e]);
-  const uint4* row = w + ((size_t)e * N + cr) * (D / 8);
-  uint2* crow = reinterpret_cast<uint2*>(codes + ((size_t)e * N + ir) * (D / 2));
+  uint2* crow = reinterpret_cast<uint2*>(codes + ((size_t)e * Np + ir) * (Dp / 2));
   uint8_t* plane = sf + (size_t)e * sf_expert_bytes;
-  const uint32_t c16 = (uint32_t)(D / 16);
-  if (amax == 0.0f) {
-    for (int b = lane; b < D / 16; b += 32) {
-      crow[b] = make_uint2(0u, 0u);
-      plane[sf_offset(ir, b, c16)] = 0;
-    }
-    return;
+  const uint32_t c16 = (uint32_t)(Dp / 16);
+  const int real_blocks = (amax == 0.0f || src < 0) ? 0 : D / 16;
+  for (int b = real_blocks + lane; b < Dp / 16; b += 32) {
+    crow[b] = make_uint2(0u, 0u);
+    plane[sf_offset(ir, b, c16)] = 0;
   }
+  if (real_blocks == 0) return;
+  const uint4* row = w + ((size_t)e * N + src) * (D / 8);
   const float enc = __fdiv_rn(kRecipeMax, amax);
   for (int b = lane; b < D / 16; b += 32) {
     float v[16];
@@ -131,19 +138,19 @@ __global__ void expert_alpha_kernel(int E, float* alpha) {
   alpha[e] = amax == 0.0f ? 0.0f : __fdiv_rn(1.0f, __fdiv_rn(kRecipeMax, amax));
 }
 
-void launch_prepare_fc(int E, int N, int D, int swiglu_I, const void* w, uint8_t* codes,
-                       uint8_t* sf, float* alpha, cudaStream_t s) {
+void launch_prepare_fc(int E, int N, int D, int Np, int Dp, int swiglu_I, const void* w,
+                       uint8_t* codes, uint8_t* sf, float* alpha, cudaStream_t s) {
   cudaMemsetAsync(alpha, 0, sizeof(float) * E, s);
   const int64_t vec = (int64_t)N * D / 8;
   int bx = (int)((vec + 256 * 8 - 1) / (256 * 8));
   if (bx > 64) bx = 64;
   expert_amax_kernel<<<dim3(bx, E), 256, 0, s>>>(static_cast<const uint4*>(w), vec,
                                                  reinterpret_cast<uint32_t*>(alpha));
-  const int64_t warps = (int64_t)E * N;
-  const uint64_t sf_bytes = (uint64_t)N * (D / 16);  // N % 128 == 0 and D/16 % 4 == 0: no pad
+  const int64_t warps = (int64_t)E * Np;
+  const uint64_t sf_bytes = (uint64_t)Np * (Dp / 16);  // Np % 128 == 0 and Dp/16 % 4 == 0: no pad
   quantize_weights_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(
-      static_cast<const uint4*>(w), E, N, D, swiglu_I, reinterpret_cast<const uint32_t*>(alpha),
-      codes, sf, sf_bytes);
+      static_cast<const uint4*>(w), E, N, D, Np, Dp, swiglu_I,
+      reinterpret_cast<const uint32_t*>(alpha), codes, sf, sf_bytes);
   expert_alpha_kernel<<<(E + 255) / 256, 256, 0, s>>>(E, alpha);
 }
 
@@ -265,9 +272,11 @@ __global__ void __launch_bounds__(kChunk) route_scatter_kernel(
 }
 
 // Gather: one warp per route copies its token's row to the route's permuted row.
+// W4A4 rows are already padded to Hp by the quantizer; W4A16 copies H bf16
+// values and zero-fills the Hp - H padding columns.
 template <bool kW4A16>
 __global__ void __launch_bounds__(256) gather_rows_kernel(
-    int TK, int K, int H, const int32_t* __restrict__ inv, const uint8_t* __restrict__ xc,
+    int TK, int K, int H, int Hp, const int32_t* __restrict__ inv, const uint8_t* __restrict__ xc,
     const uint8_t* __restrict__ xsf, const float* __restrict__ xs, uint8_t* __restrict__ pc,
     uint8_t* __restrict__ psf, float* __restrict__ ps, const uint4* __restrict__ xb,
     uint4* __restrict__ pb) {
@@ -281,15 +290,16 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(
   const int t = idx / K;
   if constexpr (kW4A16) {
     const uint4* src = xb + (size_t)t * (H / 8);
-    uint4* dst = pb + (size_t)p * (H / 8);
+    uint4* dst = pb + (size_t)p * (Hp / 8);
     for (int i = lane; i < H / 8; i += 32) dst[i] = __ldg(src + i);
+    for (int i = H / 8 + lane; i < Hp / 8; i += 32) dst[i] = make_uint4(0u, 0u, 0u, 0u);
   } else {
-    const uint4* src = reinterpret_cast<const uint4*>(xc + (size_t)t * (H / 2));
-    uint4* dst = reinterpret_cast<uint4*>(pc + (size_t)p * (H / 2));
-    for (int i = lane; i < H / 32; i += 32) dst[i] = __ldg(src + i);
-    const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(xsf + (size_t)t * (H / 16));
-    const uint32_t c16 = (uint32_t)(H / 16);
-    for (int g = lane; g < H / 64; g += 32)
+    const uint4* src = reinterpret_cast<const uint4*>(xc + (size_t)t * (Hp / 2));
+    uint4* dst = reinterpret_cast<uint4*>(pc + (size_t)p * (Hp / 2));
+    for (int i = lane; i < Hp / 32; i += 32) dst[i] = __ldg(src + i);
+    const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(xsf + (size_t)t * (Hp / 16));
+    const uint32_t c16 = (uint32_t)(Hp / 16);
+    for (int g = lane; g < Hp / 64; g += 32)
       *reinterpret_cast<uint32_t*>(psf + sf_offset(p, 4 * g, c16)) = __ldg(ssrc + g);
     if (lane == 0) ps[p] = xs[t];
   }
@@ -307,12 +317,12 @@ void launch_route(const RouteArgs& a, cudaStream_t s) {
              (const int32_t*)a.chunk_prefix, (const int32_t*)a.group_row0, a.inv, a.perm);
   const int gblocks = (a.TK + 7) / 8;
   if (a.w4a16)
-    launch_pdl(gather_rows_kernel<true>, dim3(gblocks), dim3(256), 0, s, a.TK, a.K, a.H,
+    launch_pdl(gather_rows_kernel<true>, dim3(gblocks), dim3(256), 0, s, a.TK, a.K, a.H, a.Hp,
                (const int32_t*)a.inv, (const uint8_t*)nullptr, (const uint8_t*)nullptr,
                (const float*)nullptr, (uint8_t*)nullptr, (uint8_t*)nullptr, (float*)nullptr,
                static_cast<const uint4*>(a.xb), static_cast<uint4*>(a.pb));
   else
-    launch_pdl(gather_rows_kernel<false>, dim3(gblocks), dim3(256), 0, s, a.TK, a.K, a.H,
+    launch_pdl(gather_rows_kernel<false>, dim3(gblocks), dim3(256), 0, s, a.TK, a.K, a.H, a.Hp,
                (const int32_t*)a.inv, a.xc, a.xsf, a.xs, a.pc, a.psf, a.ps,
                (const uint4*)nullptr, (uint4*)nullptr);
 }
@@ -380,7 +390,8 @@ void launch_requant(int TK, int I, const int32_t* inv, const float* act, uint8_t
 // token's top-k routes in a fixed order; FlashInfer PR #5019, "Tensor and
 // numerical contract": bf16 per-route terms times fp32 scores, one final bf16
 // conversion.  fp32 accumulator from +0, k ascending, one fma per term.
-__global__ void __launch_bounds__(128) finalize_kernel(int K, int H, const int32_t* __restrict__ inv,
+__global__ void __launch_bounds__(128) finalize_kernel(int K, int H, int Hp,
+                                                       const int32_t* __restrict__ inv,
                                                        const float* __restrict__ w,
                                                        const uint4* __restrict__ route,
                                                        uint4* __restrict__ out) {
@@ -404,7 +415,7 @@ __global__ void __launch_bounds__(128) finalize_kernel(int K, int H, const int32
 #pragma unroll
     for (int j = 0; j < 8; ++j) {  // issue the loads of 8 routes before using any
       const int p = k0 + j < K ? s_p[k0 + j] : -1;
-      r[j] = p >= 0 ? route[(size_t)p * (H / 8) + v] : make_uint4(0u, 0u, 0u, 0u);
+      r[j] = p >= 0 ? route[(size_t)p * (Hp / 8) + v] : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -427,11 +438,11 @@ __global__ void __launch_bounds__(128) finalize_kernel(int K, int H, const int32
   out[(size_t)t * (H / 8) + v] = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-void launch_finalize(int T, int K, int H, const int32_t* inv, const float* w, const void* route,
-                     void* out, cudaStream_t s) {
+void launch_finalize(int T, int K, int H, int Hp, const int32_t* inv, const float* w,
+                     const void* route, void* out, cudaStream_t s) {
   const int threads = 128;
   dim3 grid(T, (H / 8 + threads - 1) / threads);
-  launch_pdl(finalize_kernel, grid, dim3(threads), 0, s, K, H, inv, w,
+  launch_pdl(finalize_kernel, grid, dim3(threads), 0, s, K, H, Hp, inv, w,
              static_cast<const uint4*>(route), static_cast<uint4*>(out));
 }
 

@@ -56,6 +56,19 @@ def test_weight_sizes_match_the_contract(lib):
     assert M.moe_nvfp4_weight_sizes(d2)[0] == 8 * 512 * 128
 
 
+def test_non_aligned_shapes_are_stored_padded_to_256(lib):
+    # H = 320 -> Hp = 512, I = 192 -> Ip = 256; SwiGLU pads each half: N1p = 512
+    d = M.dims(8, 320, 192, "swiglu")
+    assert M.moe_nvfp4_weight_sizes(d) == [8 * 512 * 256, 8 * 512 * 32, 32, 8 * 512 * 128,
+                                           8 * 512 * 16, 32]
+    d = M.dims(8, 2688, 1856, "relu2")   # 2688 -> 2816 (the pages' example), 1856 -> 2048
+    assert M.moe_nvfp4_weight_sizes(d)[0] == 8 * 2048 * 1408
+    assert M.moe_nvfp4_weight_sizes(d)[3] == 8 * 2816 * 1024
+    L = M.moe_nvfp4_workspace_layout(d, 4, 2, False)
+    assert L["fc2q_codes"] - L["act"] >= L["rows_cap"] * 2048 * 4
+    assert M.padded(2688) == 2816 and M.padded(256) == 256 and M.padded(64) == 256
+
+
 @pytest.mark.parametrize("act", ["relu2", "swiglu"])
 @pytest.mark.parametrize("w4a16", [False, True])
 def test_workspace_layout_is_aligned_disjoint_and_monotone(lib, act, w4a16):
@@ -77,7 +90,8 @@ def test_workspace_layout_is_aligned_disjoint_and_monotone(lib, act, w4a16):
 
 
 def test_invalid_shapes_are_rejected_on_the_host(lib):
-    for E, H, I in [(0, 256, 256), (2000, 256, 256), (8, 200, 256), (8, 256, 300), (8, 128, 256)]:
+    for E, H, I in [(0, 256, 256), (2000, 256, 256), (8, 200, 256), (8, 256, 300), (8, 32, 256),
+                    (8, 256, 65600)]:
         d = M.dims(E, H, I, "relu2")
         assert M.moe_nvfp4_workspace_bytes(d, 4, 2) == 0
         with pytest.raises(M.MoeError) as ei:
