@@ -49,6 +49,8 @@ def parse():
     p.add_argument("--w4a16", action="store_true", help="time the BF16-activation variant")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--prep", action="store_true",
+                   help="time in-place weight re-preparation (a refit) instead of the forward")
     return p.parse_args()
 
 
@@ -437,6 +439,51 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+# Refit shape: the pages time a full requantization of 32 local experts of a
+# Nemotron-3 Super layer (hidden 2688; Megatron-LM PR #8262, "Why CuTe DSL" and
+# "Performance").  They do not print the expert intermediate size; 2048 (the
+# intermediate of the pages' GB300 table) stands in for it, squared ReLU.
+PREP_E, PREP_H, PREP_I = 32, 2688, 2048
+
+
+def run_prep(args):
+    """In-place moe_nvfp4_prepare_weights of PREP_E experts, CUDA events per call,
+    L2 flushed between calls; the bound is HBM (BF16 read + NVFP4 written)."""
+    dev = torch.device("cuda", 0)
+    wl = W.Workload("relu2_prep_E32_H2688_I2048", 1, PREP_H, PREP_I, PREP_E, 1, "relu2")
+    w1, w2 = W.make_weights(wl, device=dev)
+    w = M.prepare_weights(w1, w2, wl.act)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    for _ in range(max(3, args.warmup)):
+        M.prepare_weights(w1, w2, wl.act, out=w)
+    torch.cuda.synchronize()
+    steps = min(args.steps, 200)
+    ms = []
+    for _ in range(steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        M.prepare_weights(w1, w2, wl.act, out=w)
+        b.record()
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    mean = statistics.fmean(ms)
+    read = 2 * (w1.numel() + w2.numel()) * 2  # amax pass + quantize pass over the BF16 stacks
+    written = w.nbytes()
+    hbm, src = peaks()
+    gbs = (read + written) / (mean * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "in-place weight re-preparation (refit) of 32 experts", "value": mean * 1e3,
+        "unit": "us", "higher_is_better": False, "steps": steps, "dtype": "bf16 -> nvfp4",
+        "data": "synthetic", "config": {"workload": wl.name, "E": PREP_E, "H": PREP_H, "I": PREP_I,
+                                        "act": "relu2", "l2": "flushed between calls"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": gbs / hbm, "peak_source": src, "bytes": read + written},
+        "context": "pages: 16.7 ms for 32 Nemotron-3 Super experts with CuTe DSL (other shape)",
+    }), flush=True)
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -444,6 +491,10 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.prep:
+        if rank == 0:
+            run_prep(args)
         return
     if world > 1:
         torch.distributed.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo")
