@@ -65,7 +65,7 @@ def peaks():
 
 def kernel_hash():
     h = hashlib.sha256()
-    for f in ("gemm_w4a4.cu", "ptx.cuh", "internal.h"):
+    for f in ("gemm_w4a4.cu", "gemm_common.cuh", "ptx.cuh", "internal.h"):
         with open(os.path.join(ROOT, "nvfp4_token_routed_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
