@@ -36,6 +36,12 @@
  *       the same finalize.
  *   R8  SwiGLU: canonical FC1 rows [0,I) are the gate, [I,2I) the up projection;
  *       a = silu(g)*u with silu(g) = g/(1+exp(-g)); no clamp.
+ *   R12 Per-tensor recipe (How to extend, "Per-tensor NVFP4 x NVFP4"): the static
+ *       FC1 / FC2 input scales a1, a2 are encode scales like w_scale: token rows
+ *       and FC2-input rows are quantized with enc = a1 (resp. a2) and carry no
+ *       per-row scale; the alphas become fl(1/fl(w_scale*a1)) and
+ *       fl(1/fl(w_scale*a2)); codes and block scales of the weights are those of
+ *       the per-token recipe.
  *
  * Everything here is scalar C compiled with -ffp-contract=off so every float
  * expression is one IEEE binary32 operation.
@@ -206,6 +212,39 @@ void orc_quantize_tokens(int64_t T, int64_t H, const uint16_t* x, uint8_t* codes
     }
 }
 
+/* Per-tensor token quantization (R12): every row with the static encode scale
+ * a1 (How to extend: "nvfp4_quantize(x, a1_scale) with a fixed scale tensor",
+ * no per-token scale). */
+void orc_quantize_tokens_static(int64_t T, int64_t H, const uint16_t* x, float a1, uint8_t* codes,
+                                uint8_t* sf) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        float* row = (float*)malloc(sizeof(float) * (size_t)H);
+        for (int64_t h = 0; h < H; ++h) row[h] = bf16_to_f32(x[t * H + h]);
+        orc_quantize_row(row, H, a1, codes + t * (H / 2), sf + t * (H / 16));
+        free(row);
+    }
+}
+
+/* Per-tensor alphas (R12; How to extend: fc1_alpha = 1 / (w_scale * a1_scale),
+ * fc2_alpha = 1 / (w_scale * a2_scale)) of one FC stack w bf16 [E][N][D]:
+ * w_scale = fl(2688/amax) per expert as in weight prep; 0 for a zero expert. */
+void orc_alpha_per_tensor(int64_t E, int64_t N, int64_t D, const uint16_t* w, float a,
+                          float* alpha) {
+    for (int64_t e = 0; e < E; ++e) {
+        const uint16_t* we = w + e * N * D;
+        float amax = 0.0f;
+        for (int64_t i = 0; i < N * D; ++i) amax = fmaxf(amax, fabsf(bf16_to_f32(we[i])));
+        if (amax == 0.0f) {
+            alpha[e] = 0.0f;
+            continue;
+        }
+        float w_scale = 2688.0f / amax;
+        float prod = w_scale * a;
+        alpha[e] = 1.0f / prod;
+    }
+}
+
 /* Float-input variant used for the requantized FC2 input (R6). */
 float orc_quantize_row_per_token_f32(const float* v, int64_t D, uint8_t* codes, uint8_t* sf) {
     return quantize_row_per_token(v, D, codes, sf);
@@ -316,13 +355,15 @@ typedef struct {
 } orc_dims;
 
 /* One route of the W4A4 expert (R6), for token row (xc, xsf, xs) and expert e.
+ * a2_static > 0 selects the per-tensor FC2-input quantization (R12).
  * Writes the fp32 activated row (act_out, I values), the requantized FC2 input
  * (fc2c I/2 bytes, fc2sf I/16 bytes, returns s2 through *s2_out) and the bf16
  * route row (route_out, H values). */
 static void expert_w4a4(const orc_dims* d, int64_t e, const uint8_t* w1c, const uint8_t* w1sf,
                         const float* a1, const uint8_t* w2c, const uint8_t* w2sf, const float* a2,
-                        const uint8_t* xc, const uint8_t* xsf, float xs, float* act_out,
-                        uint8_t* fc2c, uint8_t* fc2sf, float* s2_out, uint16_t* route_out) {
+                        const uint8_t* xc, const uint8_t* xsf, float xs, float a2_static,
+                        float* act_out, uint8_t* fc2c, uint8_t* fc2sf, float* s2_out,
+                        uint16_t* route_out) {
     int64_t H = d->H, I = d->I, N1 = d->act ? 2 * I : I;
     double* y = (double*)malloc(sizeof(double) * (size_t)N1);
     double* a = (double*)malloc(sizeof(double) * (size_t)I);
@@ -336,7 +377,13 @@ static void expert_w4a4(const orc_dims* d, int64_t e, const uint8_t* w1c, const 
     }
     activation(d->act, I, y, a);
     for (int64_t n = 0; n < I; ++n) act_out[n] = (float)a[n];
-    float s2 = orc_quantize_row_per_token_f32(act_out, I, fc2c, fc2sf);
+    float s2;
+    if (a2_static > 0.0f) { /* per-tensor (R12): static encode scale, no row scale */
+        orc_quantize_row(act_out, I, a2_static, fc2c, fc2sf);
+        s2 = 1.0f;
+    } else {
+        s2 = orc_quantize_row_per_token_f32(act_out, I, fc2c, fc2sf);
+    }
     *s2_out = s2;
     const uint8_t* c2 = w2c + e * H * (I / 2);
     const uint8_t* sc2 = w2sf + e * H * (I / 16);
@@ -412,12 +459,13 @@ int orc_num_threads(void) {
  * compact permuted order q in [0, R): perm[R], act[R][I] fp32, fc2 codes
  * [R][I/2], scales [R][I/16], s2[R], route rows [R][H]; counts[E]; inv[T*K];
  * out[T][H].  Returns R. */
-int64_t orc_forward_w4a4(const orc_dims* d, int64_t T, int64_t K, const uint8_t* w1c,
-                         const uint8_t* w1sf, const float* a1, const uint8_t* w2c,
-                         const uint8_t* w2sf, const float* a2, const uint8_t* xc,
-                         const uint8_t* xsf, const float* xs, const int32_t* ids, const float* w,
-                         int32_t* counts, int32_t* perm, int32_t* inv, float* act, uint8_t* fc2c,
-                         uint8_t* fc2sf, float* s2, uint16_t* route, uint16_t* out) {
+static int64_t forward_w4a4(const orc_dims* d, int64_t T, int64_t K, const uint8_t* w1c,
+                            const uint8_t* w1sf, const float* a1, const uint8_t* w2c,
+                            const uint8_t* w2sf, const float* a2, const uint8_t* xc,
+                            const uint8_t* xsf, const float* xs, float a2_static,
+                            const int32_t* ids, const float* w, int32_t* counts, int32_t* perm,
+                            int32_t* inv, float* act, uint8_t* fc2c, uint8_t* fc2sf, float* s2,
+                            uint16_t* route, uint16_t* out) {
     int64_t H = d->H, I = d->I;
     int64_t R = orc_route(T, K, d->E, ids, counts, perm, inv);
 #pragma omp parallel for schedule(dynamic, 1)
@@ -425,10 +473,37 @@ int64_t orc_forward_w4a4(const orc_dims* d, int64_t T, int64_t K, const uint8_t*
         int64_t t = perm[q] / K;
         int64_t e = ids[perm[q]];
         expert_w4a4(d, e, w1c, w1sf, a1, w2c, w2sf, a2, xc + t * (H / 2), xsf + t * (H / 16),
-                    xs[t], act + q * I, fc2c + q * (I / 2), fc2sf + q * (I / 16), s2 + q,
-                    route + q * H);
+                    xs ? xs[t] : 1.0f, a2_static, act + q * I, fc2c + q * (I / 2),
+                    fc2sf + q * (I / 16), s2 + q, route + q * H);
     }
     orc_finalize(T, K, H, route, inv, w, out);
+    return R;
+}
+
+int64_t orc_forward_w4a4(const orc_dims* d, int64_t T, int64_t K, const uint8_t* w1c,
+                         const uint8_t* w1sf, const float* a1, const uint8_t* w2c,
+                         const uint8_t* w2sf, const float* a2, const uint8_t* xc,
+                         const uint8_t* xsf, const float* xs, const int32_t* ids, const float* w,
+                         int32_t* counts, int32_t* perm, int32_t* inv, float* act, uint8_t* fc2c,
+                         uint8_t* fc2sf, float* s2, uint16_t* route, uint16_t* out) {
+    return forward_w4a4(d, T, K, w1c, w1sf, a1, w2c, w2sf, a2, xc, xsf, xs, 0.0f, ids, w, counts,
+                        perm, inv, act, fc2c, fc2sf, s2, route, out);
+}
+
+/* Per-tensor W4A4 forward (R12): tokens quantized with the static scale a1
+ * (orc_quantize_tokens_static), alphas from orc_alpha_per_tensor, FC2 input
+ * quantized with the static scale a2; no per-row scales. */
+int64_t orc_forward_w4a4_per_tensor(const orc_dims* d, int64_t T, int64_t K, const uint8_t* w1c,
+                                    const uint8_t* w1sf, const float* a1, const uint8_t* w2c,
+                                    const uint8_t* w2sf, const float* a2, const uint8_t* xc,
+                                    const uint8_t* xsf, float a2_static, const int32_t* ids,
+                                    const float* w, int32_t* counts, int32_t* perm, int32_t* inv,
+                                    float* act, uint8_t* fc2c, uint8_t* fc2sf, uint16_t* route,
+                                    uint16_t* out) {
+    float* s2 = (float*)malloc(sizeof(float) * (size_t)(T * K > 0 ? T * K : 1));
+    int64_t R = forward_w4a4(d, T, K, w1c, w1sf, a1, w2c, w2sf, a2, xc, xsf, NULL, a2_static, ids,
+                             w, counts, perm, inv, act, fc2c, fc2sf, s2, route, out);
+    free(s2);
     return R;
 }
 
@@ -472,7 +547,7 @@ void orc_dense_w4a4(const orc_dims* d, int64_t T, int64_t K, const uint8_t* w1c,
             if (!used) continue;
             float s2;
             expert_w4a4(d, e, w1c, w1sf, a1, w2c, w2sf, a2, xc + t * (H / 2), xsf + t * (H / 16),
-                        xs[t], act, c, s, &s2, r + e * H);
+                        xs[t], 0.0f, act, c, s, &s2, r + e * H);
             have[e] = 1;
         }
         for (int64_t k = 0; k < K; ++k) {

@@ -45,13 +45,15 @@ def lib():
         L.orc_route.restype = C.c_int64
         L.orc_forward_w4a4.restype = C.c_int64
         L.orc_forward_w4a16.restype = C.c_int64
+        L.orc_forward_w4a4_per_tensor.restype = C.c_int64
         L.orc_num_threads.restype = C.c_int
         L.orc_quantize_row_per_token_f32.restype = C.c_float
         for name in ["orc_e2m1_encode_n", "orc_e4m3_encode_n", "orc_e4m3_decode_n",
                      "orc_f64_to_bf16_n", "orc_sf_to_swizzled", "orc_quantize_row",
                      "orc_quantize_tokens", "orc_prepare_fc", "orc_finalize", "orc_dense_w4a4",
                      "orc_route", "orc_forward_w4a4", "orc_forward_w4a16",
-                     "orc_quantize_row_per_token_f32"]:
+                     "orc_quantize_row_per_token_f32", "orc_quantize_tokens_static",
+                     "orc_alpha_per_tensor", "orc_forward_w4a4_per_tensor"]:
             getattr(L, name).argtypes = None
     return _lib
 
@@ -137,6 +139,27 @@ def quantize_tokens(x_bf16):
     s = np.empty(T, np.float32)
     lib().orc_quantize_tokens(C.c_int64(T), C.c_int64(H), _p(x), _p(codes), _p(sf), _p(s))
     return codes, sf, s
+
+
+def quantize_tokens_static(x_bf16, a1):
+    """Per-tensor recipe: every row quantized with the static encode scale a1 (R12)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    T, H = x.shape
+    codes = np.empty((T, H // 2), np.uint8)
+    sf = np.empty((T, H // 16), np.uint8)
+    lib().orc_quantize_tokens_static(C.c_int64(T), C.c_int64(H), _p(x), C.c_float(a1), _p(codes),
+                                     _p(sf))
+    return codes, sf
+
+
+def alpha_per_tensor(w_bf16, a):
+    """Per-tensor alphas fl(1/fl(w_scale*a)) of one BF16 FC stack [E][N][D] (R12)."""
+    w = np.ascontiguousarray(w_bf16, dtype=np.uint16)
+    E, N, D = w.shape
+    alpha = np.empty(E, np.float32)
+    lib().orc_alpha_per_tensor(C.c_int64(E), C.c_int64(N), C.c_int64(D), _p(w), C.c_float(a),
+                               _p(alpha))
+    return alpha
 
 
 def prepare_fc(w_bf16):
@@ -225,6 +248,43 @@ def forward_w4a4(W, xc, xsf, xs, ids, w, E, H, I, act):
                                _p(act_rows), _p(fc2c), _p(fc2sf), _p(s2), _p(routes), _p(out))
     return dict(R=R, counts=counts, perm=perm[:R].copy(), inv=inv, act=act_rows[:R],
                 fc2c=fc2c[:R], fc2sf=fc2sf[:R], s2=s2[:R], route=routes[:R], out=out)
+
+
+def forward_w4a4_per_tensor(W, xc, xsf, a2_static, ids, w, E, H, I, act):
+    """Per-tensor W4A4 forward (R12): W holds the per-tensor alphas (a1/a2 folded),
+    tokens come from quantize_tokens_static, the FC2 input uses a2_static."""
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    T, K = ids.shape
+    TK = T * K
+    d = _dims(E, H, I, act)
+    counts = np.empty(E, np.int32)
+    perm = np.empty(TK, np.int32)
+    inv = np.empty(TK, np.int32)
+    act_rows = np.empty((TK, I), np.float32)
+    fc2c = np.empty((TK, I // 2), np.uint8)
+    fc2sf = np.empty((TK, I // 16), np.uint8)
+    routes = np.empty((TK, H), np.uint16)
+    out = np.empty((T, H), np.uint16)
+    xc = np.ascontiguousarray(xc, np.uint8)
+    xsf = np.ascontiguousarray(xsf, np.uint8)
+    R = lib().orc_forward_w4a4_per_tensor(
+        C.byref(d), C.c_int64(T), C.c_int64(K), _p(W.w1c), _p(W.w1sf), _p(W.a1), _p(W.w2c),
+        _p(W.w2sf), _p(W.a2), _p(xc), _p(xsf), C.c_float(a2_static), _p(ids), _p(w), _p(counts),
+        _p(perm), _p(inv), _p(act_rows), _p(fc2c), _p(fc2sf), _p(routes), _p(out))
+    return dict(R=R, counts=counts, perm=perm[:R].copy(), inv=inv, act=act_rows[:R],
+                fc2c=fc2c[:R], fc2sf=fc2sf[:R], route=routes[:R], out=out)
+
+
+class WeightsPerTensor:
+    """Oracle-prepared weights of the per-tensor recipe: per-token codes and
+    scales, alphas with the static input scales folded in (R12)."""
+
+    def __init__(self, w1_bf16, w2_bf16, a1, a2):
+        self.w1c, self.w1sf, _ = prepare_fc(w1_bf16)
+        self.w2c, self.w2sf, _ = prepare_fc(w2_bf16)
+        self.a1 = alpha_per_tensor(w1_bf16, a1)
+        self.a2 = alpha_per_tensor(w2_bf16, a2)
 
 
 def forward_w4a16(W, x_bf16, ids, w, E, H, I, act):

@@ -313,3 +313,82 @@ def test_relu2_output_scales_by_four_to_the_m():
     r1 = O.forward_w4a4(Wt, *O.quantize_tokens(W.bf16_bits(x2)), ids, wts, wl.E, wl.H, wl.I, "relu2")
     assert np.array_equal(O.bf16_to_f32(r1["route"]), O.bf16_to_f32(r0["route"]) * 16.0)
     assert np.array_equal(r1["fc2c"], r0["fc2c"]) and np.array_equal(r1["fc2sf"], r0["fc2sf"])
+
+
+# --------------------------------------------------------------------------- per-tensor recipe
+# Megatron-LM PR #8262, "How to extend", "Per-tensor NVFP4 x NVFP4": static FC1 /
+# FC2 input scales (encode scales, like w_scale), folded into the alphas.
+
+def test_static_quantization_with_the_tokens_own_scale_is_per_token():
+    """A row quantized with the static scale fl(2688/amax) of its own amax gets
+    exactly the per-token codes and block scales."""
+    x = W.make_x(W.TINY_RELU2)
+    bits = W.bf16_bits(x)
+    c_pt, f_pt, s_pt = O.quantize_tokens(bits)
+    for t in range(4):
+        amax = np.float32(np.abs(x[t].float().numpy()).max())
+        a1 = np.float32(np.float32(2688.0) / amax)
+        c, f = O.quantize_tokens_static(bits[t:t + 1], a1)
+        assert np.array_equal(c[0], c_pt[t]) and np.array_equal(f[0], f_pt[t])
+
+
+def test_static_quantization_scales_against_the_values():
+    """x * 2^m quantized with a1 * 2^-m gives the same codes and block scales."""
+    x = W.make_x(W.TINY_RELU2)
+    c0, f0 = O.quantize_tokens_static(W.bf16_bits(x), np.float32(64.0))
+    for m in (-3, 2, 5):
+        xs = (x.float() * 2.0 ** m).to(torch.bfloat16)
+        c1, f1 = O.quantize_tokens_static(W.bf16_bits(xs), np.float32(64.0 * 2.0 ** -m))
+        assert np.array_equal(c0, c1) and np.array_equal(f0, f1)
+
+
+def test_static_quantization_saturates():
+    """A static scale far too large clips: block scales 448 (0x7E) and codes +-6,
+    so the dequantized magnitude is 6 * 448 / a1 whatever the input."""
+    row = np.array([1.0, -1.0, 2.0, -3.0] * 4, np.float32)
+    c, f = O.quantize_tokens_static(bf16_bits_of(row)[None, :], np.float32(1e6))
+    assert f[0, 0] == 0x7E
+    deq = O.dequant(c, f)[0]
+    assert np.all(np.abs(deq) == 6.0 * 448.0)
+
+
+def test_per_tensor_alpha_folds_the_input_scale():
+    """alpha = fl(1/fl(w_scale * a)); an amax-6 expert has w_scale 448, so with
+    a = 2 the alpha is fl(1/896); a zero expert keeps alpha 0."""
+    row = np.array(GRID + [-g for g in GRID], np.float32)
+    w = torch.from_numpy(np.tile(row, (2, 4, 2))).to(torch.bfloat16)
+    w[1] = 0
+    alpha = O.alpha_per_tensor(W.bf16_bits(w), np.float32(2.0))
+    assert alpha[0] == np.float32(1.0) / np.float32(896.0) and alpha[1] == 0.0
+
+
+def test_per_tensor_forward_matches_a_direct_dequantized_matmul():
+    """Per-tensor FC1 rows and route rows against numpy: weights dequantized from
+    the oracle codes over w_scale, tokens dequantized over a1 (no row scales),
+    FC2 input dequantized over a2.  A missing or doubled a1/a2 factor moves every
+    value by that factor."""
+    wl, x, w1, w2, ids, wts = _tiny("relu2", I=512)
+    a1, a2 = np.float32(8.0), np.float32(0.25)
+    Wt = O.WeightsPerTensor(W.bf16_bits(w1), W.bf16_bits(w2), a1, a2)
+    xc, xsf = O.quantize_tokens_static(W.bf16_bits(x), a1)
+    res = O.forward_w4a4_per_tensor(Wt, xc, xsf, a2, ids, wts, wl.E, wl.H, wl.I, "relu2")
+    # independent numpy composition
+    w1f, w2f = w1.float().numpy().astype(np.float64), w2.float().numpy().astype(np.float64)
+    xq = O.dequant(xc, xsf) / np.float64(a1)                        # tokens as the MMA sees them
+    for q in range(min(res["R"], 12)):
+        r = int(res["perm"][q]); t, e = r // wl.K, int(ids[r // wl.K, r % wl.K])
+        amax1 = np.float32(np.abs(w1f[e]).max())
+        ws1 = np.float32(np.float32(2688.0) / amax1)
+        c1, f1, _ = O.prepare_fc(W.bf16_bits(w1[e:e + 1]))
+        w1q = O.dequant(c1[0], f1[0]) / np.float64(ws1)
+        y = w1q @ xq[t]
+        a = np.maximum(y, 0) ** 2
+        assert np.allclose(res["act"][q], a, rtol=1e-5, atol=1e-6 * np.abs(a).max())
+        fq = O.dequant(res["fc2c"][q:q + 1], res["fc2sf"][q:q + 1])[0] / np.float64(a2)
+        amax2 = np.float32(np.abs(w2f[e]).max())
+        ws2 = np.float32(np.float32(2688.0) / amax2)
+        c2, f2, _ = O.prepare_fc(W.bf16_bits(w2[e:e + 1]))
+        w2q = O.dequant(c2[0], f2[0]) / np.float64(ws2)
+        route = w2q @ fq
+        got = O.bf16_to_f32(res["route"][q]).astype(np.float64)
+        assert np.allclose(got, route, rtol=1e-2, atol=1e-2 * np.abs(route).max())
