@@ -195,6 +195,42 @@ moe_status moe_nvfp4_forward_w4a16(const moe_dims* d, const moe_nvfp4_weights* w
                                    const float* topk_w, void* out_bf16, void* ws,
                                    size_t ws_bytes, moe_stream_t stream);
 
+/* Per-tensor NVFP4 x NVFP4 recipe ([MLM] How to extend, "Per-tensor NVFP4 x
+ * NVFP4": serving calibrated checkpoints).  a1_scale and a2_scale are the
+ * static FC1 / FC2 input scales, DEVICE fp32 scalars (4-byte aligned) that stay
+ * fixed across calls so graph replays need no host sync.  They are encode
+ * scales, like w_scale: a row is quantized with enc = a (block scale
+ * E4M3(fl(fl(amax_b/6)*a)), saturating), and a dequantized value is
+ * code * block_scale / a.  They must be positive and finite.
+ *
+ * Weight prep of the recipe: the same codes and block scales as
+ * moe_nvfp4_prepare_weights, with the input scales folded into the alphas:
+ * fc1_alpha = 1 / (w_scale1 * a1_scale), fc2_alpha = 1 / (w_scale2 * a2_scale)
+ * (each product and quotient one fp32 rounding; 0 for an all-zero expert). */
+moe_status moe_nvfp4_prepare_weights_per_tensor(const moe_dims* d, const void* fc1_bf16,
+                                                const void* fc2_bf16, const float* a1_scale,
+                                                const float* a2_scale,
+                                                const moe_nvfp4_weights* out,
+                                                moe_stream_t stream);
+
+/* Token quantization of the recipe: x_bf16 [T][H] -> codes [T][Hp/2] and
+ * linear block scales sf [T][Hp/16] with the static encode scale a1_scale; no
+ * per-token scale.  Alignment and padding as moe_nvfp4_quantize_tokens. */
+moe_status moe_nvfp4_quantize_tokens_static(int32_t T, int32_t H, const void* x_bf16,
+                                            const float* a1_scale, uint8_t* codes, uint8_t* sf,
+                                            moe_stream_t stream);
+
+/* W4A4 forward of the recipe: tokens from moe_nvfp4_quantize_tokens_static,
+ * weights from moe_nvfp4_prepare_weights_per_tensor.  FC1 applies fc1_alpha
+ * only (no per-token scale), the FC2 input is quantized with the static encode
+ * scale a2_scale (fc2_input_scale = a2_scale), FC2 applies fc2_alpha only; the
+ * finalize and every other argument as moe_nvfp4_forward (same workspace size). */
+moe_status moe_nvfp4_forward_per_tensor(const moe_dims* d, const moe_nvfp4_weights* w, int32_t T,
+                                        int32_t K, const uint8_t* codes, const uint8_t* sf,
+                                        const float* a2_scale, const int32_t* topk_ids,
+                                        const float* topk_w, void* out_bf16, void* ws,
+                                        size_t ws_bytes, moe_stream_t stream);
+
 /* Device-reported status of the last forward that used `ws`: synchronises
  * `stream`, then returns MOE_ERR_BAD_EXPERT_ID, MOE_ERR_DEVICE_TIMEOUT or
  * MOE_OK.  The flags are rewritten by every forward.  Debug/test

@@ -81,7 +81,15 @@ def lib():
         L.moe_nvfp4_forward_noalloc.argtypes = [C.POINTER(moe_dims), C.POINTER(moe_nvfp4_weights),
                                                 i32, i32, vp, vp, vp, vp, vp, vp, vp]
         L.moe_nvfp4_profile_events.argtypes = [C.POINTER(C.c_void_p), i32]
-        for f in ["moe_nvfp4_weight_sizes", "moe_nvfp4_prepare_weights",
+        L.moe_nvfp4_prepare_weights_per_tensor.argtypes = [
+            C.POINTER(moe_dims), vp, vp, vp, vp, C.POINTER(moe_nvfp4_weights), vp]
+        L.moe_nvfp4_quantize_tokens_static.argtypes = [i32, i32, vp, vp, vp, vp, vp]
+        L.moe_nvfp4_forward_per_tensor.argtypes = [C.POINTER(moe_dims),
+                                                   C.POINTER(moe_nvfp4_weights), i32, i32, vp, vp,
+                                                   vp, vp, vp, vp, vp, sz, vp]
+        for f in ["moe_nvfp4_prepare_weights_per_tensor", "moe_nvfp4_quantize_tokens_static",
+                  "moe_nvfp4_forward_per_tensor",
+                  "moe_nvfp4_weight_sizes", "moe_nvfp4_prepare_weights",
                   "moe_nvfp4_quantize_tokens", "moe_nvfp4_workspace_layout", "moe_nvfp4_forward",
                   "moe_nvfp4_forward_w4a16", "moe_nvfp4_read_status", "moe_nvfp4_profile_events",
                   "moe_nvfp4_forward_noalloc"]:
@@ -150,6 +158,33 @@ def moe_nvfp4_quantize_tokens(x_bf16, codes, sf, scale, stream=None):
     _check(lib().moe_nvfp4_quantize_tokens(T, H, _ptr(x_bf16), _ptr(codes), _ptr(sf),
                                            _ptr(scale), _stream(stream)),
            "moe_nvfp4_quantize_tokens")
+
+
+def moe_nvfp4_prepare_weights_per_tensor(d, fc1_bf16, fc2_bf16, a1_scale, a2_scale, w,
+                                         stream=None):
+    _need_cuda(fc1_bf16, fc2_bf16, a1_scale, a2_scale)
+    _check(lib().moe_nvfp4_prepare_weights_per_tensor(
+        C.byref(d), _ptr(fc1_bf16), _ptr(fc2_bf16), _ptr(a1_scale), _ptr(a2_scale), C.byref(w.c),
+        _stream(stream)), "moe_nvfp4_prepare_weights_per_tensor")
+
+
+def moe_nvfp4_quantize_tokens_static(x_bf16, a1_scale, codes, sf, stream=None):
+    _need_cuda(x_bf16, a1_scale, codes, sf)
+    T, H = x_bf16.shape
+    _check(lib().moe_nvfp4_quantize_tokens_static(T, H, _ptr(x_bf16), _ptr(a1_scale), _ptr(codes),
+                                                  _ptr(sf), _stream(stream)),
+           "moe_nvfp4_quantize_tokens_static")
+
+
+def moe_nvfp4_forward_per_tensor(d, w, codes, sf, a2_scale, topk_ids, topk_w, out, ws,
+                                 stream=None):
+    _need_cuda(codes, sf, a2_scale, topk_ids, topk_w, out, ws)
+    T, K = topk_ids.shape
+    _check(lib().moe_nvfp4_forward_per_tensor(C.byref(d), C.byref(w.c), T, K, _ptr(codes),
+                                              _ptr(sf), _ptr(a2_scale), _ptr(topk_ids),
+                                              _ptr(topk_w), _ptr(out), _ptr(ws),
+                                              ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_nvfp4_forward_per_tensor")
 
 
 def moe_nvfp4_workspace_bytes(d, T_max, K, w4a16=False):
@@ -252,6 +287,36 @@ def quantize_tokens(x_bf16, stream=None):
     scale = torch.empty(T, dtype=torch.float32, device=dev)
     moe_nvfp4_quantize_tokens(x_bf16, codes, sf, scale, stream)
     return codes, sf, scale
+
+
+def prepare_weights_per_tensor(fc1_bf16, fc2_bf16, act, a1_scale, a2_scale, out=None,
+                               stream=None):
+    """Per-tensor recipe weights: codes/scales as prepare_weights, alphas with the
+    static device scalars a1_scale / a2_scale folded in."""
+    E, N1, H = fc1_bf16.shape
+    I = fc2_bf16.shape[2]
+    w = out if out is not None else PreparedWeights(E, H, I, act, device=fc1_bf16.device)
+    moe_nvfp4_prepare_weights_per_tensor(w.dims, fc1_bf16, fc2_bf16, a1_scale, a2_scale, w, stream)
+    return w
+
+
+def quantize_tokens_static(x_bf16, a1_scale, stream=None):
+    T, H = x_bf16.shape
+    Hp = padded(H)
+    codes = torch.empty(T, Hp // 2, dtype=torch.uint8, device=x_bf16.device)
+    sf = torch.empty(T, Hp // 16, dtype=torch.uint8, device=x_bf16.device)
+    moe_nvfp4_quantize_tokens_static(x_bf16, a1_scale, codes, sf, stream)
+    return codes, sf
+
+
+def forward_per_tensor(w, codes, sf, a2_scale, topk_ids, topk_w, ws=None, out=None, stream=None):
+    T, K = topk_ids.shape
+    if ws is None:
+        ws = workspace(w, T, K, device=codes.device)
+    if out is None:
+        out = torch.empty(T, w.H, dtype=torch.bfloat16, device=codes.device)
+    moe_nvfp4_forward_per_tensor(w.dims, w, codes, sf, a2_scale, topk_ids, topk_w, out, ws, stream)
+    return out
 
 
 def workspace(w, T_max, K, w4a16=False, device="cuda"):

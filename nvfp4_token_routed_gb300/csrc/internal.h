@@ -91,13 +91,17 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// static_enc: null for the per-token recipe, else the device encode scale a1 of
+// the per-tensor recipe (scale is then not written).
 void launch_quantize_tokens(int T, int H, int Hp, const void* x, uint8_t* codes, uint8_t* sf,
-                            float* scale, cudaStream_t s);
+                            float* scale, const float* static_enc, cudaStream_t s);
+// a_scale: null, or the device static input scale folded into alpha.
 void launch_prepare_fc(int E, int N, int D, int Np, int Dp, int swiglu_I, const void* w,
-                       uint8_t* codes, uint8_t* sf, float* alpha, cudaStream_t s);
+                       uint8_t* codes, uint8_t* sf, float* alpha, const float* a_scale,
+                       cudaStream_t s);
 void launch_route(const RouteArgs& a, cudaStream_t s);
 void launch_requant(int TK, int I, const int32_t* inv, const float* act, uint8_t* qc, uint8_t* qsf,
-                    float* qs, cudaStream_t s);
+                    float* qs, const float* static_enc, cudaStream_t s);
 void launch_finalize(int T, int K, int H, int Hp, const int32_t* inv, const float* w,
                      const void* route, void* out, cudaStream_t s);
 // Token-tile tensor maps of one operand: the same [rows][row_bytes] buffer with

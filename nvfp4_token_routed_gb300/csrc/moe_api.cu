@@ -239,9 +239,9 @@ moe_status moe_nvfp4_weight_sizes(const moe_dims* d, size_t bytes_out[6]) {
   return MOE_OK;
 }
 
-moe_status moe_nvfp4_prepare_weights(const moe_dims* d, const void* fc1_bf16,
-                                     const void* fc2_bf16, const moe_nvfp4_weights* out,
-                                     moe_stream_t stream) {
+static moe_status prepare_impl(const moe_dims* d, const void* fc1_bf16, const void* fc2_bf16,
+                               const float* a1_scale, const float* a2_scale,
+                               const moe_nvfp4_weights* out, moe_stream_t stream) {
   moe_status st = check_dims(d);
   if (st != MOE_OK) return st;
   if (!fc1_bf16 || !fc2_bf16) return MOE_ERR_INVALID_ARG;
@@ -252,25 +252,56 @@ moe_status moe_nvfp4_prepare_weights(const moe_dims* d, const void* fc1_bf16,
   const bool swiglu = d->act == MOE_ACT_SWIGLU;
   const int N1 = swiglu ? 2 * d->I : d->I;
   launch_prepare_fc(d->E, N1, d->H, (int)n1p_of(d), (int)hp_of(d), swiglu ? d->I : 0, fc1_bf16,
-                    out->fc1_codes, out->fc1_sf, out->fc1_alpha, s);
+                    out->fc1_codes, out->fc1_sf, out->fc1_alpha, a1_scale, s);
   launch_prepare_fc(d->E, d->H, d->I, (int)hp_of(d), (int)ip_of(d), 0, fc2_bf16, out->fc2_codes,
-                    out->fc2_sf, out->fc2_alpha, s);
+                    out->fc2_sf, out->fc2_alpha, a2_scale, s);
+  return cuda_status(cudaGetLastError());
+}
+
+moe_status moe_nvfp4_prepare_weights(const moe_dims* d, const void* fc1_bf16,
+                                     const void* fc2_bf16, const moe_nvfp4_weights* out,
+                                     moe_stream_t stream) {
+  return prepare_impl(d, fc1_bf16, fc2_bf16, nullptr, nullptr, out, stream);
+}
+
+moe_status moe_nvfp4_prepare_weights_per_tensor(const moe_dims* d, const void* fc1_bf16,
+                                                const void* fc2_bf16, const float* a1_scale,
+                                                const float* a2_scale,
+                                                const moe_nvfp4_weights* out,
+                                                moe_stream_t stream) {
+  if (!a1_scale || !a2_scale) return MOE_ERR_INVALID_ARG;
+  if (!aligned(a1_scale, 4) || !aligned(a2_scale, 4)) return MOE_ERR_MISALIGNED;
+  return prepare_impl(d, fc1_bf16, fc2_bf16, a1_scale, a2_scale, out, stream);
+}
+
+static moe_status quantize_impl(int32_t T, int32_t H, const void* x_bf16, uint8_t* codes,
+                                uint8_t* sf, float* scale, const float* a1_scale,
+                                moe_stream_t stream) {
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (!dim_ok(H)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (T == 0) return MOE_OK;
+  if (!x_bf16 || !codes || !sf || (!scale && !a1_scale)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x_bf16, 16) || !aligned(codes, 16) || !aligned(sf, 16) ||
+      (scale && !aligned(scale, 4)) || (a1_scale && !aligned(a1_scale, 4)))
+    return MOE_ERR_MISALIGNED;
+  moe_status st = check_device(nullptr);
+  if (st != MOE_OK) return st;
+  launch_quantize_tokens(T, H, (int)pad256(H), x_bf16, codes, sf, scale, a1_scale,
+                         reinterpret_cast<cudaStream_t>(stream));
   return cuda_status(cudaGetLastError());
 }
 
 moe_status moe_nvfp4_quantize_tokens(int32_t T, int32_t H, const void* x_bf16, uint8_t* codes,
                                      uint8_t* sf, float* scale, moe_stream_t stream) {
-  if (T < 0) return MOE_ERR_INVALID_ARG;
-  if (!dim_ok(H)) return MOE_ERR_UNSUPPORTED_SHAPE;
-  if (T == 0) return MOE_OK;
-  if (!x_bf16 || !codes || !sf || !scale) return MOE_ERR_INVALID_ARG;
-  if (!aligned(x_bf16, 16) || !aligned(codes, 16) || !aligned(sf, 16) || !aligned(scale, 4))
-    return MOE_ERR_MISALIGNED;
-  moe_status st = check_device(nullptr);
-  if (st != MOE_OK) return st;
-  launch_quantize_tokens(T, H, (int)pad256(H), x_bf16, codes, sf, scale,
-                         reinterpret_cast<cudaStream_t>(stream));
-  return cuda_status(cudaGetLastError());
+  if (T > 0 && !scale) return MOE_ERR_INVALID_ARG;
+  return quantize_impl(T, H, x_bf16, codes, sf, scale, nullptr, stream);
+}
+
+moe_status moe_nvfp4_quantize_tokens_static(int32_t T, int32_t H, const void* x_bf16,
+                                            const float* a1_scale, uint8_t* codes, uint8_t* sf,
+                                            moe_stream_t stream) {
+  if (T > 0 && !a1_scale) return MOE_ERR_INVALID_ARG;
+  return quantize_impl(T, H, x_bf16, codes, sf, nullptr, a1_scale, stream);
 }
 
 size_t moe_nvfp4_workspace_bytes(const moe_dims* d, int32_t T_max, int32_t K, int32_t w4a16) {
@@ -328,14 +359,18 @@ static RouteArgs route_args(const moe_dims* d, int32_t T, int32_t K, const int32
   return r;
 }
 
-moe_status moe_nvfp4_forward(const moe_dims* d, const moe_nvfp4_weights* w, int32_t T, int32_t K,
-                             const uint8_t* codes, const uint8_t* sf, const float* scale,
-                             const int32_t* topk_ids, const float* topk_w, void* out_bf16,
-                             void* ws, size_t ws_bytes, moe_stream_t stream) {
+// scale: per-token row scales (per-token recipe) or null with a2_static set (the
+// per-tensor recipe: no row scales, FC2 input quantized with the static scale).
+static moe_status forward_w4a4_impl(const moe_dims* d, const moe_nvfp4_weights* w, int32_t T,
+                                    int32_t K, const uint8_t* codes, const uint8_t* sf,
+                                    const float* scale, const float* a2_static,
+                                    const int32_t* topk_ids, const float* topk_w, void* out_bf16,
+                                    void* ws, size_t ws_bytes, moe_stream_t stream) {
   moe_ws_layout L;
   int sms = 0;
-  if (T > 0 && (!codes || !sf || !scale)) return MOE_ERR_INVALID_ARG;
-  if (T > 0 && (!aligned(codes, 16) || !aligned(sf, 16) || !aligned(scale, 4)))
+  if (T > 0 && (!codes || !sf || (!scale && !a2_static))) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!aligned(codes, 16) || !aligned(sf, 16) || (scale && !aligned(scale, 4)) ||
+                (a2_static && !aligned(a2_static, 4))))
     return MOE_ERR_MISALIGNED;
   moe_status st =
       forward_common(d, w, T, K, topk_ids, topk_w, out_bf16, ws, ws_bytes, 0, &L, &sms);
@@ -390,7 +425,7 @@ moe_status moe_nvfp4_forward(const moe_dims* d, const moe_nvfp4_weights* w, int3
 
   launch_requant(T * K, I, at<int32_t>(ws, L.inv), at<float>(ws, L.act),
                  at<uint8_t>(ws, L.fc2q_codes), at<uint8_t>(ws, L.fc2q_sf),
-                 at<float>(ws, L.fc2q_scale), s);
+                 at<float>(ws, L.fc2q_scale), a2_static, s);
   mark(3, s);
 
   GemmArgs g2 = g;
@@ -413,6 +448,25 @@ moe_status moe_nvfp4_forward(const moe_dims* d, const moe_nvfp4_weights* w, int3
                   out_bf16, s);
   mark(5, s);
   return cuda_status(cudaGetLastError());
+}
+
+moe_status moe_nvfp4_forward(const moe_dims* d, const moe_nvfp4_weights* w, int32_t T, int32_t K,
+                             const uint8_t* codes, const uint8_t* sf, const float* scale,
+                             const int32_t* topk_ids, const float* topk_w, void* out_bf16,
+                             void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (T > 0 && !scale) return MOE_ERR_INVALID_ARG;
+  return forward_w4a4_impl(d, w, T, K, codes, sf, scale, nullptr, topk_ids, topk_w, out_bf16, ws,
+                           ws_bytes, stream);
+}
+
+moe_status moe_nvfp4_forward_per_tensor(const moe_dims* d, const moe_nvfp4_weights* w, int32_t T,
+                                        int32_t K, const uint8_t* codes, const uint8_t* sf,
+                                        const float* a2_scale, const int32_t* topk_ids,
+                                        const float* topk_w, void* out_bf16, void* ws,
+                                        size_t ws_bytes, moe_stream_t stream) {
+  if (T > 0 && !a2_scale) return MOE_ERR_INVALID_ARG;
+  return forward_w4a4_impl(d, w, T, K, codes, sf, nullptr, a2_scale, topk_ids, topk_w, out_bf16,
+                           ws, ws_bytes, stream);
 }
 
 moe_status moe_nvfp4_forward_w4a16(const moe_dims* d, const moe_nvfp4_weights* w, int32_t T,

@@ -20,20 +20,27 @@ namespace moe {
 // past H are zero (zero codes, zero scale bytes), which leaves every dot product
 // with a zero-padded weight row unchanged (Megatron-LM PR #8262, "Why CuTe DSL":
 // hidden sizes are padded to 256).
+// With `static_enc` (the per-tensor recipe, Megatron-LM PR #8262, "How to
+// extend": nvfp4_quantize(x, a1_scale) with a fixed scale tensor) every row uses
+// that encode scale and no per-token scale is written.
 __global__ void __launch_bounds__(256) quantize_tokens_kernel(int T, int H, int Hp,
                                                               const uint4* __restrict__ x,
                                                               uint8_t* __restrict__ codes,
                                                               uint8_t* __restrict__ sf,
-                                                              float* __restrict__ scale) {
+                                                              float* __restrict__ scale,
+                                                              const float* __restrict__ static_enc) {
   pdl_wait();
   pdl_trigger();
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
   const uint4* row = x + (size_t)t * (H / 8);
-  float m = 0.0f;
-  for (int i = lane; i < H / 8; i += 32) m = fmaxf(m, bf16x8_absmax(__ldg(row + i)));
-  m = warp_max(m);
+  float m = 1.0f;  // any non-zero value: the static path quantizes every real block
+  if (!static_enc) {
+    m = 0.0f;
+    for (int i = lane; i < H / 8; i += 32) m = fmaxf(m, bf16x8_absmax(__ldg(row + i)));
+    m = warp_max(m);
+  }
   uint2* crow = reinterpret_cast<uint2*>(codes + (size_t)t * (Hp / 2));
   uint8_t* srow = sf + (size_t)t * (Hp / 16);
   for (int b = (m == 0.0f ? 0 : H / 16) + lane; b < Hp / 16; b += 32) {
@@ -44,7 +51,7 @@ __global__ void __launch_bounds__(256) quantize_tokens_kernel(int T, int H, int 
     if (lane == 0) scale[t] = 0.0f;
     return;
   }
-  const float enc = __fdiv_rn(kRecipeMax, m);
+  const float enc = static_enc ? *static_enc : __fdiv_rn(kRecipeMax, m);
   for (int b = lane; b < H / 16; b += 32) {
     float v[16];
     bf16x16_to_f32(__ldg(row + 2 * b), __ldg(row + 2 * b + 1), v);
@@ -52,15 +59,15 @@ __global__ void __launch_bounds__(256) quantize_tokens_kernel(int T, int H, int 
     srow[b] = (uint8_t)quant_block16(v, enc, q);
     crow[b] = q;
   }
-  if (lane == 0) scale[t] = __fmul_rn(m, kRecipeInv);
+  if (lane == 0 && !static_enc) scale[t] = __fmul_rn(m, kRecipeInv);
 }
 
 void launch_quantize_tokens(int T, int H, int Hp, const void* x, uint8_t* codes, uint8_t* sf,
-                            float* scale, cudaStream_t s) {
+                            float* scale, const float* static_enc, cudaStream_t s) {
   const int warps = 8;
   const int blocks = (T + warps - 1) / warps;
   launch_pdl(quantize_tokens_kernel, dim3(blocks), dim3(warps * 32), 0, s, T, H, Hp,
-             static_cast<const uint4*>(x), codes, sf, scale);
+             static_cast<const uint4*>(x), codes, sf, scale, static_enc);
 }
 
 // ============================================================== weight preparation
@@ -130,16 +137,21 @@ __global__ void __launch_bounds__(256) quantize_weights_kernel(
   }
 }
 
-// Stage 3: alpha = 1 / w_scale with w_scale = 2688 / amax (0 for an all-zero expert).
-__global__ void expert_alpha_kernel(int E, float* alpha) {
+// Stage 3: alpha = 1 / w_scale with w_scale = 2688 / amax (0 for an all-zero
+// expert); with a static input scale a (per-tensor recipe, "How to extend":
+// fc_alpha = 1 / (w_scale * a_scale)) alpha = 1 / (w_scale * a).
+__global__ void expert_alpha_kernel(int E, float* alpha, const float* a_scale) {
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= E) return;
   const float amax = alpha[e];  // still holds the amax bit pattern
-  alpha[e] = amax == 0.0f ? 0.0f : __fdiv_rn(1.0f, __fdiv_rn(kRecipeMax, amax));
+  const float w_scale = __fdiv_rn(kRecipeMax, amax);
+  alpha[e] = amax == 0.0f ? 0.0f
+                          : __fdiv_rn(1.0f, a_scale ? __fmul_rn(w_scale, *a_scale) : w_scale);
 }
 
 void launch_prepare_fc(int E, int N, int D, int Np, int Dp, int swiglu_I, const void* w,
-                       uint8_t* codes, uint8_t* sf, float* alpha, cudaStream_t s) {
+                       uint8_t* codes, uint8_t* sf, float* alpha, const float* a_scale,
+                       cudaStream_t s) {
   cudaMemsetAsync(alpha, 0, sizeof(float) * E, s);
   const int64_t vec = (int64_t)N * D / 8;
   int bx = (int)((vec + 256 * 8 - 1) / (256 * 8));
@@ -151,7 +163,7 @@ void launch_prepare_fc(int E, int N, int D, int Np, int Dp, int swiglu_I, const 
   quantize_weights_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(
       static_cast<const uint4*>(w), E, N, D, Np, Dp, swiglu_I,
       reinterpret_cast<const uint32_t*>(alpha), codes, sf, sf_bytes);
-  expert_alpha_kernel<<<(E + 255) / 256, 256, 0, s>>>(E, alpha);
+  expert_alpha_kernel<<<(E + 255) / 256, 256, 0, s>>>(E, alpha, a_scale);
 }
 
 // ============================================================== routing permutation
@@ -301,7 +313,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(
     const uint32_t c16 = (uint32_t)(Hp / 16);
     for (int g = lane; g < Hp / 64; g += 32)
       *reinterpret_cast<uint32_t*>(psf + sf_offset(p, 4 * g, c16)) = __ldg(ssrc + g);
-    if (lane == 0) ps[p] = xs[t];
+    if (lane == 0) ps[p] = xs ? xs[t] : 1.0f;  // per-tensor tokens carry no row scale
   }
 }
 
@@ -331,11 +343,14 @@ void launch_route(const RouteArgs& a, cudaStream_t s) {
 // Megatron-LM PR #8262, "How to extend": fc2_input_scale = 1/(448*6) for the
 // per-token recipe; the FC2 input is quantized per routed row.  One warp per
 // route reads the fp32 activated row written by the FC1 epilogue.
+// With `static_enc` (per-tensor recipe: fc2_input_scale = a2_scale) every row
+// uses that encode scale and its row scale is 1.
 __global__ void __launch_bounds__(256) requant_kernel(int TK, int I, const int32_t* __restrict__ inv,
                                                       const float* __restrict__ act,
                                                       uint8_t* __restrict__ qc,
                                                       uint8_t* __restrict__ qsf,
-                                                      float* __restrict__ qs) {
+                                                      float* __restrict__ qs,
+                                                      const float* __restrict__ static_enc) {
   pdl_wait();
   pdl_trigger();
   const int idx = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -344,12 +359,15 @@ __global__ void __launch_bounds__(256) requant_kernel(int TK, int I, const int32
   const int p = inv[idx];
   if (p < 0) return;
   const float4* row = reinterpret_cast<const float4*>(act + (size_t)p * I);
-  float m = 0.0f;
-  for (int i = lane; i < I / 4; i += 32) {
-    const float4 v = row[i];
-    m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  float m = 1.0f;
+  if (!static_enc) {
+    m = 0.0f;
+    for (int i = lane; i < I / 4; i += 32) {
+      const float4 v = row[i];
+      m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+    m = warp_max(m);
   }
-  m = warp_max(m);
   uint2* crow = reinterpret_cast<uint2*>(qc + (size_t)p * (I / 2));
   const uint32_t c16 = (uint32_t)(I / 16);
   if (m == 0.0f) {
@@ -360,7 +378,7 @@ __global__ void __launch_bounds__(256) requant_kernel(int TK, int I, const int32
     if (lane == 0) qs[p] = 0.0f;
     return;
   }
-  const float enc = __fdiv_rn(kRecipeMax, m);
+  const float enc = static_enc ? *static_enc : __fdiv_rn(kRecipeMax, m);
   for (int b = lane; b < I / 16; b += 32) {
     float v[16];
 #pragma unroll
@@ -375,14 +393,14 @@ __global__ void __launch_bounds__(256) requant_kernel(int TK, int I, const int32
     qsf[sf_offset(p, b, c16)] = (uint8_t)quant_block16(v, enc, q);
     crow[b] = q;
   }
-  if (lane == 0) qs[p] = __fmul_rn(m, kRecipeInv);
+  if (lane == 0) qs[p] = static_enc ? 1.0f : __fmul_rn(m, kRecipeInv);
 }
 
 void launch_requant(int TK, int I, const int32_t* inv, const float* act, uint8_t* qc, uint8_t* qsf,
-                    float* qs, cudaStream_t s) {
+                    float* qs, const float* static_enc, cudaStream_t s) {
   const int warps = 8;
   launch_pdl(requant_kernel, dim3((TK + warps - 1) / warps), dim3(warps * 32), 0, s, TK, I, inv,
-             act, qc, qsf, qs);
+             act, qc, qsf, qs, static_enc);
 }
 
 // ============================================================== finalize
