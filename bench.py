@@ -49,6 +49,8 @@ def parse():
     p.add_argument("--w4a16", action="store_true", help="time the BF16-activation variant")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--with-router", action="store_true",
+                   help="start each step from router logits: top-K router kernel + the layer")
     p.add_argument("--prep", action="store_true",
                    help="time in-place weight re-preparation (a refit) instead of the forward")
     return p.parse_args()
@@ -269,7 +271,15 @@ def run_ours(args, rank, world, local_rank):
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
+    logits_d = None
+    if args.with_router:
+        g = torch.Generator(device=dev)
+        g.manual_seed(W.BASE_SEED + 5)
+        logits_d = torch.randn(T, wl.E, generator=g, device=dev)
+
     def step():
+        if logits_d is not None:
+            M.moe_nvfp4_route_topk(logits_d, ids_d, wts_d, stream)
         if args.w4a16:
             M.moe_nvfp4_forward_w4a16(w.dims, w, x_d, ids_d, wts_d, out, ws, stream)
             return
@@ -370,10 +380,17 @@ def run_ours(args, rank, world, local_rank):
     wts_e = torch.empty_like(wts_d)
     e2e_steps = min(args.steps, 500)
 
+    logits_h = logits_d.cpu().pin_memory() if logits_d is not None else None
+    logits_e = torch.empty_like(logits_d) if logits_d is not None else None
+
     def e2e_step():
         x_e.copy_(x_h, non_blocking=True)
-        ids_e.copy_(ids_h, non_blocking=True)
-        wts_e.copy_(wts_h, non_blocking=True)
+        if logits_e is not None:
+            logits_e.copy_(logits_h, non_blocking=True)
+            M.moe_nvfp4_route_topk(logits_e, ids_e, wts_e, stream)
+        else:
+            ids_e.copy_(ids_h, non_blocking=True)
+            wts_e.copy_(wts_h, non_blocking=True)
         if args.w4a16:
             M.moe_nvfp4_forward_w4a16(w.dims, w, x_e, ids_e, wts_e, out, ws, stream)
         else:
@@ -401,7 +418,8 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
         e2e_ms = float(tt.item())
     e2e_value = world * T * e2e_steps / (e2e_ms / 1e3)
-    h2d = x_h.numel() * 2 + ids_h.numel() * 4 + wts_h.numel() * 4
+    h2d = x_h.numel() * 2 + (logits_h.numel() * 4 if logits_h is not None
+                             else ids_h.numel() * 4 + wts_h.numel() * 4)
     d2h = out_h.numel() * 2
 
     if rank != 0:
@@ -416,7 +434,8 @@ def run_ours(args, rank, world, local_rank):
         "us_per_layer": ms_per_step * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16 x nvfp4" if args.w4a16 else "nvfp4",
         "data": "synthetic (seeded N(0,1)-family inputs)",
-        "config": {"workload": wl.name + ("+w4a16" if args.w4a16 else ""), "T": T, "H": H, "I": wl.I, "E": wl.E, "K": K,
+        "config": {"workload": wl.name + ("+w4a16" if args.w4a16 else "") + ("+router" if args.with_router else ""),
+                   "T": T, "H": H, "I": wl.I, "E": wl.E, "K": K,
                    "act": wl.act, "routes": R, "experts_touched": U,
                    "l2": "flushed (256 MB write) between timed steps",
                    "graph": graph is not None, "parallelism": f"replicas x{world}"},
@@ -430,7 +449,8 @@ def run_ours(args, rank, world, local_rank):
                                "over a second pass of the same K steps"},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": (KERNELS_PER_STEP - (2 if args.w4a16 else 0)) * args.steps,
+        "gpu_launches": (KERNELS_PER_STEP - (2 if args.w4a16 else 0) + (1 if args.with_router else 0))
+                        * args.steps,
         "clocks": clocks,
         "wall_s": t_wall,
     }

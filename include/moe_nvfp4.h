@@ -231,6 +231,18 @@ moe_status moe_nvfp4_forward_per_tensor(const moe_dims* d, const moe_nvfp4_weigh
                                         const float* topk_w, void* out_bf16, void* ws,
                                         size_t ws_bytes, moe_stream_t stream);
 
+/* The plain top-K router upstream of the layer ([MLM] Performance: "plain
+ * top-8" routing, no group-limited routing; the router GEMM that produces the
+ * logits is the caller's).  logits fp32 [T][E] -> topk_ids int32 [T][K]: the K
+ * largest logits in descending order, equal logits to the lower expert id;
+ * topk_w fp32 [T][K]: softmax over the K selected logits (shifted by the
+ * largest, summed for k ascending), i.e. the full softmax renormalised over the
+ * selected experts.  Logits must not be NaN.  1 <= E <= 1024,
+ * 1 <= K <= min(32, E); pointers 4-byte aligned; T == 0 is a no-op.  Each
+ * token's result depends only on its own row (batch invariant). */
+moe_status moe_nvfp4_route_topk(int32_t T, int32_t E, int32_t K, const float* logits,
+                                int32_t* topk_ids, float* topk_w, moe_stream_t stream);
+
 /* Device-reported status of the last forward that used `ws`: synchronises
  * `stream`, then returns MOE_ERR_BAD_EXPERT_ID, MOE_ERR_DEVICE_TIMEOUT or
  * MOE_OK.  The flags are rewritten by every forward.  Debug/test

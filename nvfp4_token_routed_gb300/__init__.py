@@ -87,7 +87,9 @@ def lib():
         L.moe_nvfp4_forward_per_tensor.argtypes = [C.POINTER(moe_dims),
                                                    C.POINTER(moe_nvfp4_weights), i32, i32, vp, vp,
                                                    vp, vp, vp, vp, vp, sz, vp]
-        for f in ["moe_nvfp4_prepare_weights_per_tensor", "moe_nvfp4_quantize_tokens_static",
+        L.moe_nvfp4_route_topk.argtypes = [i32, i32, i32, vp, vp, vp, vp]
+        for f in ["moe_nvfp4_route_topk",
+                  "moe_nvfp4_prepare_weights_per_tensor", "moe_nvfp4_quantize_tokens_static",
                   "moe_nvfp4_forward_per_tensor",
                   "moe_nvfp4_weight_sizes", "moe_nvfp4_prepare_weights",
                   "moe_nvfp4_quantize_tokens", "moe_nvfp4_workspace_layout", "moe_nvfp4_forward",
@@ -185,6 +187,14 @@ def moe_nvfp4_forward_per_tensor(d, w, codes, sf, a2_scale, topk_ids, topk_w, ou
                                               _ptr(topk_w), _ptr(out), _ptr(ws),
                                               ws.numel() * ws.element_size(), _stream(stream)),
            "moe_nvfp4_forward_per_tensor")
+
+
+def moe_nvfp4_route_topk(logits, topk_ids, topk_w, stream=None):
+    _need_cuda(logits, topk_ids, topk_w)
+    T, E = logits.shape
+    K = topk_ids.shape[1]
+    _check(lib().moe_nvfp4_route_topk(T, E, K, _ptr(logits), _ptr(topk_ids), _ptr(topk_w),
+                                      _stream(stream)), "moe_nvfp4_route_topk")
 
 
 def moe_nvfp4_workspace_bytes(d, T_max, K, w4a16=False):
@@ -317,6 +327,15 @@ def forward_per_tensor(w, codes, sf, a2_scale, topk_ids, topk_w, ws=None, out=No
         out = torch.empty(T, w.H, dtype=torch.bfloat16, device=codes.device)
     moe_nvfp4_forward_per_tensor(w.dims, w, codes, sf, a2_scale, topk_ids, topk_w, out, ws, stream)
     return out
+
+
+def route_topk(logits, K, stream=None):
+    """Plain top-K router: fp32 logits [T,E] -> (int32 ids [T,K], fp32 scores [T,K])."""
+    T = logits.shape[0]
+    ids = torch.empty(T, K, dtype=torch.int32, device=logits.device)
+    w = torch.empty(T, K, dtype=torch.float32, device=logits.device)
+    moe_nvfp4_route_topk(logits, ids, w, stream)
+    return ids, w
 
 
 def workspace(w, T_max, K, w4a16=False, device="cuda"):

@@ -100,6 +100,8 @@ void launch_prepare_fc(int E, int N, int D, int Np, int Dp, int swiglu_I, const 
                        uint8_t* codes, uint8_t* sf, float* alpha, const float* a_scale,
                        cudaStream_t s);
 void launch_route(const RouteArgs& a, cudaStream_t s);
+void launch_route_topk(int T, int E, int K, const float* logits, int32_t* ids, float* w,
+                       cudaStream_t s);
 void launch_requant(int TK, int I, const int32_t* inv, const float* act, uint8_t* qc, uint8_t* qsf,
                     float* qs, const float* static_enc, cudaStream_t s);
 void launch_finalize(int T, int K, int H, int Hp, const int32_t* inv, const float* w,

@@ -536,6 +536,20 @@ moe_status moe_nvfp4_forward_w4a16(const moe_dims* d, const moe_nvfp4_weights* w
   return cuda_status(cudaGetLastError());
 }
 
+moe_status moe_nvfp4_route_topk(int32_t T, int32_t E, int32_t K, const float* logits,
+                                int32_t* topk_ids, float* topk_w, moe_stream_t stream) {
+  if (T < 0 || E < 1 || K < 1) return MOE_ERR_INVALID_ARG;
+  if (E > 1024 || K > 32 || K > E) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (T == 0) return MOE_OK;
+  if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (!aligned(logits, 4) || !aligned(topk_ids, 4) || !aligned(topk_w, 4))
+    return MOE_ERR_MISALIGNED;
+  moe_status st = check_device(nullptr);
+  if (st != MOE_OK) return st;
+  launch_route_topk(T, E, K, logits, topk_ids, topk_w, reinterpret_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
+}
+
 moe_status moe_nvfp4_profile_events(void* const* events, int32_t n) {
   if (n < 0 || n > kMaxProfileEvents) return MOE_ERR_INVALID_ARG;
   if (!events) n = 0;

@@ -36,6 +36,8 @@
  *       the same finalize.
  *   R8  SwiGLU: canonical FC1 rows [0,I) are the gate, [I,2I) the up projection;
  *       a = silu(g)*u with silu(g) = g/(1+exp(-g)); no clamp.
+ *   R14 Router: top-K logits per token (ties to the lower expert id, descending),
+ *       scores = softmax over the selected K, fp64, rounded to fp32.
  *   R12 Per-tensor recipe (How to extend, "Per-tensor NVFP4 x NVFP4"): the static
  *       FC1 / FC2 input scales a1, a2 are encode scales like w_scale: token rows
  *       and FC2-input rows are quantized with enc = a1 (resp. a2) and carry no
@@ -289,6 +291,41 @@ void orc_prepare_fc(int64_t E, int64_t N, int64_t D, const uint16_t* w, uint8_t*
 int64_t orc_sf_swizzle_offset(int64_t r, int64_t j, int64_t ncols16) {
     int64_t cpad = (ncols16 + 3) / 4 * 4;
     return ((r / 128) * (cpad / 4) + j / 4) * 512 + (r % 32) * 16 + ((r / 32) % 4) * 4 + (j % 4);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Router: top-k selection and scores (upstream of the expert layer)          */
+/* ------------------------------------------------------------------------ */
+
+/* Plain top-K router ([MLM] Performance: "plain top-8", no group-limited
+ * routing; R14): per token the K largest logits, ties to the lower expert id,
+ * in descending order; scores = softmax over the K selected logits, computed in
+ * fp64 (shift by the largest, exp, sum for k ascending) and rounded to fp32.
+ * This equals softmax over all experts renormalised over the selected K. */
+void orc_route_topk(int64_t T, int64_t E, int64_t K, const float* logits, int32_t* ids,
+                    float* w) {
+    for (int64_t t = 0; t < T; ++t) {
+        const float* l = logits + t * E;
+        unsigned char* taken = (unsigned char*)calloc((size_t)E, 1);
+        for (int64_t k = 0; k < K; ++k) {
+            int64_t best = -1;
+            for (int64_t e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                if (best < 0 || l[e] > l[best]) best = e; /* strict: lower id wins ties */
+            }
+            taken[best] = 1;
+            ids[t * K + k] = (int32_t)best;
+        }
+        double ex[64];
+        double m = (double)l[ids[t * K]];
+        double sum = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            ex[k] = exp((double)l[ids[t * K + k]] - m);
+            sum += ex[k];
+        }
+        for (int64_t k = 0; k < K; ++k) w[t * K + k] = (float)(ex[k] / sum);
+        free(taken);
+    }
 }
 
 /* ------------------------------------------------------------------------ */

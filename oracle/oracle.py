@@ -53,7 +53,7 @@ def lib():
                      "orc_quantize_tokens", "orc_prepare_fc", "orc_finalize", "orc_dense_w4a4",
                      "orc_route", "orc_forward_w4a4", "orc_forward_w4a16",
                      "orc_quantize_row_per_token_f32", "orc_quantize_tokens_static",
-                     "orc_alpha_per_tensor", "orc_forward_w4a4_per_tensor"]:
+                     "orc_alpha_per_tensor", "orc_forward_w4a4_per_tensor", "orc_route_topk"]:
             getattr(L, name).argtypes = None
     return _lib
 
@@ -189,6 +189,17 @@ def sf_to_swizzled(lin):
 
 
 # ----------------------------------------------------------------------------- routing + forward
+
+def route_topk(logits, K):
+    """Plain top-K router (R14): ids int32 [T][K] (descending, ties to the lower
+    id) and fp32 softmax scores over the selected logits."""
+    lg = np.ascontiguousarray(logits, dtype=np.float32)
+    T, E = lg.shape
+    ids = np.empty((T, K), np.int32)
+    w = np.empty((T, K), np.float32)
+    lib().orc_route_topk(C.c_int64(T), C.c_int64(E), C.c_int64(K), _p(lg), _p(ids), _p(w))
+    return ids, w
+
 
 def route(ids, E):
     ids = np.ascontiguousarray(ids, dtype=np.int32)

@@ -392,3 +392,28 @@ def test_per_tensor_forward_matches_a_direct_dequantized_matmul():
         route = w2q @ fq
         got = O.bf16_to_f32(res["route"][q]).astype(np.float64)
         assert np.allclose(got, route, rtol=1e-2, atol=1e-2 * np.abs(route).max())
+
+
+# --------------------------------------------------------------------------- router
+
+def test_router_topk_matches_a_stable_sort_and_the_softmax_closed_form():
+    """ids = the K largest logits (descending; equal logits to the lower id, as a
+    stable sort of -logits gives them); scores = exp(l - l_max) / sum over the
+    selected, which is the full softmax renormalised over the selected K."""
+    g = np.random.default_rng(3)
+    T, E, K = 64, 96, 6
+    lg = g.standard_normal((T, E)).astype(np.float32)
+    lg[5, 10] = lg[5, 3] = lg[5].max() + 1.0            # an exact tie at the top
+    lg[7, :] = 0.5                                       # all equal
+    ids, w = O.route_topk(lg, K)
+    ref_ids = np.argsort(-lg, axis=1, kind="stable")[:, :K]
+    assert np.array_equal(ids, ref_ids)
+    assert ids[5, 0] == 3 and ids[5, 1] == 10 and list(ids[7]) == list(range(K))
+    full = np.exp(lg.astype(np.float64) - lg.max(axis=1, keepdims=True))
+    full /= full.sum(axis=1, keepdims=True)
+    sel = np.take_along_axis(full, ref_ids, axis=1)
+    assert np.allclose(w, sel / sel.sum(axis=1, keepdims=True), rtol=1e-6, atol=0)
+    assert np.allclose(w.sum(axis=1), 1.0, atol=1e-6)
+    assert np.all(np.diff(w, axis=1) <= 0)
+    # top-1 always scores exactly 1
+    assert np.all(O.route_topk(lg, 1)[1] == 1.0)
