@@ -123,10 +123,15 @@ typedef struct {
   size_t x_perm;         /* W4A16: bf16[rows_cap][Hp] permuted token rows   */
   size_t act_bf16;       /* W4A16: bf16[rows_cap][Ip] activated FC1 rows    */
   size_t route;          /* bf16[rows_cap][Hp] per-route FC2 rows           */
+  size_t tile_sync;      /* int32[2][rows_cap/128] then f32[rows_cap]: per
+                            token tile the FC1 items stored and the FC2-input
+                            ready flag, per row the activated row's amax, of
+                            the one-launch FC1 -> FC2 path, taken when
+                            T*K <= min(2048, 8*E)                           */
 } moe_ws_layout;
 
 /* ABI version of this header (bumped on any incompatible change). */
-#define MOE_NVFP4_ABI_VERSION 1
+#define MOE_NVFP4_ABI_VERSION 2
 int32_t moe_nvfp4_abi_version(void);
 
 /* Human-readable text of a status code (static storage). */

@@ -1,24 +1,32 @@
 // gemm_w4a4.cu -- block-scaled NVFP4 x NVFP4 grouped GEMMs (FC1 with fused
-// activation, FC2) on tcgen05 tensor cores.
+// activation, FC2) on tcgen05 tensor cores, as separate launches or as one
+// persistent FC1 -> requant -> FC2 launch.
 //
 // Megatron-LM PR #8262, "Background" / "What is added": FC1 and FC2 are block-
 // scaled grouped GEMMs over expert groups; FC1's epilogue applies the expert
 // alpha and the per-token scale, then squared-ReLU or SwiGLU.  The FC2 input
 // requantization of each route row needs the row's amax over all of I, so the
-// FC1 epilogue writes the fp32 activated row and a row-parallel pass quantizes it.
+// FC1 epilogue writes the fp32 activated row and the row is quantized once the
+// whole tile is written: by a row-parallel pass between two launches, or, in
+// the fused launch, by a requant work item of the tile that waits for the
+// tile's FC1 items (the pages' MegaMoE keeps FC1 and FC2 in one persistent
+// kernel, FlashInfer PR #5019).
 //
 // Structure (swap-AB: weights are the M=128 operand, tokens the N operand, so a
 // decode-sized group of a few tokens does not waste a 128-row MMA):
 //   * persistent CTAs, one per SM; work item = (token tile of <= 128 rows of one
-//     expert, 128-row weight tile of that expert); each CTA starts with item
-//     blockIdx.x and then claims items from a global counter, and its roles
-//     receive them through a shared-memory ring
+//     expert, 128-row weight tile of that expert) of FC1 or of FC2; FC1 items are
+//     numbered first.  Each CTA starts with item blockIdx.x and then claims items
+//     from a global counter, and its roles receive them through a shared-memory
+//     ring
 //   * two TMA producers, each one thread, both filling every stage: warp 0
 //     claims the items and loads the weight tile (128 rows x 128 B, 128-byte
 //     swizzle) and its scale atoms; warp 10 loads the token tile (one to three
 //     boxes of 128/64/32/16 rows) and its scale atoms.  Each copy costs its
 //     issuing thread a few hundred cycles, so a stage is split between two
-//     threads and issued in as few copies as its shape allows.
+//     threads and issued in as few copies as its shape allows.  In the fused
+//     launch the token producer of an FC2 item first waits for its tile's
+//     requantized rows (the weight producer keeps streaming meanwhile).
 //   * warps 6-9: scale staging -- move each stage's E4M3 scale atoms from shared
 //     memory into that stage's TMEM scale slot with tcgen05.st, in the layout the
 //     block-scaled MMA reads (row r of a 128-row atom at lane r%32, column r/32,
@@ -26,16 +34,15 @@
 //   * warp 1: TMEM allocator and single-thread MMA issuer:
 //     tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X, K = 64 per
 //     instruction, N = the tile's token count rounded up to 16
-//   * warps 2-5: epilogue, one TMEM lane (= one weight row) per thread
+//   * warps 2-5: epilogue, one TMEM lane (= one weight row) per thread; each
+//     chunk of up to 32 tokens is staged in shared memory as [token][feature]
+//     rows and one thread writes it with TMA tensor stores
 //   * the shared-memory stage ring is sized at run time from the largest token
-//     tile of the launch (5 stages at 128 tokens, 9 at 16); two accumulator
+//     tile of the launch (5 stages at 128 tokens, 8 at 16); two accumulator
 //     buffers (four when no tile exceeds 64 tokens) let the epilogue of one tile
 //     overlap the MMAs of the next ones.
-//   * every mbarrier wait is bounded; on timeout the CTA records an error flag,
-//     drains its own copies and MMAs, frees TMEM and returns.
-//   * the epilogue stages each chunk of up to 32 tokens in shared memory as
-//     [token][feature] rows and one thread writes them with TMA tensor stores,
-//     so global writes are whole 16-byte sectors however few tokens a tile has
+//   * every wait is bounded; on timeout the CTA records an error flag, drains its
+//     own copies and MMAs, frees TMEM and returns.
 // SwiGLU: the stored FC1 rows interleave 64-row blocks [gate | up], so TMEM
 // lanes 0-63 hold gate rows and 64-127 the matching up rows; both halves are
 // staged in shared memory and all four epilogue warps apply silu(gate) * up.
@@ -48,6 +55,7 @@
 #include "gemm_common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace moe {
 
@@ -79,15 +87,116 @@ constexpr int kBarItemFull = kBarAccEmpty + kMaxAcc;
 constexpr int kBarItemEmpty = kBarItemFull + kItemSlots;
 constexpr int kBarDrain = kBarItemEmpty + kItemSlots;
 constexpr int kNumBars = kBarDrain + 1;
-constexpr int kFlagsOff = 8 * kNumBars;     // tmem slot, abort flag, epilogue stop flag
+constexpr int kFlagsOff = 8 * kNumBars;     // tmem slot, abort flag, epilogue stop flag, requant flag
 constexpr int kRingOff = 768;               // kItemSlots int4
 static_assert(kFlagsOff + 16 <= kRingOff && kRingOff + 16 * kItemSlots <= 1024, "flag area");
 }  // namespace w4a4
 
-template <int MODE>
+// ---------------------------------------------------------------- work items
+// FC1 items [0, n1), then (fused launch) one requant item per token tile
+// [n1, n1 + nr), then FC2 items [n1 + nr, n1 + nr + n2).  Within a GEMM phase
+// the numbering of tile_decode (an expert's token tiles for one weight tile side
+// by side).  Every item waits only on lower-numbered items.  (Interleaving the
+// phases per tile was measured slower: a CTA whose FC2 item waits holds FC1
+// items it has already claimed, and the waits chain up.)  The phase (0 FC1, 1
+// FC2, 2 requant) rides in bits 16.. of TileInfo::mt.
+constexpr int kPhaseRequant = 2;
+struct ItemSpace {
+  int n1, nr, n2, m1, m2;
+};
+__device__ __forceinline__ int4 item_raw(const W4A4Args& a, const ItemSpace& sp, int item) {
+  if (item >= sp.n1 + sp.nr + sp.n2) return make_int4(0, 0, 1, 0);
+  if (item < sp.n1) return a.tiles[item / sp.m1];
+  if (item < sp.n1 + sp.nr) return a.tiles[item - sp.n1];
+  return a.tiles[(item - sp.n1 - sp.nr) / sp.m2];
+}
+__device__ __forceinline__ TileInfo item_decode(const ItemSpace& sp, int item, const int4& t) {
+  if (item >= sp.n1 + sp.nr + sp.n2) return TileInfo{0, 0, 0, 0};
+  if (item >= sp.n1 && item < sp.n1 + sp.nr) {
+    const int tt = item - sp.n1;
+    return TileInfo{t.x, tt, kPhaseRequant << 16, min(kTileRows, t.w - kTileRows * (tt - t.y))};
+  }
+  const int ph = item >= sp.n1 ? 1 : 0;
+  const int m = ph ? sp.m2 : sp.m1;
+  const int local = (ph ? item - sp.n1 - sp.nr : item) - m * t.y;
+  const int j = local % t.z;
+  return TileInfo{t.x, t.y + j, (local / t.z) | (ph << 16), min(kTileRows, t.w - kTileRows * j)};
+}
+
+// Block pass of the fused requant: the tile's rows x Ip/16 blocks of 16 values
+// spread over 128 threads, two blocks in flight per thread (loads first, then the
+// quantization and the stores).  row_amax: per-row amax, or anything non-zero
+// for the static-scale recipe.  Same arithmetic as requant_row_warp.
+__device__ __forceinline__ void requant_blocks(const float* __restrict__ act0, int Ip, int rows,
+                                               int row0, const float* __restrict__ row_amax,
+                                               const float* __restrict__ static_enc,
+                                               uint8_t* __restrict__ qc, uint8_t* __restrict__ qsf,
+                                               int et) {
+  const int nb = Ip / 16;  // blocks per row
+  const uint32_t c16 = (uint32_t)nb;
+  const int total = rows * nb;
+  for (int b0 = et; b0 < total; b0 += 256) {
+    float v[2][16];
+    int rr[2], jj[2];
+    bool have[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int b = b0 + 128 * u;
+      have[u] = b < total;
+      rr[u] = have[u] ? b / nb : 0;
+      jj[u] = have[u] ? b - rr[u] * nb : 0;
+      if (have[u]) {
+        const float4* src = reinterpret_cast<const float4*>(act0 + (size_t)rr[u] * Ip) + 4 * jj[u];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 f = src[i];
+          v[u][4 * i] = f.x;
+          v[u][4 * i + 1] = f.y;
+          v[u][4 * i + 2] = f.z;
+          v[u][4 * i + 3] = f.w;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (!have[u]) continue;
+      const uint64_t p = (uint64_t)(row0 + rr[u]);
+      const float mm = row_amax[rr[u]];
+      uint2* crow = reinterpret_cast<uint2*>(qc + p * (uint64_t)(Ip / 2));
+      if (mm == 0.0f) {
+        crow[jj[u]] = make_uint2(0u, 0u);
+        qsf[sf_offset(p, jj[u], c16)] = 0;
+        continue;
+      }
+      const float enc = static_enc ? *static_enc : __fdiv_rn(kRecipeMax, mm);
+      uint2 qv;
+      qsf[sf_offset(p, jj[u], c16)] = (uint8_t)quant_block16(v[u], enc, qv);
+      crow[jj[u]] = qv;
+    }
+  }
+}
+
+// Bounded wait for another CTA's flag to reach `target` (acquire); records a
+// timeout like the mbarrier waits.
+__device__ __forceinline__ bool wait_flag_geq(const int32_t* flag, int target,
+                                              volatile int* abort_flag, int32_t* status) {
+  if (ld_acquire_gpu(flag) >= target) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    __nanosleep(128);
+    if (ld_acquire_gpu(flag) >= target) return true;
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      atomicOr(status + kStatusFlags, kFlagWaitTimeout);
+      return false;
+    }
+  }
+}
+
+template <int ACT>
 __global__ void __launch_bounds__(w4a4::kThreads, 1)
-    gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ TokenMaps tmB,
-                     const __grid_constant__ CUtensorMap tmO, const GemmArgs a) {
+    gemm_w4a4_kernel(const __grid_constant__ W4A4Maps maps, const __grid_constant__ W4A4Args a) {
   using namespace w4a4;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -96,6 +205,7 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kFlagsOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* epi_stop = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  volatile int* rq_flag = reinterpret_cast<volatile int*>(tmem_slot + 3);
   const ItemQueue Q{reinterpret_cast<int4*>(smem + kRingOff), R.bar(kBarItemFull),
                     R.bar(kBarItemEmpty)};
   float* s_scale = reinterpret_cast<float*>(smem + 1024);  // row scales of the current tile (128)
@@ -121,10 +231,14 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
     mbar_init(R.bar(kBarDrain), 1);
     *abort_flag = 0;
     *epi_stop = 0;
+    *rq_flag = 0;
     fence_barrier_init();
-    prefetch_tmap(&tmA);
-    for (int i = 0; i < 4; ++i) prefetch_tmap(&tmB.box[i]);
-    prefetch_tmap(&tmO);
+    for (int p = 0; p < 2; ++p) {
+      if (!(p ? a.run_fc2 : a.run_fc1)) continue;
+      prefetch_tmap(&maps.a[p]);
+      for (int i = 0; i < 4; ++i) prefetch_tmap(&maps.b[p].box[i]);
+      prefetch_tmap(&maps.o[p]);
+    }
   }
   __syncwarp();  // thread 0's set-up branch rejoins its warp before the barrier
   if (warp == 1) {
@@ -138,7 +252,11 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
   pdl_wait();
   pdl_trigger();
 
-  const int n_items = a.status[kStatusTiles] * a.m_tiles;
+  const int n_tiles = a.status[kStatusTiles];
+  const ItemSpace sp{a.run_fc1 ? n_tiles * a.ph[0].m_tiles : 0, a.fused ? n_tiles : 0,
+                     a.run_fc2 ? n_tiles * a.ph[1].m_tiles : 0, a.ph[0].m_tiles,
+                     a.ph[1].m_tiles};
+  const int n_items = sp.n1 + sp.nr + sp.n2;
 
   // ---- geometry from the largest token tile (<= 128 rows) of this launch
   const int max_n16 = (a.status[kStatusMaxRows] + 15) & ~15;
@@ -153,12 +271,8 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
   if (n_stages > kMaxStages) n_stages = kMaxStages;
   while (n_stages > 2 && sf_base + n_stages * slot_cols > kTmemCols) --n_stages;
 
-  const int kblocks = a.K / kBK;
-  const int atoms = a.K / 64;                          // scale atoms per 128-row block
-  const size_t plane = (size_t)a.w_rows * (a.K / 16);  // weight scale bytes per expert
-
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ weight producer
     if (lane == 0) {
       int last_par[kMaxStages];
 #pragma unroll
@@ -172,19 +286,30 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
       // the raw values are only used an item later, so neither the atomic's nor
       // the load's latency stalls the copy stream.
       int item = blockIdx.x;
-      TileInfo cur = tile_info(a, item, n_items);        // rows == 0 past the end
+      TileInfo cur = item_decode(sp, item, item_raw(a, sp, item));  // rows == 0 past the end
       int next = (int)gridDim.x + (item < n_items ? atomicAdd(a.item_counter, 1) : n_items);
-      int4 next_raw = tile_raw(a, next, n_items);
+      int4 next_raw = item_raw(a, sp, next);
       int claim = next < n_items ? atomicAdd(a.item_counter, 1) : n_items;  // raw counter value
       while (ok) {
         if (!queue_push(Q, qp, cur, abort_flag, a.status) || cur.rows == 0) break;
         const int next2 = (int)gridDim.x + claim;         // claimed one item ago
-        const int4 next2_raw = tile_raw(a, next2, n_items);
+        const int4 next2_raw = item_raw(a, sp, next2);
         claim = next2 < n_items ? atomicAdd(a.item_counter, 1) : n_items;
-        const TileInfo nxt = tile_decode(a, next, n_items, next_raw);  // loaded one item ago
-        // claim the next item now so the atomic's latency hides behind this one
-        const int a_row = cur.e * a.w_rows + cur.mt * 128;
-        const uint8_t* sfa0 = a.sfa + (size_t)cur.e * plane + (size_t)cur.mt * atoms * kAtom;
+        const TileInfo nxt = item_decode(sp, next, next_raw);  // loaded one item ago
+        const int ph = cur.mt >> 16, mt = cur.mt & 0xFFFF;
+        if (ph == kPhaseRequant) {  // no stages: the epilogue warps do it alone
+          cur = nxt;
+          next = next2;
+          next_raw = next2_raw;
+          continue;
+        }
+        const W4A4Phase& P = a.ph[ph];
+        const int kblocks = P.K / kBK;
+        const int atoms = P.K / 64;                              // scale atoms per 128-row block
+        const size_t plane = (size_t)P.w_rows * (P.K / 16);      // weight scale bytes per expert
+        const int a_row = cur.e * P.w_rows + mt * 128;
+        const uint8_t* sfa0 = P.sfa + (size_t)cur.e * plane + (size_t)mt * atoms * kAtom;
+        const CUtensorMap* tmA = &maps.a[ph];
         constexpr uint32_t tx = kABytes + kSfaBytes;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!wait_or_abort(R.bar(kBarEmpty + stage), phase ^ 1, abort_flag, a.status)) {
@@ -194,7 +319,7 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
           uint8_t* sb = stages + stage * stage_bytes;
           const uint32_t full = R.bar(kBarFull + stage);
           mbar_expect_tx(full, tx);
-          tma_load_2d_hint(smem_u32(sb), &tmA, full, kb * kRowBytes, a_row, pol_w);
+          tma_load_2d_hint(smem_u32(sb), tmA, full, kb * kRowBytes, a_row, pol_w);
           bulk_load(smem_u32(sb + off_sfa), sfa0 + (size_t)(kb * 4) * kAtom, 4 * kAtom, full);
           last_par[stage] = (int)phase;
           if (++stage == n_stages) {
@@ -222,9 +347,23 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
       while (ok) {
         const TileInfo cur = queue_pop_thread(Q, qp, abort_flag, a.status);
         if (cur.rows == 0) break;
+        const int ph = cur.mt >> 16;
+        if (ph == kPhaseRequant) continue;
+        const W4A4Phase& P = a.ph[ph];
+        if (a.fused && ph == 1) {
+          // the tile's FC2 input is written by another CTA's epilogue (generic
+          // stores); acquire it, then order it before this thread's TMA reads
+          if (!wait_flag_geq(a.rq_done + cur.tt, 1, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();
+        }
+        const int kblocks = P.K / kBK;
+        const int atoms = P.K / 64;
         const int n16 = (cur.rows + 15) & ~15;
         const int b_row = cur.tt * kTileRows;
-        const uint8_t* sfb0 = a.sfb + (size_t)cur.tt * atoms * kAtom;
+        const uint8_t* sfb0 = P.sfb + (size_t)cur.tt * atoms * kAtom;
         const uint32_t tx = n16 * kRowBytes + 4 * kAtom;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!wait_or_abort(R.bar(kBarEmpty + stage), phase ^ 1, abort_flag, a.status)) {
@@ -238,7 +377,7 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
             // largest box that still fits the rows left: n16 in 1-3 copies
             const int rem = n16 - r0;
             const int lg = rem >= 128 ? 3 : rem >= 64 ? 2 : rem >= 32 ? 1 : 0;
-            tma_load_2d_hint(smem_u32(sb + off_b + r0 * kRowBytes), &tmB.box[lg], full,
+            tma_load_2d_hint(smem_u32(sb + off_b + r0 * kRowBytes), &maps.b[ph].box[lg], full,
                              kb * kRowBytes, b_row + r0, pol_x);
             r0 += 16 << lg;
           }
@@ -264,6 +403,8 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
     while (ok) {
       const TileInfo cur = queue_pop_warp(Q, qp, abort_flag, a.status);
       if (cur.rows == 0) break;
+      if ((cur.mt >> 16) == kPhaseRequant) continue;
+      const int kblocks = a.ph[cur.mt >> 16].K / kBK;
       for (int kb = 0; kb < kblocks; ++kb) {
         if (!wait_or_abort(R.bar(kBarFull + stage), phase, abort_flag, a.status)) {
           ok = false;
@@ -297,6 +438,8 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
       while (ok) {
         const TileInfo cur = queue_pop_thread(Q, qp, abort_flag, a.status);
         if (cur.rows == 0) break;
+        if ((cur.mt >> 16) == kPhaseRequant) continue;
+        const int kblocks = a.ph[cur.mt >> 16].K / kBK;
         const int n16 = (cur.rows + 15) & ~15;
         const uint32_t idesc = idesc_mxf4nvf4(128, n16);
         const int buf = local % nbuf;
@@ -356,30 +499,78 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
     int local = 0;
     int eb = 0;                              // staging buffer of the next chunk
     QueuePos qp;
+    // row scale of this thread's token column in an item; in the fused launch the
+    // FC2 row scales come from another CTA and are read once the tile is released
+    auto row_scale = [&](const TileInfo& t) -> float {
+      const int ph = t.mt >> 16;
+      if (!t.rows || r >= ((t.rows + 15) & ~15) || ph == kPhaseRequant || (a.fused && ph == 1))
+        return 0.0f;
+      return a.ph[ph].row_scale[(size_t)t.tt * kTileRows + r];
+    };
     TileInfo cur = queue_pop_warp(Q, qp, abort_flag, a.status);
-    float s_r = 0.0f;
-    if (cur.rows && r < ((cur.rows + 15) & ~15)) s_r = a.row_scale[(size_t)cur.tt * kTileRows + r];
+    float s_r = row_scale(cur);
     while (true) {
-      const int mt = cur.mt;
+      if ((cur.mt >> 16) == kPhaseRequant) {
+        // FC2-input requant of one token tile: wait until all its FC1 items are
+        // stored (their epilogues also folded every row's amax), then quantize
+        // the 16-element blocks spread over the 128 threads; the arithmetic of
+        // requant_row_warp.
+        const int tt = cur.tt, rows = cur.rows, row0 = tt * kTileRows, Ip = a.Ip;
+        if (issuer)
+          *rq_flag = wait_flag_geq(a.fc1_done + tt, a.ph[0].m_tiles, abort_flag, a.status);
+        named_bar_sync(1, 128);
+        if (!*rq_flag) break;  // timed out: the abort flag is set
+        fence_acq_rel_gpu();
+        const float* act0 = a.act + (size_t)row0 * Ip;
+        if (et < rows) {
+          // the row amax that the tile's FC1 epilogues folded together
+          const float mm = a.a2_static ? 1.0f : __uint_as_float(ld_acquire_gpu(
+                                                    reinterpret_cast<const int32_t*>(a.row_amax) +
+                                                    row0 + et));
+          s_scale[et] = mm;
+          a.qs[row0 + et] = a.a2_static ? 1.0f : (mm == 0.0f ? 0.0f : __fmul_rn(mm, kRecipeInv));
+        }
+        named_bar_sync(1, 128);
+        requant_blocks(act0, Ip, rows, row0, s_scale, a.a2_static, a.qc, a.qsf, et);
+        fence_proxy_async_global();  // the FC2 producers read these rows with TMA
+        named_bar_sync(1, 128);
+        if (issuer) {
+          fence_acq_rel_gpu();
+          st_release_gpu(a.rq_done + tt, 1);
+        }
+        cur = queue_pop_warp(Q, qp, abort_flag, a.status);
+        s_r = row_scale(cur);
+        continue;
+      }
+      const int ph = cur.mt >> 16;
+      const int mt = cur.mt & 0xFFFF;
+      const int tt = cur.tt;
       const int rows = cur.rows;
       const int n16 = (rows + 15) & ~15;
-      const int row0 = cur.tt * kTileRows;
+      const int row0 = tt * kTileRows;
       const int buf = local % nbuf;
       const uint32_t acc_par = (uint32_t)(local / nbuf) & 1u;
-      const float alpha = rows ? a.alpha[cur.e] : 0.0f;
+      const float alpha = rows ? a.ph[ph].alpha[cur.e] : 0.0f;
       // all four epilogue warps take the same stop decision, so none is left
       // waiting alone at a named barrier; the first barrier also ends every
       // read of the previous tile's staged scales
       if (rows == 0 || !wait_or_abort(R.bar(kBarAccFull + buf), acc_par, abort_flag, a.status))
         *epi_stop = 1;
+      if (rows && a.fused && ph == 1 && r < n16) {
+        // the tile's FC2 input (and its row scales) were released before its
+        // MMAs ran; acquire the release on this thread too
+        if (wait_flag_geq(a.rq_done + tt, 1, abort_flag, a.status))
+          s_r = a.ph[1].row_scale[(size_t)row0 + r];
+        else
+          *epi_stop = 1;
+      }
       named_bar_sync(1, 128);
       s_scale[r] = s_r;
       const bool stop = *epi_stop != 0;
       named_bar_sync(1, 128);
       if (stop) break;
       cur = queue_pop_warp(Q, qp, abort_flag, a.status);  // the next item (rows 0: end)
-      s_r = 0.0f;
-      if (cur.rows && r < ((cur.rows + 15) & ~15)) s_r = a.row_scale[(size_t)cur.tt * kTileRows + r];
+      s_r = row_scale(cur);
       tc_fence_after();
       const uint32_t acc = tmem + lane_addr + buf * acc_stride;
       for (int c0 = 0; c0 < n16; c0 += 32) {
@@ -410,7 +601,14 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
         }
         int out_x;                           // first output feature of the tile
         uint32_t box_bytes;                  // bytes of one staged token row
-        if constexpr (MODE == kFc1Swiglu) {
+        if (ph == 1) {
+          uint16_t* o = reinterpret_cast<uint16_t*>(ob);
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < ncol) o[j * 128 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(y[j]));
+          out_x = mt * 128;
+          box_bytes = 128 * 2;
+        } else if constexpr (ACT == kFc1Swiglu) {
           // lanes 0-63: gate rows of features mt*64 + (r & 63); lanes 64-127: up rows
           float* g = reinterpret_cast<float*>(ob);
           float* u = g + 32 * 64;
@@ -435,7 +633,7 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
                   __fmul_rn(__fdividef(yg[k], __fadd_rn(1.0f, __expf(-yg[k]))), yu[k]);
           out_x = mt * 64;
           box_bytes = 64 * 4;
-        } else if constexpr (MODE == kFc1Relu2) {
+        } else {
           float* o = reinterpret_cast<float*>(ob);
 #pragma unroll
           for (int j = 0; j < 32; ++j)
@@ -445,29 +643,48 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
             }
           out_x = mt * 128;
           box_bytes = 128 * 4;
-        } else {
-          uint16_t* o = reinterpret_cast<uint16_t*>(ob);
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < ncol) o[j * 128 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(y[j]));
-          out_x = mt * 128;
-          box_bytes = 128 * 2;
         }
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
         if (issuer) {
           for (int p = 0; p < ncol; p += 16)
-            tma_store_2d(&tmO, smem_u32(ob + p * box_bytes), out_x, row0 + c0 + p);
+            tma_store_2d(&maps.o[ph], smem_u32(ob + p * box_bytes), out_x, row0 + c0 + p);
           bulk_commit_group();
+        }
+        if (a.fused && ph == 0 && !a.a2_static) {
+          // this item's part of each token's row amax (the FC2-input scale): four
+          // threads per staged token row, |value| maxima folded with fmaxf as the
+          // stand-alone requant does, then one atomic max per row (non-negative
+          // floats order like their bit patterns)
+          const int j = et >> 2, part = et & 3;
+          const int nf = box_bytes / 4;  // staged features per token: 64 or 128
+          const float* srow = reinterpret_cast<const float*>(ob) + j * nf + part * (nf / 4);
+          float mx = 0.0f;
+          for (int k = 0; k < nf / 4; ++k) mx = fmaxf(mx, fabsf(srow[k]));
+          mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+          if (part == 0 && c0 + j < rows)
+            atomicMax(reinterpret_cast<unsigned int*>(a.row_amax) + row0 + c0 + j,
+                      __float_as_uint(mx));
         }
         eb ^= 1;
       }
       ++local;
+      if (a.fused && ph == 0) {
+        // count this FC1 item of the tile once its rows (and its part of the row
+        // maxima) are in global memory
+        named_bar_sync(1, 128);
+        if (issuer) {
+          bulk_wait_group<0>();
+          fence_proxy_async_global();
+          atom_add_acq_rel_gpu(a.fc1_done + tt, 1);
+        }
+      }
     }
     if (issuer) bulk_wait_group<0>();  // every store has completed before the CTA ends
   }
 
-  // Lane 0 of warps 0 and 1 ran its role alone; the warp reconverges before
+  // Lane 0 of warps 0, 1 and 10 ran its role alone; the warp reconverges before
   // the CTA barrier (bar.sync is a per-warp, aligned barrier), so TMEM is
   // released only after every role has finished.
   __syncwarp();
@@ -479,28 +696,24 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
   }
 }
 
-template <int MODE>
-static cudaError_t launch_mode(const CUtensorMap& tmA, const TokenMaps& tmB, const CUtensorMap& tmO,
-                               const GemmArgs& a, int grid, cudaStream_t s) {
+template <int ACT>
+static cudaError_t launch_act(const W4A4Maps& maps, const W4A4Args& a, int grid, cudaStream_t s) {
   static bool configured = false;  // the attribute is per function
   if (!configured) {
-    cudaError_t err = cudaFuncSetAttribute(gemm_w4a4_kernel<MODE>,
+    cudaError_t err = cudaFuncSetAttribute(gemm_w4a4_kernel<ACT>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            w4a4::kSmemBytes);
     if (err != cudaSuccess) return err;
     configured = true;
   }
-  return launch_pdl(gemm_w4a4_kernel<MODE>, dim3(grid), dim3(w4a4::kThreads),
-                    (size_t)w4a4::kSmemBytes, s, tmA, tmB, tmO, a);
+  return launch_pdl(gemm_w4a4_kernel<ACT>, dim3(grid), dim3(w4a4::kThreads),
+                    (size_t)w4a4::kSmemBytes, s, maps, a);
 }
 
-cudaError_t launch_gemm_w4a4(const CUtensorMap& tmA, const TokenMaps& tmB, const CUtensorMap& tmO,
-                             const GemmArgs& a, int grid, cudaStream_t s) {
-  switch (a.mode) {
-    case kFc1Relu2: return launch_mode<kFc1Relu2>(tmA, tmB, tmO, a, grid, s);
-    case kFc1Swiglu: return launch_mode<kFc1Swiglu>(tmA, tmB, tmO, a, grid, s);
-    default: return launch_mode<kFc2>(tmA, tmB, tmO, a, grid, s);
-  }
+cudaError_t launch_gemm_w4a4(const W4A4Maps& maps, const W4A4Args& a, int act, int grid,
+                             cudaStream_t s) {
+  return act == kFc1Swiglu ? launch_act<kFc1Swiglu>(maps, a, grid, s)
+                           : launch_act<kFc1Relu2>(maps, a, grid, s);
 }
 
 }  // namespace moe

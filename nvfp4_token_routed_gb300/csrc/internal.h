@@ -12,6 +12,11 @@ namespace moe {
 // Rows of one token tile of the grouped GEMMs.  Every expert group in the
 // permuted buffers starts at a multiple of this, so a tile has one expert.
 constexpr int kTileRows = 128;
+// Batches of at most this many routes, and at most kFusedRoutesPerExpert routes
+// per expert on average, run FC1 -> requant -> FC2 as one launch (measured on
+// GB300: 2-11% faster at 1-4 routes per expert, 4% slower at 16).
+constexpr int64_t kFusedMaxRoutes = 2048;
+constexpr int64_t kFusedRoutesPerExpert = 8;
 
 // Workspace status words (int32).
 constexpr int kStatusFlags = 0;   // error bits, see below
@@ -36,6 +41,8 @@ struct RouteArgs {
   int32_t* counts;
   int32_t* group_row0;
   int4* tiles;  // per token tile: {expert, expert's first tile, expert's tiles, expert's routes}
+  int32_t* tile_sync;     // fused GEMM: per-tile counters zeroed by the scan (or null)
+  int tile_sync_words;
   int32_t* inv;
   int32_t* perm;
   // W4A4 gather
@@ -106,17 +113,57 @@ void launch_requant(int TK, int I, const int32_t* inv, const float* act, uint8_t
                     float* qs, const float* static_enc, cudaStream_t s);
 void launch_finalize(int T, int K, int H, int Hp, const int32_t* inv, const float* w,
                      const void* route, void* out, cudaStream_t s);
+// One GEMM of the W4A4 kernel (FC1 or FC2).
+struct W4A4Phase {
+  int K;                   // reduction length (Hp for FC1, Ip for FC2)
+  int m_tiles;             // 128-row weight tiles per expert
+  int w_rows;              // weight rows per expert
+  const uint8_t* sfa;      // weight scales, swizzled, [E][w_rows * K/16]
+  const uint8_t* sfb;      // token scales, swizzled over permuted rows
+  const float* alpha;      // [E]
+  const float* row_scale;  // per permuted row: s_t (FC1) or s2 (FC2)
+};
+
+// Arguments of one W4A4 GEMM launch: FC1 items, FC2 items, or both.  Fused
+// (both phases, one launch): the epilogue that stores a token tile's last FC1
+// item requantizes that tile's rows and releases rq_done[tile]; the token
+// producer of an FC2 item waits for it.  Items are claimed in order, FC1 items
+// first, and every wait is on a lower-numbered item, so the launch always makes
+// progress while its CTAs are resident.
+struct W4A4Args {
+  W4A4Phase ph[2];          // [0] FC1, [1] FC2
+  int run_fc1, run_fc2, fused;
+  const int4* tiles;        // per token tile: {expert, first tile, tiles, routes}
+  int32_t* status;
+  int32_t* item_counter;    // items claimed beyond the first gridDim.x (zeroed by the scan)
+  int32_t* fc1_done;        // fused: per token tile, FC1 items whose rows are stored
+  int32_t* rq_done;         // fused: per token tile, 1 once its FC2 input is quantized
+  float* row_amax;          // fused: per permuted row, amax of the activated row (atomic max)
+  const float* act;         // fused requant: fp32 activated rows [rows][Ip]
+  int Ip;
+  uint8_t* qc;              // FC2-input codes [rows][Ip/2]
+  uint8_t* qsf;             // FC2-input scales, swizzled
+  float* qs;                // FC2-input row scales
+  const float* a2_static;   // per-tensor recipe: static FC2-input encode scale (else null)
+};
+
 // Token-tile tensor maps of one operand: the same [rows][row_bytes] buffer with
 // boxes of 16, 32, 64 and 128 rows (128-byte swizzle), so that a tile of n rows
 // (a multiple of 16) arrives in at most three copies.
 struct TokenMaps {
   CUtensorMap box[4];
 };
-// tmO: the output rows as TMA store target, 16-row boxes of the tile's features
-// (FC1 ReLU2: fp32 x 128 of act_out; SwiGLU: fp32 x 64 of act_out; FC2: bf16 x
-// 128 of route_out).
-cudaError_t launch_gemm_w4a4(const CUtensorMap& tmA, const TokenMaps& tmB, const CUtensorMap& tmO,
-                             const GemmArgs& a, int grid, cudaStream_t s);
+// Tensor maps of both phases: weights, tokens (four box heights) and the output
+// rows as TMA store target, 16-row boxes of the tile's features (FC1 ReLU2: fp32
+// x 128 of act; SwiGLU: fp32 x 64 of act; FC2: bf16 x 128 of the route rows).
+struct W4A4Maps {
+  CUtensorMap a[2];
+  TokenMaps b[2];
+  CUtensorMap o[2];
+};
+// act: kFc1Relu2 or kFc1Swiglu (the FC1 epilogue; FC2 items need no choice).
+cudaError_t launch_gemm_w4a4(const W4A4Maps& maps, const W4A4Args& a, int act, int grid,
+                             cudaStream_t s);
 // W4A16: tmA over packed weights (128-byte boxes, 128-byte swizzle), tmB over bf16
 // token rows (128-byte boxes, 128-byte swizzle); route_out receives the bf16
 // activated rows (FC1, row stride I) or the bf16 route rows (FC2, stride H).

@@ -113,6 +113,7 @@ void compute_layout(const moe_dims* d, int32_t T, int32_t K, int32_t w4a16, moe_
     L->act_bf16 = take(sizeof(uint16_t) * (size_t)rows * I);
   }
   L->route = take(sizeof(uint16_t) * (size_t)rows * H);
+  L->tile_sync = take(sizeof(int32_t) * (2 * (size_t)(tiles ? tiles : 1) + (size_t)rows));
   L->total = off;
 }
 
@@ -379,18 +380,25 @@ static moe_status forward_w4a4_impl(const moe_dims* d, const moe_nvfp4_weights* 
   // padded sizes: stored weights, token rows and every workspace row
   const int H = (int)hp_of(d), I = (int)ip_of(d), N1 = (int)n1p_of(d);
 
-  CUtensorMap tmA1, tmA2, tmO1, tmO2;
-  TokenMaps tmB1, tmB2;
+  W4A4Maps maps;
   const bool swiglu = d->act == MOE_ACT_SWIGLU;
-  if (!make_tmap_bytes(&tmA1, w->fc1_codes, H / 2, (uint64_t)d->E * N1, 128) ||
-      !make_token_maps(&tmB1, at<uint8_t>(ws, L.xq_codes), H / 2, L.rows_cap) ||
-      !make_tmap_out(&tmO1, at<float>(ws, L.act), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, I,
+  if (!make_tmap_bytes(&maps.a[0], w->fc1_codes, H / 2, (uint64_t)d->E * N1, 128) ||
+      !make_token_maps(&maps.b[0], at<uint8_t>(ws, L.xq_codes), H / 2, L.rows_cap) ||
+      !make_tmap_out(&maps.o[0], at<float>(ws, L.act), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, I,
                      L.rows_cap, swiglu ? 64 : 128, 16) ||
-      !make_tmap_bytes(&tmA2, w->fc2_codes, I / 2, (uint64_t)d->E * H, 128) ||
-      !make_token_maps(&tmB2, at<uint8_t>(ws, L.fc2q_codes), I / 2, L.rows_cap) ||
-      !make_tmap_out(&tmO2, at<uint16_t>(ws, L.route), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H,
+      !make_tmap_bytes(&maps.a[1], w->fc2_codes, I / 2, (uint64_t)d->E * H, 128) ||
+      !make_token_maps(&maps.b[1], at<uint8_t>(ws, L.fc2q_codes), I / 2, L.rows_cap) ||
+      !make_tmap_out(&maps.o[1], at<uint16_t>(ws, L.route), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H,
                      L.rows_cap, 128, 16))
     return MOE_ERR_CUDA;
+
+  // Decode-sized batches with few routes per expert run FC1, the FC2-input
+  // requant and FC2 as one persistent launch (no launch gaps, no FC1 tail before
+  // FC2 starts); other batches run them as three launches, where the requant is
+  // one wide pass.  Both compute the same bits.
+  const int64_t tiles_cap = L.rows_cap / kTileRows;
+  const int64_t TK = (int64_t)T * K;
+  const bool fused = TK <= kFusedMaxRoutes && TK <= kFusedRoutesPerExpert * d->E;
 
   mark(0, s);
   RouteArgs r = route_args(d, T, K, topk_ids, ws, L, 0);
@@ -400,49 +408,55 @@ static moe_status forward_w4a4_impl(const moe_dims* d, const moe_nvfp4_weights* 
   r.pc = at<uint8_t>(ws, L.xq_codes);
   r.psf = at<uint8_t>(ws, L.xq_sf);
   r.ps = at<float>(ws, L.xq_scale);
+  if (fused) {
+    r.tile_sync = at<int32_t>(ws, L.tile_sync);
+    r.tile_sync_words = (int)(2 * tiles_cap + L.rows_cap);
+  }
   launch_route(r, s);
   mark(1, s);
 
-  const int64_t tiles_cap = L.rows_cap / kTileRows;
-  GemmArgs g{};
-  g.mode = d->act == MOE_ACT_SWIGLU ? kFc1Swiglu : kFc1Relu2;
-  g.K = H;
-  g.m_tiles = N1 / 128;
-  g.w_rows = N1;
-  g.sfa = w->fc1_sf;
-  g.sfb = at<uint8_t>(ws, L.xq_sf);
-  g.alpha = w->fc1_alpha;
-  g.row_scale = at<float>(ws, L.xq_scale);
+  W4A4Args g{};
+  g.ph[0] = W4A4Phase{H, N1 / 128, N1, w->fc1_sf, at<uint8_t>(ws, L.xq_sf), w->fc1_alpha,
+                      at<float>(ws, L.xq_scale)};
+  g.ph[1] = W4A4Phase{I, H / 128, H, w->fc2_sf, at<uint8_t>(ws, L.fc2q_sf), w->fc2_alpha,
+                      at<float>(ws, L.fc2q_scale)};
   g.tiles = at<int4>(ws, L.tiles);
   g.status = at<int32_t>(ws, L.status);
   g.item_counter = g.status + kStatusItemCtr;
-  g.act_out = at<float>(ws, L.act);
-  g.I = I;
-  g.H = H;
-  int grid = (int)std::min<int64_t>(sms, tiles_cap * g.m_tiles);
-  if (launch_gemm_w4a4(tmA1, tmB1, tmO1, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
-  mark(2, s);
-
-  launch_requant(T * K, I, at<int32_t>(ws, L.inv), at<float>(ws, L.act),
-                 at<uint8_t>(ws, L.fc2q_codes), at<uint8_t>(ws, L.fc2q_sf),
-                 at<float>(ws, L.fc2q_scale), a2_static, s);
-  mark(3, s);
-
-  GemmArgs g2 = g;
-  g2.mode = kFc2;
-  g2.K = I;
-  g2.m_tiles = H / 128;
-  g2.w_rows = H;
-  g2.sfa = w->fc2_sf;
-  g2.sfb = at<uint8_t>(ws, L.fc2q_sf);
-  g2.alpha = w->fc2_alpha;
-  g2.row_scale = at<float>(ws, L.fc2q_scale);
-  g2.act_out = nullptr;
-  g2.item_counter = g.status + kStatusItemCtr + 1;
-  g2.route_out = at<uint16_t>(ws, L.route);
-  grid = (int)std::min<int64_t>(sms, tiles_cap * g2.m_tiles);
-  if (launch_gemm_w4a4(tmA2, tmB2, tmO2, g2, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
-  mark(4, s);
+  g.fc1_done = at<int32_t>(ws, L.tile_sync);
+  g.rq_done = g.fc1_done + tiles_cap;
+  g.row_amax = reinterpret_cast<float*>(g.rq_done + tiles_cap);
+  g.act = at<float>(ws, L.act);
+  g.Ip = I;
+  g.qc = at<uint8_t>(ws, L.fc2q_codes);
+  g.qsf = at<uint8_t>(ws, L.fc2q_sf);
+  g.qs = at<float>(ws, L.fc2q_scale);
+  g.a2_static = a2_static;
+  const int act = swiglu ? kFc1Swiglu : kFc1Relu2;
+  if (fused) {
+    g.run_fc1 = g.run_fc2 = g.fused = 1;
+    const int grid = (int)std::min<int64_t>(sms, tiles_cap * (g.ph[0].m_tiles + g.ph[1].m_tiles));
+    if (launch_gemm_w4a4(maps, g, act, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
+    mark(2, s);
+    mark(3, s);
+    mark(4, s);
+  } else {
+    g.run_fc1 = 1;
+    int grid = (int)std::min<int64_t>(sms, tiles_cap * g.ph[0].m_tiles);
+    if (launch_gemm_w4a4(maps, g, act, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
+    mark(2, s);
+    launch_requant(T * K, I, at<int32_t>(ws, L.inv), at<float>(ws, L.act),
+                   at<uint8_t>(ws, L.fc2q_codes), at<uint8_t>(ws, L.fc2q_sf),
+                   at<float>(ws, L.fc2q_scale), a2_static, s);
+    mark(3, s);
+    W4A4Args g2 = g;
+    g2.run_fc1 = 0;
+    g2.run_fc2 = 1;
+    g2.item_counter = g.status + kStatusItemCtr + 1;
+    grid = (int)std::min<int64_t>(sms, tiles_cap * g2.ph[1].m_tiles);
+    if (launch_gemm_w4a4(maps, g2, act, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
+    mark(4, s);
+  }
 
   launch_finalize(T, K, d->H, H, at<int32_t>(ws, L.inv), topk_w, at<uint16_t>(ws, L.route),
                   out_bf16, s);

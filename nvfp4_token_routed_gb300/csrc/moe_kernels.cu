@@ -200,9 +200,11 @@ __global__ void __launch_bounds__(kChunk) route_count_kernel(const int32_t* __re
 __global__ void __launch_bounds__(1024) route_scan_kernel(
     int nchunks, int E, const int32_t* __restrict__ chunk_counts, int32_t* __restrict__ chunk_prefix,
     int32_t* __restrict__ counts, int32_t* __restrict__ group_row0, int4* __restrict__ tiles,
-    int32_t* __restrict__ status) {
+    int32_t* __restrict__ status, int32_t* __restrict__ tile_sync, int tile_sync_words) {
   pdl_wait();
   pdl_trigger();
+  // per-token-tile counters of the fused FC1 -> FC2 GEMM start at zero
+  for (int i = threadIdx.x; i < tile_sync_words; i += blockDim.x) tile_sync[i] = 0;
   const int e = threadIdx.x;
   int total = 0;
   if (e < E) {
@@ -323,7 +325,7 @@ void launch_route(const RouteArgs& a, cudaStream_t s) {
              a.E, a.chunk_counts);
   launch_pdl(route_scan_kernel, dim3(1), dim3(1024), 0, s, nchunks, a.E,
              (const int32_t*)a.chunk_counts, a.chunk_prefix, a.counts, a.group_row0, a.tiles,
-             a.status);
+             a.status, a.tile_sync, a.tile_sync_words);
   const size_t smem = sizeof(int) * (kChunk / 32) * a.E;
   launch_pdl(route_scatter_kernel, dim3(nchunks), dim3(kChunk), smem, s, a.ids, a.TK, a.E,
              (const int32_t*)a.chunk_prefix, (const int32_t*)a.group_row0, a.inv, a.perm);
@@ -358,42 +360,7 @@ __global__ void __launch_bounds__(256) requant_kernel(int TK, int I, const int32
   if (idx >= TK) return;
   const int p = inv[idx];
   if (p < 0) return;
-  const float4* row = reinterpret_cast<const float4*>(act + (size_t)p * I);
-  float m = 1.0f;
-  if (!static_enc) {
-    m = 0.0f;
-    for (int i = lane; i < I / 4; i += 32) {
-      const float4 v = row[i];
-      m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-    }
-    m = warp_max(m);
-  }
-  uint2* crow = reinterpret_cast<uint2*>(qc + (size_t)p * (I / 2));
-  const uint32_t c16 = (uint32_t)(I / 16);
-  if (m == 0.0f) {
-    for (int b = lane; b < I / 16; b += 32) {
-      crow[b] = make_uint2(0u, 0u);
-      qsf[sf_offset(p, b, c16)] = 0;
-    }
-    if (lane == 0) qs[p] = 0.0f;
-    return;
-  }
-  const float enc = static_enc ? *static_enc : __fdiv_rn(kRecipeMax, m);
-  for (int b = lane; b < I / 16; b += 32) {
-    float v[16];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 f = row[4 * b + i];
-      v[4 * i] = f.x;
-      v[4 * i + 1] = f.y;
-      v[4 * i + 2] = f.z;
-      v[4 * i + 3] = f.w;
-    }
-    uint2 q;
-    qsf[sf_offset(p, b, c16)] = (uint8_t)quant_block16(v, enc, q);
-    crow[b] = q;
-  }
-  if (lane == 0) qs[p] = static_enc ? 1.0f : __fmul_rn(m, kRecipeInv);
+  requant_row_warp(act + (size_t)p * I, I, (uint64_t)p, qc, qsf, qs, static_enc, lane);
 }
 
 void launch_requant(int TK, int I, const int32_t* inv, const float* act, uint8_t* qc, uint8_t* qsf,

@@ -82,4 +82,54 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// FC2-input requantization of one activated fp32 row (I values) by one warp:
+// per-row NVFP4 with the recipe constant (Megatron-LM PR #8262, "How to
+// extend": fc2_input_scale = 1/(448*6)), or with a static encode scale (the
+// per-tensor recipe: fc2_input_scale = a2_scale, row scale 1).  Writes the I/2
+// code bytes of permuted row p, its block scales into the 128x4-swizzled plane
+// and its row scale.  The same function serves the stand-alone requant pass
+// and the fused GEMM, so both give the same bits.
+__device__ __forceinline__ void requant_row_warp(const float* __restrict__ row, int I, uint64_t p,
+                                                 uint8_t* __restrict__ qc,
+                                                 uint8_t* __restrict__ qsf,
+                                                 float* __restrict__ qs,
+                                                 const float* __restrict__ static_enc, int lane) {
+  const float4* r4 = reinterpret_cast<const float4*>(row);
+  float m = 1.0f;
+  if (!static_enc) {
+    m = 0.0f;
+    for (int i = lane; i < I / 4; i += 32) {
+      const float4 v = r4[i];
+      m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+    m = warp_max(m);
+  }
+  uint2* crow = reinterpret_cast<uint2*>(qc + p * (uint64_t)(I / 2));
+  const uint32_t c16 = (uint32_t)(I / 16);
+  if (m == 0.0f) {
+    for (int b = lane; b < I / 16; b += 32) {
+      crow[b] = make_uint2(0u, 0u);
+      qsf[sf_offset(p, b, c16)] = 0;
+    }
+    if (lane == 0) qs[p] = 0.0f;
+    return;
+  }
+  const float enc = static_enc ? *static_enc : __fdiv_rn(kRecipeMax, m);
+  for (int b = lane; b < I / 16; b += 32) {
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 f = r4[4 * b + i];
+      v[4 * i] = f.x;
+      v[4 * i + 1] = f.y;
+      v[4 * i + 2] = f.z;
+      v[4 * i + 3] = f.w;
+    }
+    uint2 q;
+    qsf[sf_offset(p, b, c16)] = (uint8_t)quant_block16(v, enc, q);
+    crow[b] = q;
+  }
+  if (lane == 0) qs[p] = static_enc ? 1.0f : __fmul_rn(m, kRecipeInv);
+}
+
 }  // namespace moe

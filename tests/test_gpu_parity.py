@@ -24,6 +24,10 @@ CASES = {
     "relu2_zipf": W.Workload("relu2_T200_H768_I512_E16_K4_zipf", 200, 768, 512, 16, 4, "relu2",
                              x_dist="logspread", routing="zipf", empty_experts=2),
     "swiglu_e64": W.SWIGLU_E64,
+    # few routes per expert: FC1, the FC2-input requant and FC2 run as one launch
+    "swiglu_fused": W.Workload("swiglu_T40_H512_I512_E32_K4", 40, 512, 512, 32, 4, "swiglu"),
+    "relu2_fused": W.Workload("relu2_T24_H768_I512_E64_K6", 24, 768, 512, 64, 6, "relu2",
+                              x_dist="logspread"),
 }
 
 
