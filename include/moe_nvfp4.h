@@ -248,6 +248,34 @@ moe_status moe_nvfp4_forward_per_tensor(const moe_dims* d, const moe_nvfp4_weigh
 moe_status moe_nvfp4_route_topk(int32_t T, int32_t E, int32_t K, const float* logits,
                                 int32_t* topk_ids, float* topk_w, moe_stream_t stream);
 
+/* Options of the *_ex forwards; a zero-initialised struct (or NULL) gives the
+ * behaviour of the plain entry points. */
+typedef struct {
+  /* 1: topk_ids is int64 [T][K], 8-byte aligned ([FI] Tensor and numerical
+   * contract: signed int32/int64 ids); a value outside the int32 range is an
+   * invalid id (ignored and reported like one outside [-1, E)). */
+  int32_t ids_int64;
+  /* > 0 (SwiGLU only): clamped SwiGLU ([FI] Tensor and numerical contract:
+   * "Clamp caps gate above the limit and clips up symmetrically"; the pages'
+   * H200 run uses 10): gate = min(gate, L), up = min(max(up, -L), L), applied to
+   * the scaled FC1 outputs before silu(gate) * up.  0: no clamp. */
+  float swiglu_limit;
+} moe_forward_opts;
+
+/* moe_nvfp4_forward with options (topk_ids as described by opts). */
+moe_status moe_nvfp4_forward_ex(const moe_dims* d, const moe_nvfp4_weights* w, int32_t T,
+                                int32_t K, const uint8_t* codes, const uint8_t* sf,
+                                const float* scale, const void* topk_ids, const float* topk_w,
+                                void* out_bf16, void* ws, size_t ws_bytes,
+                                const moe_forward_opts* opts, moe_stream_t stream);
+
+/* moe_nvfp4_forward_w4a16 with options. */
+moe_status moe_nvfp4_forward_w4a16_ex(const moe_dims* d, const moe_nvfp4_weights* w, int32_t T,
+                                      int32_t K, const void* x_bf16, const void* topk_ids,
+                                      const float* topk_w, void* out_bf16, void* ws,
+                                      size_t ws_bytes, const moe_forward_opts* opts,
+                                      moe_stream_t stream);
+
 /* Device-reported status of the last forward that used `ws`: synchronises
  * `stream`, then returns MOE_ERR_BAD_EXPERT_ID, MOE_ERR_DEVICE_TIMEOUT or
  * MOE_OK.  The flags are rewritten by every forward.  Debug/test

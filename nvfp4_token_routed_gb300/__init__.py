@@ -47,6 +47,10 @@ _LAYOUT_FIELDS = ["total", "rows_cap", "status", "counts", "group_row0", "tiles"
                   "route", "tile_sync"]
 
 
+class moe_forward_opts(C.Structure):
+    _fields_ = [("ids_int64", C.c_int32), ("swiglu_limit", C.c_float)]
+
+
 class moe_ws_layout(C.Structure):
     _fields_ = [(n, C.c_int64 if n == "rows_cap" else C.c_size_t) for n in _LAYOUT_FIELDS]
 
@@ -88,7 +92,13 @@ def lib():
                                                    C.POINTER(moe_nvfp4_weights), i32, i32, vp, vp,
                                                    vp, vp, vp, vp, vp, sz, vp]
         L.moe_nvfp4_route_topk.argtypes = [i32, i32, i32, vp, vp, vp, vp]
-        for f in ["moe_nvfp4_route_topk",
+        L.moe_nvfp4_forward_ex.argtypes = [C.POINTER(moe_dims), C.POINTER(moe_nvfp4_weights), i32,
+                                           i32, vp, vp, vp, vp, vp, vp, vp, sz,
+                                           C.POINTER(moe_forward_opts), vp]
+        L.moe_nvfp4_forward_w4a16_ex.argtypes = [C.POINTER(moe_dims),
+                                                 C.POINTER(moe_nvfp4_weights), i32, i32, vp, vp,
+                                                 vp, vp, vp, sz, C.POINTER(moe_forward_opts), vp]
+        for f in ["moe_nvfp4_route_topk", "moe_nvfp4_forward_ex", "moe_nvfp4_forward_w4a16_ex",
                   "moe_nvfp4_prepare_weights_per_tensor", "moe_nvfp4_quantize_tokens_static",
                   "moe_nvfp4_forward_per_tensor",
                   "moe_nvfp4_weight_sizes", "moe_nvfp4_prepare_weights",
@@ -215,6 +225,25 @@ def moe_nvfp4_forward(d, w, codes, sf, scale, topk_ids, topk_w, out, ws, stream=
                                    _ptr(scale), _ptr(topk_ids), _ptr(topk_w), _ptr(out), _ptr(ws),
                                    ws.numel() * ws.element_size(), _stream(stream)),
            "moe_nvfp4_forward")
+
+
+def moe_nvfp4_forward_ex(d, w, codes, sf, scale, topk_ids, topk_w, out, ws, opts, stream=None):
+    """opts: moe_forward_opts (int64 ids are taken from topk_ids' dtype)."""
+    _need_cuda(codes, sf, scale, topk_ids, topk_w, out, ws)
+    T, K = topk_ids.shape
+    _check(lib().moe_nvfp4_forward_ex(C.byref(d), C.byref(w.c), T, K, _ptr(codes), _ptr(sf),
+                                      _ptr(scale), _ptr(topk_ids), _ptr(topk_w), _ptr(out),
+                                      _ptr(ws), ws.numel() * ws.element_size(), C.byref(opts),
+                                      _stream(stream)), "moe_nvfp4_forward_ex")
+
+
+def moe_nvfp4_forward_w4a16_ex(d, w, x_bf16, topk_ids, topk_w, out, ws, opts, stream=None):
+    _need_cuda(x_bf16, topk_ids, topk_w, out, ws)
+    T, K = topk_ids.shape
+    _check(lib().moe_nvfp4_forward_w4a16_ex(C.byref(d), C.byref(w.c), T, K, _ptr(x_bf16),
+                                            _ptr(topk_ids), _ptr(topk_w), _ptr(out), _ptr(ws),
+                                            ws.numel() * ws.element_size(), C.byref(opts),
+                                            _stream(stream)), "moe_nvfp4_forward_w4a16_ex")
 
 
 def moe_nvfp4_forward_w4a16(d, w, x_bf16, topk_ids, topk_w, out, ws, stream=None):
@@ -352,6 +381,35 @@ def forward(w, codes, sf, scale, topk_ids, topk_w, ws=None, out=None, stream=Non
     if out is None:
         out = torch.empty(T, w.H, dtype=torch.bfloat16, device=codes.device)
     moe_nvfp4_forward(w.dims, w, codes, sf, scale, topk_ids, topk_w, out, ws, stream)
+    return out
+
+
+def forward_opts(topk_ids, swiglu_limit=0.0):
+    """Options for the *_ex calls: int64 ids follow from the tensor's dtype."""
+    return moe_forward_opts(1 if topk_ids.dtype == torch.int64 else 0, float(swiglu_limit))
+
+
+def forward_ex(w, codes, sf, scale, topk_ids, topk_w, swiglu_limit=0.0, ws=None, out=None,
+               stream=None):
+    T, K = topk_ids.shape
+    if ws is None:
+        ws = workspace(w, T, K, device=codes.device)
+    if out is None:
+        out = torch.empty(T, w.H, dtype=torch.bfloat16, device=codes.device)
+    moe_nvfp4_forward_ex(w.dims, w, codes, sf, scale, topk_ids, topk_w, out, ws,
+                         forward_opts(topk_ids, swiglu_limit), stream)
+    return out
+
+
+def forward_w4a16_ex(w, x_bf16, topk_ids, topk_w, swiglu_limit=0.0, ws=None, out=None,
+                     stream=None):
+    T, K = topk_ids.shape
+    if ws is None:
+        ws = workspace(w, T, K, w4a16=True, device=x_bf16.device)
+    if out is None:
+        out = torch.empty(T, w.H, dtype=torch.bfloat16, device=x_bf16.device)
+    moe_nvfp4_forward_w4a16_ex(w.dims, w, x_bf16, topk_ids, topk_w, out, ws,
+                               forward_opts(topk_ids, swiglu_limit), stream)
     return out
 
 

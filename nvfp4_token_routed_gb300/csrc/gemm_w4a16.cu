@@ -421,8 +421,13 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
               const int col = c0 + j;
               if (col >= rows) break;
               const size_t p = (size_t)row0 + col;
-              const float yg = __fmul_rn(v[j], alpha);
-              const float act = __fmul_rn(__fdiv_rn(yg, __fadd_rn(1.0f, expf(-yg))), xrow[j]);
+              float yg = __fmul_rn(v[j], alpha);
+              float yu = xrow[j];
+              if (a.swiglu_limit > 0.0f) {  // clamped SwiGLU: cap the gate, clip the up value
+                yg = fminf(yg, a.swiglu_limit);
+                yu = fmaxf(fminf(yu, a.swiglu_limit), -a.swiglu_limit);
+              }
+              const float act = __fmul_rn(__fdiv_rn(yg, __fadd_rn(1.0f, expf(-yg))), yu);
               a.route_out[p * a.I + f] = __bfloat16_as_ushort(__float2bfloat16_rn(act));
             }
           }

@@ -626,6 +626,13 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
               yg[k] = g[(jb + 2 * k) * 64 + f];
               yu[k] = u[(jb + 2 * k) * 64 + f];
             }
+          if (a.swiglu_limit > 0.0f) {  // clamped SwiGLU: cap the gate, clip the up value
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              yg[k] = fminf(yg[k], a.swiglu_limit);
+              yu[k] = fmaxf(fminf(yu[k], a.swiglu_limit), -a.swiglu_limit);
+            }
+          }
 #pragma unroll
           for (int k = 0; k < 16; ++k)
             if (jb + 2 * k < ncol)

@@ -35,6 +35,7 @@ struct RouteArgs {
   int Hp;  // H rounded up to 256: row length of the permuted token rows
   int w4a16;
   const int32_t* ids;
+  int ids64;  // ids are int64 (read as two int32 words)
   int32_t* status;
   int32_t* chunk_counts;
   int32_t* chunk_prefix;
@@ -77,6 +78,7 @@ struct GemmArgs {
   int I;
   uint16_t* route_out; // FC2: [rows][H] bf16
   int H;
+  float swiglu_limit;  // > 0: clamped SwiGLU (W4A16 FC1)
 };
 
 // Launch with programmatic stream serialization: the kernel may start while the
@@ -145,6 +147,7 @@ struct W4A4Args {
   uint8_t* qsf;             // FC2-input scales, swizzled
   float* qs;                // FC2-input row scales
   const float* a2_static;   // per-tensor recipe: static FC2-input encode scale (else null)
+  float swiglu_limit;       // > 0: clamped SwiGLU (gate <= L, |up| <= L)
 };
 
 // Token-tile tensor maps of one operand: the same [rows][row_bytes] buffer with

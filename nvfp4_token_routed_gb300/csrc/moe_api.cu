@@ -322,33 +322,40 @@ moe_status moe_nvfp4_workspace_layout(const moe_dims* d, int32_t T, int32_t K, i
   return MOE_OK;
 }
 
+static const moe_forward_opts kDefaultOpts = {0, 0.0f};
+
 static moe_status forward_common(const moe_dims* d, const moe_nvfp4_weights* w, int32_t T,
-                                 int32_t K, const int32_t* topk_ids, const float* topk_w,
+                                 int32_t K, const void* topk_ids, const float* topk_w,
                                  void* out_bf16, void* ws, size_t ws_bytes, int w4a16,
-                                 moe_ws_layout* L, int* sms) {
+                                 const moe_forward_opts& o, moe_ws_layout* L, int* sms) {
   moe_status st = check_dims(d);
   if (st != MOE_OK) return st;
   if ((st = check_tk(d, T, K)) != MOE_OK) return st;
   if ((st = check_weights(w)) != MOE_OK) return st;
+  if ((o.ids_int64 != 0 && o.ids_int64 != 1) || !(o.swiglu_limit >= 0.0f) ||
+      (o.swiglu_limit > 0.0f && d->act != MOE_ACT_SWIGLU) || o.swiglu_limit > 3.0e38f)
+    return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!topk_ids || !topk_w || !out_bf16 || !ws) return MOE_ERR_INVALID_ARG;
-  if (!aligned(topk_ids, 4) || !aligned(topk_w, 4) || !aligned(out_bf16, 16) || !aligned(ws, 256))
+  if (!aligned(topk_ids, o.ids_int64 ? 8 : 4) || !aligned(topk_w, 4) || !aligned(out_bf16, 16) ||
+      !aligned(ws, 256))
     return MOE_ERR_MISALIGNED;
   compute_layout(d, T, K, w4a16, L);
   if (ws_bytes < L->total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   return check_device(sms);
 }
 
-static RouteArgs route_args(const moe_dims* d, int32_t T, int32_t K, const int32_t* ids, void* ws,
-                            const moe_ws_layout& L, int w4a16) {
+static RouteArgs route_args(const moe_dims* d, int32_t T, int32_t K, const void* ids, int ids64,
+                            void* ws, const moe_ws_layout& L, int w4a16) {
   RouteArgs r{};
+  r.ids64 = ids64;
   r.TK = T * K;
   r.K = K;
   r.E = d->E;
   r.H = d->H;
   r.Hp = (int)hp_of(d);
   r.w4a16 = w4a16;
-  r.ids = ids;
+  r.ids = static_cast<const int32_t*>(ids);
   r.status = at<int32_t>(ws, L.status);
   r.chunk_counts = at<int32_t>(ws, L.chunk_counts);
   r.chunk_prefix = at<int32_t>(ws, L.chunk_prefix);
@@ -365,8 +372,9 @@ static RouteArgs route_args(const moe_dims* d, int32_t T, int32_t K, const int32
 static moe_status forward_w4a4_impl(const moe_dims* d, const moe_nvfp4_weights* w, int32_t T,
                                     int32_t K, const uint8_t* codes, const uint8_t* sf,
                                     const float* scale, const float* a2_static,
-                                    const int32_t* topk_ids, const float* topk_w, void* out_bf16,
-                                    void* ws, size_t ws_bytes, moe_stream_t stream) {
+                                    const void* topk_ids, const float* topk_w, void* out_bf16,
+                                    void* ws, size_t ws_bytes, const moe_forward_opts& o,
+                                    moe_stream_t stream) {
   moe_ws_layout L;
   int sms = 0;
   if (T > 0 && (!codes || !sf || (!scale && !a2_static))) return MOE_ERR_INVALID_ARG;
@@ -374,7 +382,7 @@ static moe_status forward_w4a4_impl(const moe_dims* d, const moe_nvfp4_weights* 
                 (a2_static && !aligned(a2_static, 4))))
     return MOE_ERR_MISALIGNED;
   moe_status st =
-      forward_common(d, w, T, K, topk_ids, topk_w, out_bf16, ws, ws_bytes, 0, &L, &sms);
+      forward_common(d, w, T, K, topk_ids, topk_w, out_bf16, ws, ws_bytes, 0, o, &L, &sms);
   if (st != MOE_OK || T == 0) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // padded sizes: stored weights, token rows and every workspace row
@@ -401,7 +409,7 @@ static moe_status forward_w4a4_impl(const moe_dims* d, const moe_nvfp4_weights* 
   const bool fused = TK <= kFusedMaxRoutes && TK <= kFusedRoutesPerExpert * d->E;
 
   mark(0, s);
-  RouteArgs r = route_args(d, T, K, topk_ids, ws, L, 0);
+  RouteArgs r = route_args(d, T, K, topk_ids, o.ids_int64, ws, L, 0);
   r.xc = codes;
   r.xsf = sf;
   r.xs = scale;
@@ -432,6 +440,7 @@ static moe_status forward_w4a4_impl(const moe_dims* d, const moe_nvfp4_weights* 
   g.qsf = at<uint8_t>(ws, L.fc2q_sf);
   g.qs = at<float>(ws, L.fc2q_scale);
   g.a2_static = a2_static;
+  g.swiglu_limit = o.swiglu_limit;
   const int act = swiglu ? kFc1Swiglu : kFc1Relu2;
   if (fused) {
     g.run_fc1 = g.run_fc2 = g.fused = 1;
@@ -470,7 +479,17 @@ moe_status moe_nvfp4_forward(const moe_dims* d, const moe_nvfp4_weights* w, int3
                              void* ws, size_t ws_bytes, moe_stream_t stream) {
   if (T > 0 && !scale) return MOE_ERR_INVALID_ARG;
   return forward_w4a4_impl(d, w, T, K, codes, sf, scale, nullptr, topk_ids, topk_w, out_bf16, ws,
-                           ws_bytes, stream);
+                           ws_bytes, kDefaultOpts, stream);
+}
+
+moe_status moe_nvfp4_forward_ex(const moe_dims* d, const moe_nvfp4_weights* w, int32_t T,
+                                int32_t K, const uint8_t* codes, const uint8_t* sf,
+                                const float* scale, const void* topk_ids, const float* topk_w,
+                                void* out_bf16, void* ws, size_t ws_bytes,
+                                const moe_forward_opts* opts, moe_stream_t stream) {
+  if (T > 0 && !scale) return MOE_ERR_INVALID_ARG;
+  return forward_w4a4_impl(d, w, T, K, codes, sf, scale, nullptr, topk_ids, topk_w, out_bf16, ws,
+                           ws_bytes, opts ? *opts : kDefaultOpts, stream);
 }
 
 moe_status moe_nvfp4_forward_per_tensor(const moe_dims* d, const moe_nvfp4_weights* w, int32_t T,
@@ -480,19 +499,20 @@ moe_status moe_nvfp4_forward_per_tensor(const moe_dims* d, const moe_nvfp4_weigh
                                         size_t ws_bytes, moe_stream_t stream) {
   if (T > 0 && !a2_scale) return MOE_ERR_INVALID_ARG;
   return forward_w4a4_impl(d, w, T, K, codes, sf, nullptr, a2_scale, topk_ids, topk_w, out_bf16,
-                           ws, ws_bytes, stream);
+                           ws, ws_bytes, kDefaultOpts, stream);
 }
 
-moe_status moe_nvfp4_forward_w4a16(const moe_dims* d, const moe_nvfp4_weights* w, int32_t T,
-                                   int32_t K, const void* x_bf16, const int32_t* topk_ids,
-                                   const float* topk_w, void* out_bf16, void* ws,
-                                   size_t ws_bytes, moe_stream_t stream) {
+static moe_status forward_w4a16_impl(const moe_dims* d, const moe_nvfp4_weights* w, int32_t T,
+                                     int32_t K, const void* x_bf16, const void* topk_ids,
+                                     const float* topk_w, void* out_bf16, void* ws,
+                                     size_t ws_bytes, const moe_forward_opts& o,
+                                     moe_stream_t stream) {
   moe_ws_layout L;
   int sms = 0;
   if (T > 0 && !x_bf16) return MOE_ERR_INVALID_ARG;
   if (T > 0 && !aligned(x_bf16, 16)) return MOE_ERR_MISALIGNED;
   moe_status st =
-      forward_common(d, w, T, K, topk_ids, topk_w, out_bf16, ws, ws_bytes, 1, &L, &sms);
+      forward_common(d, w, T, K, topk_ids, topk_w, out_bf16, ws, ws_bytes, 1, o, &L, &sms);
   if (st != MOE_OK || T == 0) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // padded sizes: stored weights, token rows and every workspace row
@@ -506,7 +526,7 @@ moe_status moe_nvfp4_forward_w4a16(const moe_dims* d, const moe_nvfp4_weights* w
     return MOE_ERR_CUDA;
 
   mark(0, s);
-  RouteArgs r = route_args(d, T, K, topk_ids, ws, L, 1);
+  RouteArgs r = route_args(d, T, K, topk_ids, o.ids_int64, ws, L, 1);
   r.xb = x_bf16;
   r.pb = at<uint8_t>(ws, L.x_perm);
   launch_route(r, s);
@@ -526,6 +546,7 @@ moe_status moe_nvfp4_forward_w4a16(const moe_dims* d, const moe_nvfp4_weights* w
   g.route_out = at<uint16_t>(ws, L.act_bf16);
   g.I = I;
   g.H = H;
+  g.swiglu_limit = o.swiglu_limit;
   int grid = (int)std::min<int64_t>(sms, tiles_cap * g.m_tiles);
   if (launch_gemm_w4a16(tmA1, tmB1, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
   mark(2, s);
@@ -548,6 +569,23 @@ moe_status moe_nvfp4_forward_w4a16(const moe_dims* d, const moe_nvfp4_weights* w
                   out_bf16, s);
   mark(5, s);
   return cuda_status(cudaGetLastError());
+}
+
+moe_status moe_nvfp4_forward_w4a16(const moe_dims* d, const moe_nvfp4_weights* w, int32_t T,
+                                   int32_t K, const void* x_bf16, const int32_t* topk_ids,
+                                   const float* topk_w, void* out_bf16, void* ws,
+                                   size_t ws_bytes, moe_stream_t stream) {
+  return forward_w4a16_impl(d, w, T, K, x_bf16, topk_ids, topk_w, out_bf16, ws, ws_bytes,
+                            kDefaultOpts, stream);
+}
+
+moe_status moe_nvfp4_forward_w4a16_ex(const moe_dims* d, const moe_nvfp4_weights* w, int32_t T,
+                                      int32_t K, const void* x_bf16, const void* topk_ids,
+                                      const float* topk_w, void* out_bf16, void* ws,
+                                      size_t ws_bytes, const moe_forward_opts* opts,
+                                      moe_stream_t stream) {
+  return forward_w4a16_impl(d, w, T, K, x_bf16, topk_ids, topk_w, out_bf16, ws, ws_bytes,
+                            opts ? *opts : kDefaultOpts, stream);
 }
 
 moe_status moe_nvfp4_route_topk(int32_t T, int32_t E, int32_t K, const float* logits,

@@ -173,8 +173,17 @@ void launch_prepare_fc(int E, int N, int D, int Np, int Dp, int swiglu_I, const 
 // of the token rows into expert-contiguous order.
 constexpr int kChunk = 256;
 
+// Expert id of route idx from int32 ids, or from int64 ids ([FI] Tensor and
+// numerical contract: signed int32/int64 ids) read as two words; an int64 value
+// outside the int32 range is returned as -2, an invalid id.
+__device__ __forceinline__ int load_id(const int32_t* __restrict__ ids, int idx, int ids64) {
+  if (!ids64) return ids[idx];
+  const int2 v = reinterpret_cast<const int2*>(ids)[idx];
+  return v.y == (v.x >> 31) ? v.x : -2;
+}
+
 __global__ void __launch_bounds__(kChunk) route_count_kernel(const int32_t* __restrict__ ids,
-                                                             int TK, int E,
+                                                             int ids64, int TK, int E,
                                                              int32_t* __restrict__ chunk_counts) {
   extern __shared__ int s_cnt[];
   pdl_wait();
@@ -184,7 +193,7 @@ __global__ void __launch_bounds__(kChunk) route_count_kernel(const int32_t* __re
   const int idx = blockIdx.x * kChunk + threadIdx.x;
   int bad = 0;
   if (idx < TK) {
-    const int e = ids[idx];
+    const int e = load_id(ids, idx, ids64);
     if (e >= 0 && e < E)
       atomicAdd(&s_cnt[e], 1);
     else if (e != -1)
@@ -258,7 +267,8 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(
 }
 
 __global__ void __launch_bounds__(kChunk) route_scatter_kernel(
-    const int32_t* __restrict__ ids, int TK, int E, const int32_t* __restrict__ chunk_prefix,
+    const int32_t* __restrict__ ids, int ids64, int TK, int E,
+    const int32_t* __restrict__ chunk_prefix,
     const int32_t* __restrict__ group_row0, int32_t* __restrict__ inv, int32_t* __restrict__ perm) {
   extern __shared__ int s_wcnt[];  // [kChunk/32][E]
   constexpr int kWarps = kChunk / 32;
@@ -268,7 +278,7 @@ __global__ void __launch_bounds__(kChunk) route_scatter_kernel(
   __syncthreads();
   const int idx = blockIdx.x * kChunk + threadIdx.x;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = idx < TK ? ids[idx] : -1;
+  const int e = idx < TK ? load_id(ids, idx, ids64) : -1;
   const bool valid = e >= 0 && e < E;
   // stable rank: earlier lanes of this warp with the same expert, then earlier warps
   const unsigned peers = __match_any_sync(0xFFFFFFFFu, valid ? e : -1);
@@ -321,13 +331,13 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(
 
 void launch_route(const RouteArgs& a, cudaStream_t s) {
   const int nchunks = (a.TK + kChunk - 1) / kChunk;
-  launch_pdl(route_count_kernel, dim3(nchunks), dim3(kChunk), sizeof(int) * a.E, s, a.ids, a.TK,
-             a.E, a.chunk_counts);
+  launch_pdl(route_count_kernel, dim3(nchunks), dim3(kChunk), sizeof(int) * a.E, s, a.ids,
+             a.ids64, a.TK, a.E, a.chunk_counts);
   launch_pdl(route_scan_kernel, dim3(1), dim3(1024), 0, s, nchunks, a.E,
              (const int32_t*)a.chunk_counts, a.chunk_prefix, a.counts, a.group_row0, a.tiles,
              a.status, a.tile_sync, a.tile_sync_words);
   const size_t smem = sizeof(int) * (kChunk / 32) * a.E;
-  launch_pdl(route_scatter_kernel, dim3(nchunks), dim3(kChunk), smem, s, a.ids, a.TK, a.E,
+  launch_pdl(route_scatter_kernel, dim3(nchunks), dim3(kChunk), smem, s, a.ids, a.ids64, a.TK, a.E,
              (const int32_t*)a.chunk_prefix, (const int32_t*)a.group_row0, a.inv, a.perm);
   const int gblocks = (a.TK + 7) / 8;
   if (a.w4a16)

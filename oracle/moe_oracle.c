@@ -36,6 +36,9 @@
  *       the same finalize.
  *   R8  SwiGLU: canonical FC1 rows [0,I) are the gate, [I,2I) the up projection;
  *       a = silu(g)*u with silu(g) = g/(1+exp(-g)); no clamp.
+ *   R15 Clamped SwiGLU (Tensor and numerical contract: the clamp caps the gate
+ *       above the limit and clips up symmetrically): gate = min(gate, L),
+ *       up = min(max(up, -L), L), before silu(gate) * up.
  *   R14 Router: top-K logits per token (ties to the lower expert id, descending),
  *       scores = softmax over the selected K, fp64, rounded to fp32.
  *   R12 Per-tensor recipe (How to extend, "Per-tensor NVFP4 x NVFP4"): the static
@@ -374,21 +377,30 @@ static inline double dq(const uint8_t* codes, const uint8_t* sf, int64_t i) {
 static double silu(double g) { return g / (1.0 + exp(-g)); }
 
 /* Activation of one FC1 output row in fp64 (R8).  y has N1 entries (I for
- * squared-ReLU, 2I for SwiGLU in canonical [gate; up] order); a gets I. */
-static void activation(int act, int64_t I, const double* y, double* a) {
+ * squared-ReLU, 2I for SwiGLU in canonical [gate; up] order); a gets I.  With
+ * limit > 0 the SwiGLU inputs are clamped first (R15: the gate capped at the
+ * limit, the up value clipped to [-limit, limit]). */
+static void activation(int act, double limit, int64_t I, const double* y, double* a) {
     for (int64_t n = 0; n < I; ++n) {
         if (act == 0) {
             double r = y[n] > 0.0 ? y[n] : 0.0;
             a[n] = r * r;
         } else {
-            a[n] = silu(y[n]) * y[I + n];
+            double g = y[n], u = y[I + n];
+            if (limit > 0.0) {
+                if (g > limit) g = limit;
+                if (u > limit) u = limit;
+                if (u < -limit) u = -limit;
+            }
+            a[n] = silu(g) * u;
         }
     }
 }
 
 typedef struct {
     int64_t E, H, I;
-    int32_t act; /* 0 = squared ReLU, 1 = SwiGLU */
+    int32_t act;   /* 0 = squared ReLU, 1 = SwiGLU */
+    double limit;  /* > 0: clamped SwiGLU (R15) */
 } orc_dims;
 
 /* One route of the W4A4 expert (R6), for token row (xc, xsf, xs) and expert e.
@@ -412,7 +424,7 @@ static void expert_w4a4(const orc_dims* d, int64_t e, const uint8_t* w1c, const 
             acc += dq(c1 + n * (H / 2), s1 + n * (H / 16), h) * dq(xc, xsf, h);
         y[n] = acc * (double)a1[e] * (double)xs;
     }
-    activation(d->act, I, y, a);
+    activation(d->act, d->limit, I, y, a);
     for (int64_t n = 0; n < I; ++n) act_out[n] = (float)a[n];
     float s2;
     if (a2_static > 0.0f) { /* per-tensor (R12): static encode scale, no row scale */
@@ -450,7 +462,7 @@ static void expert_w4a16(const orc_dims* d, int64_t e, const uint8_t* w1c, const
             acc += dq(c1 + n * (H / 2), s1 + n * (H / 16), h) * (double)bf16_to_f32(x[h]);
         y[n] = acc * (double)a1[e];
     }
-    activation(d->act, I, y, a);
+    activation(d->act, d->limit, I, y, a);
     for (int64_t n = 0; n < I; ++n) act_out[n] = orc_f64_to_bf16(a[n]);
     const uint8_t* c2 = w2c + e * H * (I / 2);
     const uint8_t* sc2 = w2sf + e * H * (I / 16);

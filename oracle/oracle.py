@@ -16,7 +16,8 @@ _lib = None
 
 
 class Dims(C.Structure):
-    _fields_ = [("E", C.c_int64), ("H", C.c_int64), ("I", C.c_int64), ("act", C.c_int32)]
+    _fields_ = [("E", C.c_int64), ("H", C.c_int64), ("I", C.c_int64), ("act", C.c_int32),
+                ("limit", C.c_double)]
 
 
 def _p(a):
@@ -231,16 +232,16 @@ class Weights:
         self.w2c, self.w2sf, self.a2 = prepare_fc(w2_bf16)
 
 
-def _dims(E, H, I, act):
-    return Dims(E, H, I, 1 if act == "swiglu" else 0)
+def _dims(E, H, I, act, limit=0.0):
+    return Dims(E, H, I, 1 if act == "swiglu" else 0, float(limit))
 
 
-def forward_w4a4(W, xc, xsf, xs, ids, w, E, H, I, act):
+def forward_w4a4(W, xc, xsf, xs, ids, w, E, H, I, act, limit=0.0):
     ids = np.ascontiguousarray(ids, dtype=np.int32)
     w = np.ascontiguousarray(w, dtype=np.float32)
     T, K = ids.shape
     TK = T * K
-    d = _dims(E, H, I, act)
+    d = _dims(E, H, I, act, limit)
     counts = np.empty(E, np.int32)
     perm = np.empty(TK, np.int32)
     inv = np.empty(TK, np.int32)
@@ -298,13 +299,13 @@ class WeightsPerTensor:
         self.a2 = alpha_per_tensor(w2_bf16, a2)
 
 
-def forward_w4a16(W, x_bf16, ids, w, E, H, I, act):
+def forward_w4a16(W, x_bf16, ids, w, E, H, I, act, limit=0.0):
     ids = np.ascontiguousarray(ids, dtype=np.int32)
     w = np.ascontiguousarray(w, dtype=np.float32)
     x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
     T, K = ids.shape
     TK = T * K
-    d = _dims(E, H, I, act)
+    d = _dims(E, H, I, act, limit)
     counts = np.empty(E, np.int32)
     perm = np.empty(TK, np.int32)
     inv = np.empty(TK, np.int32)

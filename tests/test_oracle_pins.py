@@ -417,3 +417,31 @@ def test_router_topk_matches_a_stable_sort_and_the_softmax_closed_form():
     assert np.all(np.diff(w, axis=1) <= 0)
     # top-1 always scores exactly 1
     assert np.all(O.route_topk(lg, 1)[1] == 1.0)
+
+
+# --------------------------------------------------------------------------- clamped SwiGLU
+
+def test_clamped_swiglu_caps_the_gate_and_clips_up():
+    """act = silu(min(g, L)) * clip(u, -L, L) on the FC1 outputs g, u (computed here
+    with numpy from the dequantized operands); a limit above every |g|, |u| is
+    no clamp at all."""
+    wl, x, w1, w2, ids, wts = _tiny("swiglu", I=256)
+    Wt = O.Weights(W.bf16_bits(w1), W.bf16_bits(w2))
+    xc, xsf, xs = O.quantize_tokens(W.bf16_bits(x))
+    plain = O.forward_w4a4(Wt, xc, xsf, xs, ids, wts, wl.E, wl.H, wl.I, "swiglu")
+    huge = O.forward_w4a4(Wt, xc, xsf, xs, ids, wts, wl.E, wl.H, wl.I, "swiglu", limit=1e30)
+    assert np.array_equal(plain["out"], huge["out"]) and np.array_equal(plain["act"], huge["act"])
+    L = 0.05
+    res = O.forward_w4a4(Wt, xc, xsf, xs, ids, wts, wl.E, wl.H, wl.I, "swiglu", limit=L)
+    xq = O.dequant(xc, xsf) * xs[:, None].astype(np.float64)
+    clamped_any = False
+    for q in range(res["R"]):
+        r = int(res["perm"][q]); t, e = r // wl.K, int(ids[r // wl.K, r % wl.K])
+        w1q = O.dequant(Wt.w1c[e], Wt.w1sf[e]) * np.float64(Wt.a1[e])
+        y = w1q @ xq[t]
+        g, u = y[: wl.I], y[wl.I:]
+        clamped_any |= bool((g > L).any() or (np.abs(u) > L).any())
+        gc, uc = np.minimum(g, L), np.clip(u, -L, L)
+        ref = gc / (1 + np.exp(-gc)) * uc
+        assert np.allclose(res["act"][q], ref, rtol=1e-5, atol=1e-7 * L * L)
+    assert clamped_any
