@@ -284,50 +284,55 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
       bool ok = true;
       // Items are claimed two ahead and their table entries loaded one ahead;
       // the raw values are only used an item later, so neither the atomic's nor
-      // the load's latency stalls the copy stream.
+      // the load's latency stalls the copy stream.  The first item's copies go
+      // out before the first claims are used, so the atomics' latency does not
+      // delay the start either.
       int item = blockIdx.x;
       TileInfo cur = item_decode(sp, item, item_raw(a, sp, item));  // rows == 0 past the end
-      int next = (int)gridDim.x + (item < n_items ? atomicAdd(a.item_counter, 1) : n_items);
-      int4 next_raw = item_raw(a, sp, next);
-      int claim = next < n_items ? atomicAdd(a.item_counter, 1) : n_items;  // raw counter value
+      const int claim0 = item < n_items ? atomicAdd(a.item_counter, 1) : n_items;
+      const int claim1 = item < n_items ? atomicAdd(a.item_counter, 1) : n_items;
+      bool primed = false;
+      int next = 0, claim = 0;
+      int4 next_raw = make_int4(0, 0, 1, 0);
       while (ok) {
         if (!queue_push(Q, qp, cur, abort_flag, a.status) || cur.rows == 0) break;
+        const int ph = cur.mt >> 16, mt = cur.mt & 0xFFFF;
+        if (ph != kPhaseRequant) {  // a requant item has no stages: the epilogue warps do it
+          const W4A4Phase& P = a.ph[ph];
+          const int kblocks = P.K / kBK;
+          const int atoms = P.K / 64;                              // scale atoms per 128-row block
+          const size_t plane = (size_t)P.w_rows * (P.K / 16);      // weight scale bytes per expert
+          const int a_row = cur.e * P.w_rows + mt * 128;
+          const uint8_t* sfa0 = P.sfa + (size_t)cur.e * plane + (size_t)mt * atoms * kAtom;
+          const CUtensorMap* tmA = &maps.a[ph];
+          constexpr uint32_t tx = kABytes + kSfaBytes;
+          for (int kb = 0; kb < kblocks; ++kb) {
+            if (!wait_or_abort(R.bar(kBarEmpty + stage), phase ^ 1, abort_flag, a.status)) {
+              ok = false;
+              break;
+            }
+            uint8_t* sb = stages + stage * stage_bytes;
+            const uint32_t full = R.bar(kBarFull + stage);
+            mbar_expect_tx(full, tx);
+            tma_load_2d_hint(smem_u32(sb), tmA, full, kb * kRowBytes, a_row, pol_w);
+            bulk_load(smem_u32(sb + off_sfa), sfa0 + (size_t)(kb * 4) * kAtom, 4 * kAtom, full);
+            last_par[stage] = (int)phase;
+            if (++stage == n_stages) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+        }
+        if (!primed) {  // the first claims, issued before the first item's copies
+          next = (int)gridDim.x + claim0;
+          next_raw = item_raw(a, sp, next);
+          claim = next < n_items ? claim1 : n_items;
+          primed = true;
+        }
         const int next2 = (int)gridDim.x + claim;         // claimed one item ago
         const int4 next2_raw = item_raw(a, sp, next2);
         claim = next2 < n_items ? atomicAdd(a.item_counter, 1) : n_items;
-        const TileInfo nxt = item_decode(sp, next, next_raw);  // loaded one item ago
-        const int ph = cur.mt >> 16, mt = cur.mt & 0xFFFF;
-        if (ph == kPhaseRequant) {  // no stages: the epilogue warps do it alone
-          cur = nxt;
-          next = next2;
-          next_raw = next2_raw;
-          continue;
-        }
-        const W4A4Phase& P = a.ph[ph];
-        const int kblocks = P.K / kBK;
-        const int atoms = P.K / 64;                              // scale atoms per 128-row block
-        const size_t plane = (size_t)P.w_rows * (P.K / 16);      // weight scale bytes per expert
-        const int a_row = cur.e * P.w_rows + mt * 128;
-        const uint8_t* sfa0 = P.sfa + (size_t)cur.e * plane + (size_t)mt * atoms * kAtom;
-        const CUtensorMap* tmA = &maps.a[ph];
-        constexpr uint32_t tx = kABytes + kSfaBytes;
-        for (int kb = 0; kb < kblocks; ++kb) {
-          if (!wait_or_abort(R.bar(kBarEmpty + stage), phase ^ 1, abort_flag, a.status)) {
-            ok = false;
-            break;
-          }
-          uint8_t* sb = stages + stage * stage_bytes;
-          const uint32_t full = R.bar(kBarFull + stage);
-          mbar_expect_tx(full, tx);
-          tma_load_2d_hint(smem_u32(sb), tmA, full, kb * kRowBytes, a_row, pol_w);
-          bulk_load(smem_u32(sb + off_sfa), sfa0 + (size_t)(kb * 4) * kAtom, 4 * kAtom, full);
-          last_par[stage] = (int)phase;
-          if (++stage == n_stages) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
-        cur = nxt;
+        cur = item_decode(sp, next, next_raw);            // loaded one item ago
         next = next2;
         next_raw = next2_raw;
       }

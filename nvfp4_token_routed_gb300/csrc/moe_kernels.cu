@@ -214,14 +214,47 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(
   pdl_trigger();
   // per-token-tile counters of the fused FC1 -> FC2 GEMM start at zero
   for (int i = threadIdx.x; i < tile_sync_words; i += blockDim.x) tile_sync[i] = 0;
-  const int e = threadIdx.x;
-  int total = 0;
-  if (e < E) {
-    for (int c = 0; c < nchunks; ++c) {
-      chunk_prefix[(size_t)c * E + e] = total;
-      total += chunk_counts[(size_t)c * (E + 1) + e];
+  // (1) per-expert exclusive prefix over the chunks: P threads per expert (the
+  // largest power of two with E * P <= 1024, P <= 32, adjacent lanes), each
+  // summing a contiguous range of chunks, then a scan across the P partial sums
+  __shared__ int s_total[1024];
+  {
+    int P = 1;
+    while (P < 32 && E * P * 2 <= (int)blockDim.x) P *= 2;
+    const int t = threadIdx.x, ea = t / P, part = t % P;
+    const int cs = (nchunks + P - 1) / P;
+    const int c0 = min(part * cs, nchunks), c1 = min(c0 + cs, nchunks);
+    int local = 0;
+    if (ea < E)
+      for (int c = c0; c < c1; ++c) local += chunk_counts[(size_t)c * (E + 1) + ea];
+    int incl = local;  // inclusive scan across the P parts of this expert
+    for (int o = 1; o < P; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o, P);
+      if (part >= o) incl += y;
+    }
+    if (ea < E) {
+      int run = incl - local;
+      int c = c0;
+      for (; c + 4 <= c1; c += 4) {  // four loads in flight ahead of their stores
+        int v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = chunk_counts[(size_t)(c + u) * (E + 1) + ea];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          chunk_prefix[(size_t)(c + u) * E + ea] = run;
+          run += v[u];
+        }
+      }
+      for (; c < c1; ++c) {
+        chunk_prefix[(size_t)c * E + ea] = run;
+        run += chunk_counts[(size_t)c * (E + 1) + ea];
+      }
+      if (part == P - 1) s_total[ea] = incl;
     }
   }
+  __syncthreads();
+  const int e = threadIdx.x;
+  const int total = e < E ? s_total[e] : 0;
   int bad = 0;
   for (int c = e; c < nchunks; c += blockDim.x) bad |= chunk_counts[(size_t)c * (E + 1) + E];
   bad = __syncthreads_or(bad);

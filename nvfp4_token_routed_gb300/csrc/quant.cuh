@@ -87,47 +87,80 @@ __device__ __forceinline__ float warp_max(float v) {
 // extend": fc2_input_scale = 1/(448*6)), or with a static encode scale (the
 // per-tensor recipe: fc2_input_scale = a2_scale, row scale 1).  Writes the I/2
 // code bytes of permuted row p, its block scales into the 128x4-swizzled plane
-// and its row scale.  The same function serves the stand-alone requant pass
-// and the fused GEMM, so both give the same bits.
+// and its row scale.  Lane l owns blocks l, l+32, ... (16 consecutive values
+// each, 64 contiguous bytes); a row of up to 2048 values is loaded once into
+// registers (one round trip), longer rows in groups of 128 blocks read twice.
+// The fused GEMM's requant uses the same quant_block16 and amax, so both give
+// the same bits.
+__device__ __forceinline__ void requant_group_load(const float4* __restrict__ r4, int b0, int nb,
+                                                   int lane, float (&v)[4][16]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int b = b0 + lane + 32 * k;
+    if (b < nb) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 f = r4[4 * b + i];
+        v[k][4 * i] = f.x;
+        v[k][4 * i + 1] = f.y;
+        v[k][4 * i + 2] = f.z;
+        v[k][4 * i + 3] = f.w;
+      }
+    }
+  }
+}
 __device__ __forceinline__ void requant_row_warp(const float* __restrict__ row, int I, uint64_t p,
                                                  uint8_t* __restrict__ qc,
                                                  uint8_t* __restrict__ qsf,
                                                  float* __restrict__ qs,
                                                  const float* __restrict__ static_enc, int lane) {
   const float4* r4 = reinterpret_cast<const float4*>(row);
+  const int nb = I / 16;  // a multiple of 16: lanes come in groups of four in range
+  const uint32_t c16 = (uint32_t)nb;
+  float v[4][16];
   float m = 1.0f;
   if (!static_enc) {
     m = 0.0f;
-    for (int i = lane; i < I / 4; i += 32) {
-      const float4 v = r4[i];
-      m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    for (int b0 = 0; b0 < nb; b0 += 128) {
+      requant_group_load(r4, b0, nb, lane, v);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (b0 + lane + 32 * k < nb) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[k][i]));
+        }
     }
     m = warp_max(m);
   }
   uint2* crow = reinterpret_cast<uint2*>(qc + p * (uint64_t)(I / 2));
-  const uint32_t c16 = (uint32_t)(I / 16);
   if (m == 0.0f) {
-    for (int b = lane; b < I / 16; b += 32) {
+    for (int b = lane; b < nb; b += 32) {
       crow[b] = make_uint2(0u, 0u);
-      qsf[sf_offset(p, b, c16)] = 0;
+      if ((b & 3) == 0) *reinterpret_cast<uint32_t*>(qsf + sf_offset(p, b, c16)) = 0u;
     }
     if (lane == 0) qs[p] = 0.0f;
     return;
   }
   const float enc = static_enc ? *static_enc : __fdiv_rn(kRecipeMax, m);
-  for (int b = lane; b < I / 16; b += 32) {
-    float v[16];
+  for (int b0 = 0; b0 < nb; b0 += 128) {
+    // rows of up to 2048 values (and the static-scale path) are still in registers
+    if (nb > 128 || static_enc) requant_group_load(r4, b0, nb, lane, v);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 f = r4[4 * b + i];
-      v[4 * i] = f.x;
-      v[4 * i + 1] = f.y;
-      v[4 * i + 2] = f.z;
-      v[4 * i + 3] = f.w;
+    for (int k = 0; k < 4; ++k) {
+      const int b = b0 + lane + 32 * k;
+      uint32_t sfb = 0;
+      if (b < nb) {
+        uint2 q;
+        sfb = quant_block16(v[k], enc, q);
+        crow[b] = q;
+      }
+      // a group of four lanes holds four consecutive blocks: one 4-byte store of
+      // their scale bytes (consecutive in the swizzled plane)
+      const uint32_t w = sfb | (__shfl_down_sync(0xFFFFFFFFu, sfb, 1) << 8) |
+                         (__shfl_down_sync(0xFFFFFFFFu, sfb, 2) << 16) |
+                         (__shfl_down_sync(0xFFFFFFFFu, sfb, 3) << 24);
+      if ((lane & 3) == 0 && b < nb) *reinterpret_cast<uint32_t*>(qsf + sf_offset(p, b, c16)) = w;
     }
-    uint2 q;
-    qsf[sf_offset(p, b, c16)] = (uint8_t)quant_block16(v, enc, q);
-    crow[b] = q;
   }
   if (lane == 0) qs[p] = static_enc ? 1.0f : __fmul_rn(m, kRecipeInv);
 }
