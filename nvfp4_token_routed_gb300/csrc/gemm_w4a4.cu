@@ -282,20 +282,16 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
       uint32_t phase = 0;
       QueuePos qp;
       bool ok = true;
-      // Items are claimed two ahead and their table entries loaded one ahead;
-      // the raw values are only used an item later, so neither the atomic's nor
-      // the load's latency stalls the copy stream.  The first item's copies go
-      // out before the first claims are used, so the atomics' latency does not
-      // delay the start either.
+      // The next item is claimed when the current one starts (its copies hide
+      // the atomic's latency) and its table entry is read when the current one's
+      // copies are out; the ring is about one item deep, so that read does not
+      // starve the MMAs.  Claiming only one item ahead keeps the CTAs' finish
+      // times within about one item of each other.
       int item = blockIdx.x;
       TileInfo cur = item_decode(sp, item, item_raw(a, sp, item));  // rows == 0 past the end
-      const int claim0 = item < n_items ? atomicAdd(a.item_counter, 1) : n_items;
-      const int claim1 = item < n_items ? atomicAdd(a.item_counter, 1) : n_items;
-      bool primed = false;
-      int next = 0, claim = 0;
-      int4 next_raw = make_int4(0, 0, 1, 0);
       while (ok) {
         if (!queue_push(Q, qp, cur, abort_flag, a.status) || cur.rows == 0) break;
+        const int claim = atomicAdd(a.item_counter, 1);  // the next item: gridDim.x + claim
         const int ph = cur.mt >> 16, mt = cur.mt & 0xFFFF;
         if (ph != kPhaseRequant) {  // a requant item has no stages: the epilogue warps do it
           const W4A4Phase& P = a.ph[ph];
@@ -323,18 +319,8 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
             }
           }
         }
-        if (!primed) {  // the first claims, issued before the first item's copies
-          next = (int)gridDim.x + claim0;
-          next_raw = item_raw(a, sp, next);
-          claim = next < n_items ? claim1 : n_items;
-          primed = true;
-        }
-        const int next2 = (int)gridDim.x + claim;         // claimed one item ago
-        const int4 next2_raw = item_raw(a, sp, next2);
-        claim = next2 < n_items ? atomicAdd(a.item_counter, 1) : n_items;
-        cur = item_decode(sp, next, next_raw);            // loaded one item ago
-        next = next2;
-        next_raw = next2_raw;
+        item = (int)gridDim.x + claim;
+        cur = item_decode(sp, item, item_raw(a, sp, item));
       }
       if (!ok || *abort_flag) drain_stages(R, kBarFull, last_par, kMaxStages);
     }
