@@ -264,6 +264,24 @@ def run_reference(args, rank, world):
 
 # ----------------------------------------------------------------------------- GPU arm
 
+def max_over_ranks(value, world, device=None):
+    """The largest `value` over all ranks (the slowest replica sets the time);
+    the identity on one rank.  The tensor lives where the backend reduces it."""
+    if world <= 1:
+        return float(value)
+    on_gpu = torch.distributed.get_backend() == "nccl"
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if on_gpu else "cpu")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world, tokens_per_step, steps, max_total_ms):
+    """Whole-job tokens/s of `world` independent replicas: every rank processes
+    tokens_per_step per step; the job takes the slowest rank's time."""
+    return world * tokens_per_step * steps / (max_total_ms / 1e3)
+
+
 def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -375,13 +393,9 @@ def run_ours(args, rank, world, local_rank):
     M.moe_nvfp4_profile_events([])
 
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     ms_per_step = total_ms / args.steps
-    value = world * T * args.steps / (total_ms / 1e3)
+    value = replica_throughput(world, T, args.steps, total_ms)
 
     # ---- end to end through the public API with host buffers
     x_h = x.cpu().pin_memory()
@@ -426,11 +440,8 @@ def run_ours(args, rank, world, local_rank):
             e_e.record(stream)
             e_e.synchronize()
             e2e_ms += e_s.elapsed_time(e_e)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e_value = world * T * e2e_steps / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    e2e_value = replica_throughput(world, T, e2e_steps, e2e_ms)
     h2d = x_h.numel() * 2 + (logits_h.numel() * 4 if logits_h is not None
                              else ids_h.numel() * 4 + wts_h.numel() * 4)
     d2h = out_h.numel() * 2
