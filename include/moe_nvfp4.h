@@ -276,6 +276,15 @@ moe_status moe_nvfp4_forward_w4a16_ex(const moe_dims* d, const moe_nvfp4_weights
                                       size_t ws_bytes, const moe_forward_opts* opts,
                                       moe_stream_t stream);
 
+/* Test hook of the in-kernel failure detection: launches one thread that waits
+ * on an mbarrier nothing arrives on and then on a flag nothing sets, with the
+ * bounded waits of the GEMM kernels (2 s limit each, so the call's work takes
+ * about 4 s).  Both waits give up and record a timeout, the kernel returns
+ * normally and the context stays usable: moe_nvfp4_read_status(ws) then gives
+ * MOE_ERR_DEVICE_TIMEOUT.  Uses (and zeroes) the first 68 bytes of ws; nothing
+ * traps or faults. */
+moe_status moe_nvfp4_selftest_wait_timeout(void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* Device-reported status of the last forward that used `ws`: synchronises
  * `stream`, then returns MOE_ERR_BAD_EXPERT_ID, MOE_ERR_DEVICE_TIMEOUT or
  * MOE_OK.  The flags are rewritten by every forward.  Debug/test

@@ -92,13 +92,15 @@ def lib():
                                                    C.POINTER(moe_nvfp4_weights), i32, i32, vp, vp,
                                                    vp, vp, vp, vp, vp, sz, vp]
         L.moe_nvfp4_route_topk.argtypes = [i32, i32, i32, vp, vp, vp, vp]
+        L.moe_nvfp4_selftest_wait_timeout.argtypes = [vp, sz, vp]
         L.moe_nvfp4_forward_ex.argtypes = [C.POINTER(moe_dims), C.POINTER(moe_nvfp4_weights), i32,
                                            i32, vp, vp, vp, vp, vp, vp, vp, sz,
                                            C.POINTER(moe_forward_opts), vp]
         L.moe_nvfp4_forward_w4a16_ex.argtypes = [C.POINTER(moe_dims),
                                                  C.POINTER(moe_nvfp4_weights), i32, i32, vp, vp,
                                                  vp, vp, vp, sz, C.POINTER(moe_forward_opts), vp]
-        for f in ["moe_nvfp4_route_topk", "moe_nvfp4_forward_ex", "moe_nvfp4_forward_w4a16_ex",
+        for f in ["moe_nvfp4_selftest_wait_timeout",
+                  "moe_nvfp4_route_topk", "moe_nvfp4_forward_ex", "moe_nvfp4_forward_w4a16_ex",
                   "moe_nvfp4_prepare_weights_per_tensor", "moe_nvfp4_quantize_tokens_static",
                   "moe_nvfp4_forward_per_tensor",
                   "moe_nvfp4_weight_sizes", "moe_nvfp4_prepare_weights",
@@ -197,6 +199,13 @@ def moe_nvfp4_forward_per_tensor(d, w, codes, sf, a2_scale, topk_ids, topk_w, ou
                                               _ptr(topk_w), _ptr(out), _ptr(ws),
                                               ws.numel() * ws.element_size(), _stream(stream)),
            "moe_nvfp4_forward_per_tensor")
+
+
+def moe_nvfp4_selftest_wait_timeout(ws, stream=None):
+    _need_cuda(ws)
+    _check(lib().moe_nvfp4_selftest_wait_timeout(_ptr(ws), ws.numel() * ws.element_size(),
+                                                 _stream(stream)),
+           "moe_nvfp4_selftest_wait_timeout")
 
 
 def moe_nvfp4_route_topk(logits, topk_ids, topk_w, stream=None):

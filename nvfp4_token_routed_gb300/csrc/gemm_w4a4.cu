@@ -694,6 +694,30 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
   }
 }
 
+// Self-test of the bounded waits: one thread waits on an mbarrier that nothing
+// arrives on, then on a flag that nothing sets, with the same helpers the GEMM
+// roles use.  Each wait gives up after its time limit and records
+// kFlagWaitTimeout in status[]; the kernel then returns normally.
+__global__ void selftest_wait_kernel(const int32_t* never_set, int32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  fence_barrier_init();
+  abort_flag = 0;
+  volatile int* ab = &abort_flag;
+  const bool mbar_ok = wait_or_abort(b, 0, ab, status);  // no arrival: times out
+  *ab = 0;
+  const bool flag_ok = wait_flag_geq(never_set, 1, ab, status);  // never set: times out
+  if (mbar_ok || flag_ok) status[kStatusFlags] = 0;  // a wait that "succeeded" fails the test
+}
+
+cudaError_t launch_selftest_wait(const int32_t* never_set, int32_t* status, cudaStream_t s) {
+  selftest_wait_kernel<<<1, 32, 0, s>>>(never_set, status);
+  return cudaGetLastError();
+}
+
 template <int ACT>
 static cudaError_t launch_act(const W4A4Maps& maps, const W4A4Args& a, int grid, cudaStream_t s) {
   static bool configured = false;  // the attribute is per function

@@ -167,6 +167,8 @@ struct W4A4Maps {
 // act: kFc1Relu2 or kFc1Swiglu (the FC1 epilogue; FC2 items need no choice).
 cudaError_t launch_gemm_w4a4(const W4A4Maps& maps, const W4A4Args& a, int act, int grid,
                              cudaStream_t s);
+// Test hook of the bounded in-kernel waits (moe_nvfp4_selftest_wait_timeout).
+cudaError_t launch_selftest_wait(const int32_t* never_set, int32_t* status, cudaStream_t s);
 // W4A16: tmA over packed weights (128-byte boxes, 128-byte swizzle), tmB over bf16
 // token rows (128-byte boxes, 128-byte swizzle); route_out receives the bf16
 // activated rows (FC1, row stride I) or the bf16 route rows (FC2, stride H).

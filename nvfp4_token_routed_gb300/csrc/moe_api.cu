@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cstdint>
 #include <cstring>
@@ -189,7 +190,15 @@ constexpr int kMaxProfileEvents = 8;
 cudaEvent_t g_prof[kMaxProfileEvents];
 int g_nprof = 0;
 
+// Stage boundaries of a forward: 0 before routing, 1 before FC1, 2 before the
+// requant, 3 before FC2, 4 before the finalize, 5 at the end.  Each stage is an
+// NVTX range (host-side enqueue; a no-op unless a profiler is attached), and the
+// events registered with moe_nvfp4_profile_events are recorded at the boundaries.
 void mark(int i, cudaStream_t s) {
+  static const char* const kStage[5] = {"moe.route", "moe.fc1", "moe.requant", "moe.fc2",
+                                        "moe.finalize"};
+  if (i > 0) nvtxRangePop();
+  if (i < 5) nvtxRangePushA(kStage[i]);
   if (i >= g_nprof || !g_prof[i]) return;
   // inside stream capture the record must become an event-record node of the graph
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
@@ -609,6 +618,19 @@ moe_status moe_nvfp4_profile_events(void* const* events, int32_t n) {
     g_prof[i] = i < n ? static_cast<cudaEvent_t>(events[i]) : nullptr;
   g_nprof = n;
   return MOE_OK;
+}
+
+moe_status moe_nvfp4_selftest_wait_timeout(void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned(ws, 256)) return MOE_ERR_MISALIGNED;
+  const size_t need = sizeof(int32_t) * (kStatusWords + 1);
+  if (ws_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  moe_status st = check_device(nullptr);
+  if (st != MOE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t* status = static_cast<int32_t*>(ws);
+  if (cudaMemsetAsync(ws, 0, need, s) != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(launch_selftest_wait(status + kStatusWords, status, s));
 }
 
 moe_status moe_nvfp4_read_status(const void* ws, moe_stream_t stream) {
