@@ -13,15 +13,20 @@
 //     elements, 128-byte swizzle, so each row is read in 128-byte runs) with
 //     their E4M3 scale atoms (bulk copy), and bf16 token stages (two 64-element
 //     K chunks, 128-byte swizzle, 16-row boxes) -- two token stages per slot
-//   * warps 6-13: decode -- two warps per TMEM lane quadrant; thread r of
-//     quadrant q owns weight row 32q+r: for each 128-K half of a packed slot it
-//     reads 32 packed bytes and their scales from shared memory, forms 64 exact
-//     bf16 values (E2M1 -> f16x2, times the f16 scale, widened to bf16) and
-//     writes them into a TMEM A slot (lane = row, 2 K elements per column); the
-//     packed slot is released as soon as both halves are decoded
-//   * warp 1: TMEM allocator and single-thread MMA issuer:
-//     tcgen05.mma.kind::f16 with A from TMEM and B from shared memory, K = 16
-//     per instruction, N = the tile's token count rounded up to 16
+//   * warps 6..5+kDecodeWarps: decode -- kDecodeWarps/4 warps per TMEM lane
+//     quadrant; thread r of quadrant q owns weight row 32q+r: for each 128-K
+//     half of a packed slot its warps read the packed bytes and their scales
+//     from shared memory, form exact bf16 values of code x scale x 2^-8 with
+//     integer and bf16x2 instructions only (decode8_bf16; the epilogue's alpha
+//     carries the 2^8) and write them into a TMEM A slot (lane = row, 2 K
+//     elements per column); the packed slot is released once both halves are
+//     decoded
+//   * warp 1 (also the TMEM allocator) and the last warp: MMA issuers, one
+//     thread each -- tcgen05.mma.kind::f16 with A from TMEM and B from shared
+//     memory, K = 16 per instruction, N = the tile's token count rounded up to
+//     16; the first issues the even K steps into one partial sum, the second
+//     the odd ones into another (a thread issues one MMA about every 60 ns
+//     whatever its shape, so small token tiles are bound by issue, not math)
 //   * warps 2-5: epilogue (alpha, activation, bf16 rounding), one TMEM lane per
 //     thread; SwiGLU pairs gate and up rows through shared memory as in W4A4
 //   * three rings: packed-weight slots (4-6), token stages (up to 12) and TMEM
@@ -45,12 +50,13 @@ constexpr int kRawBytes = 128 * kRawK / 2;  // 16 KB: 128 rows x 128 B (128-byte
 constexpr int kAtom = 512;
 constexpr int kSfaBytes = 4 * kAtom;        // 4 K-atoms (4 scale columns each)
 constexpr int kRawSlotBytes = kRawBytes + kSfaBytes;
-constexpr int kBK = 128;                    // K elements per token stage / decoded TMEM slot
+constexpr int kBK = kRawK;                  // K elements per token stage / decoded TMEM slot
+constexpr int kChunks = kBK / 64;           // 64-element (128-byte) K chunks per token stage
 constexpr int kChunkRowBytes = 128;         // 64 bf16 per row per K chunk
 constexpr int kACols = kBK / 2;             // TMEM columns of one decoded A slot
 constexpr int kMaxRaw = 6;                  // packed-weight slots (released after decode)
 constexpr int kMaxStages = 12;              // token stages (released by the MMAs)
-constexpr int kMaxASlots = 6;               // TMEM slots of decoded weights
+constexpr int kMaxASlots = 3;               // TMEM slots of decoded weights
 constexpr int kMaxAcc = 2;
 constexpr int kTmemCols = 512;
 constexpr int kXchgFloats = 2 * 64 * 33;
@@ -58,8 +64,14 @@ constexpr int kXchgBytes = (kXchgFloats * 4 + 1023) / 1024 * 1024;
 constexpr int kBarBytes = 2048;
 constexpr int kSmemBytes = 227 * 1024;
 constexpr int kRingBudget = kSmemBytes - 1024 - kBarBytes - kXchgBytes;
-constexpr int kThreads = 448;               // 14 warps
-constexpr int kDecodeWarps = 8;             // warps 6-13, two per TMEM lane quadrant
+constexpr int kDecodeWarps = 8;             // warps 6.., kDecodeWarps / 4 per TMEM lane quadrant
+constexpr int kDecodePerQuad = kDecodeWarps / 4;
+constexpr int kChunksPerWarp = 4 / kDecodePerQuad;  // 16-byte chunks of a 128-K half per warp
+constexpr int kIssuers = 2;                 // MMA issuers: even and odd K steps
+constexpr int kIssuerWarp1 = 6 + kDecodeWarps;      // warp of the second issuer
+constexpr int kTokenWarp = 7 + kDecodeWarps;        // token-stage producer
+constexpr int kThreads = (8 + kDecodeWarps) * 32;
+static_assert(kDecodePerQuad * 4 == kDecodeWarps && kChunksPerWarp * kDecodePerQuad == 4, "decode");
 constexpr int kBarRawFull = 0;
 constexpr int kBarRawEmpty = kBarRawFull + kMaxRaw;
 constexpr int kBarFull = kBarRawEmpty + kMaxRaw;          // token stages
@@ -71,15 +83,20 @@ constexpr int kBarAccEmpty = kBarAccFull + kMaxAcc;
 constexpr int kBarItemFull = kBarAccEmpty + kMaxAcc;
 constexpr int kBarItemEmpty = kBarItemFull + kItemSlots;
 constexpr int kBarDrain = kBarItemEmpty + kItemSlots;
-constexpr int kNumBars = kBarDrain + 1;
+constexpr int kNumBars = kBarDrain + kIssuers;
 constexpr int kFlagsOff = 8 * kNumBars;
 constexpr int kRingOff = 768;
 static_assert(kFlagsOff + 16 <= kRingOff && kRingOff + 16 * kItemSlots <= 1024, "flag area");
+// Token boxes are 16 << box_log(n16) rows: the smallest of 16/32/64/128 >= n16.
+__device__ __forceinline__ int box_log(int n16) {
+  return n16 <= 16 ? 0 : n16 <= 32 ? 1 : n16 <= 64 ? 2 : 3;
+}
+__device__ __forceinline__ int box_rows(int n16) { return 16 << box_log(n16); }
 }  // namespace w4a16
 
 template <int MODE>
 __global__ void __launch_bounds__(w4a16::kThreads, 1)
-    gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+    gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ TokenMaps tmB,
                       const GemmArgs a) {
   using namespace w4a16;
   extern __shared__ uint8_t smem_raw[];
@@ -102,26 +119,26 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
     }
     for (int s = 0; s < kMaxStages; ++s) {
       mbar_init(R.bar(kBarFull + s), 1);
-      mbar_init(R.bar(kBarEmpty + s), 1);
+      mbar_init(R.bar(kBarEmpty + s), kIssuers);
     }
     for (int j = 0; j < kMaxASlots; ++j) {
       mbar_init(R.bar(kBarAReady + j), kDecodeWarps);
-      mbar_init(R.bar(kBarAFree + j), 1);
+      mbar_init(R.bar(kBarAFree + j), kIssuers);
     }
     for (int b = 0; b < kMaxAcc; ++b) {
-      mbar_init(R.bar(kBarAccFull + b), 1);
+      mbar_init(R.bar(kBarAccFull + b), kIssuers);
       mbar_init(R.bar(kBarAccEmpty + b), 128);
     }
     for (int s = 0; s < kItemSlots; ++s) {
       mbar_init(R.bar(kBarItemFull + s), 1);
-      mbar_init(R.bar(kBarItemEmpty + s), 1 + kDecodeWarps + 4);
+      mbar_init(R.bar(kBarItemEmpty + s), kIssuers + kDecodeWarps + 4 + 1);
     }
-    mbar_init(R.bar(kBarDrain), 1);
+    for (int i = 0; i < kIssuers; ++i) mbar_init(R.bar(kBarDrain + i), 1);
     *abort_flag = 0;
     *epi_stop = 0;
     fence_barrier_init();
     prefetch_tmap(&tmA);
-    prefetch_tmap(&tmB);
+    for (int i = 0; i < 4; ++i) prefetch_tmap(&tmB.box[i]);
   }
   __syncwarp();  // thread 0's set-up branch rejoins its warp before the barrier
   if (warp == 1) {
@@ -137,14 +154,15 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
 
   const int n_items = a.status[kStatusTiles] * a.m_tiles;
   const int max_n16 = (a.status[kStatusMaxRows] + 15) & ~15;
-  const int chunk_bytes = max_n16 * kChunkRowBytes;        // one K chunk of the token tile
-  const int stage_bytes = 2 * chunk_bytes;                 // token stage: 128 K, multiple of 1024
+  // A token stage is one 3-D box: kChunks 64-K chunks of box_rows(n16) rows
+  // each, chunk-major, so chunk c of a tile starts c x box_rows x 128 bytes in.
+  const int stage_bytes = kChunks * box_rows(max_n16) * kChunkRowBytes;  // multiple of 1024
   // Each item accumulates into two partial sums (even and odd K steps, so
   // consecutive MMAs do not wait on one another), added in a fixed order in the
   // epilogue.  The split never depends on the batch, so results stay bitwise
   // batch invariant.  nbuf items are in flight (one when tiles exceed 64 tokens).
   const int acc_cols = (max_n16 + 31) & ~31;
-  const int nacc = 2;
+  const int nacc = kIssuers;
   const int acc_stride = nacc * acc_cols;                  // TMEM columns per item
   const int nbuf = max_n16 <= 64 ? 2 : 1;                  // accumulator buffers
   const int a_base = nbuf * acc_stride;                    // decoded A slots follow the accumulators
@@ -161,17 +179,17 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
   const size_t plane = (size_t)a.w_rows * (a.K / 16);
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ weight producer
+    // Claims items, publishes them to the other roles and streams the packed
+    // weight slots (one tiled copy of 128 rows x 256 K and one bulk copy of
+    // their scale atoms per slot).
     if (lane == 0) {
-      int last_raw[kMaxRaw], last_stg[kMaxStages];
+      int last_raw[kMaxRaw];
 #pragma unroll
       for (int s = 0; s < kMaxRaw; ++s) last_raw[s] = -1;
-#pragma unroll
-      for (int s = 0; s < kMaxStages; ++s) last_stg[s] = -1;
       const uint64_t pol_w = policy_evict_first();
-      const uint64_t pol_x = policy_evict_last();
-      int rs = 0, stage = 0;
-      uint32_t rphase = 0, phase = 0;
+      int rs = 0;
+      uint32_t rphase = 0;
       QueuePos qp;
       bool ok = true;
       // Items are claimed two ahead and their table entries loaded one ahead;
@@ -188,12 +206,9 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
         const int4 next2_raw = tile_raw(a, next2, n_items);
         claim = next2 < n_items ? atomicAdd(a.item_counter, 1) : n_items;
         const TileInfo nxt = tile_decode(a, next, n_items, next_raw);  // loaded one item ago
-        const int n16 = (cur.rows + 15) & ~15;
         const int a_row = cur.e * a.w_rows + cur.mt * 128;
-        const int b_row = cur.tt * kTileRows;
         const uint8_t* sfa0 = a.sfa + (size_t)cur.e * plane + (size_t)cur.mt * atoms * kAtom;
-        for (int kr = 0; kr < kraw && ok; ++kr) {
-          // one packed-weight slot (256 K) ...
+        for (int kr = 0; kr < kraw; ++kr) {
           if (!wait_or_abort(R.bar(kBarRawEmpty + rs), rphase ^ 1, abort_flag, a.status)) {
             ok = false;
             break;
@@ -208,26 +223,6 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
             rs = 0;
             rphase ^= 1;
           }
-          // ... and the two token stages (128 K each) that go with it
-          for (int h = 0; h < 2; ++h) {
-            if (!wait_or_abort(R.bar(kBarEmpty + stage), phase ^ 1, abort_flag, a.status)) {
-              ok = false;
-              break;
-            }
-            uint8_t* sb = stage_ring + stage * stage_bytes;
-            const uint32_t full = R.bar(kBarFull + stage);
-            mbar_expect_tx(full, 2 * n16 * kChunkRowBytes);
-            for (int kc = 0; kc < 2; ++kc)
-              for (int c = 0; c < n16 / 16; ++c)
-                tma_load_2d_hint(smem_u32(sb + kc * chunk_bytes + c * 16 * kChunkRowBytes), &tmB,
-                                 full, (kr * 4 + h * 2 + kc) * kChunkRowBytes, b_row + 16 * c,
-                                 pol_x);
-            last_stg[stage] = (int)phase;
-            if (++stage == n_stages) {
-              stage = 0;
-              phase ^= 1;
-            }
-          }
         }
         cur = nxt;
         next = next2;
@@ -236,18 +231,56 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
       if (!ok || *abort_flag) {
         for (int s = 0; s < kMaxRaw; ++s)
           if (last_raw[s] >= 0) mbar_wait(R.bar(kBarRawFull + s), (uint32_t)last_raw[s]);
+      }
+    }
+  } else if (warp == kTokenWarp) {
+    // ------------------------------------------------------------ token producer
+    // One 3-D tiled copy per token stage: the kChunks 64-K chunks of the tile's
+    // rows, in the smallest of the 16/32/64/128-row boxes that covers them.
+    if (lane == 0) {
+      int last_stg[kMaxStages];
+#pragma unroll
+      for (int s = 0; s < kMaxStages; ++s) last_stg[s] = -1;
+      const uint64_t pol_x = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      QueuePos qp;
+      bool ok = true;
+      while (ok) {
+        const TileInfo cur = queue_pop_thread(Q, qp, abort_flag, a.status);
+        if (cur.rows == 0) break;
+        const int bl = box_log((cur.rows + 15) & ~15);
+        const uint32_t tx = (uint32_t)kChunks * (16u << bl) * kChunkRowBytes;
+        const int b_row = cur.tt * kTileRows;
+        for (int kb = 0; kb < a.K / kBK; ++kb) {
+          if (!wait_or_abort(R.bar(kBarEmpty + stage), phase ^ 1, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full = R.bar(kBarFull + stage);
+          mbar_expect_tx(full, tx);
+          tma_load_3d_hint(smem_u32(stage_ring + stage * stage_bytes), &tmB.box[bl], full, 0,
+                           b_row, kChunks * kb, pol_x);
+          last_stg[stage] = (int)phase;
+          if (++stage == n_stages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok || *abort_flag) {
         for (int s = 0; s < kMaxStages; ++s)
           if (last_stg[s] >= 0) mbar_wait(R.bar(kBarFull + s), (uint32_t)last_stg[s]);
       }
     }
-  } else if (warp >= 6) {
+  } else if (warp >= 6 && warp < 6 + kDecodeWarps) {
     // ------------------------------------------------------------ decode into TMEM
-    // (warps 6..13) Packed row m: 128 B per slot, 16-byte chunk c stored at
-    // chunk c ^ (m & 7) (128-byte swizzle).  Half h of the slot (K 128h..128h+127)
-    // is chunks 4h..4h+3 and goes to one TMEM A slot; each warp of a quadrant
-    // pair decodes two of those four chunks.
+    // Packed row m: 128 B per slot (256 K), 16-byte chunk c stored at chunk
+    // c ^ (m & 7) (128-byte swizzle).  A packed slot becomes one TMEM A slot:
+    // half h (K 128h..128h+127, chunks 4h..4h+3) goes to columns 64h..64h+63;
+    // the kDecodePerQuad warps of a quadrant split each half's four chunks.
     const int q = warp & 3;
-    const int wpair = (warp - 6) >> 2;
+    const int wq = (warp - 6) >> 2;            // warp within its quadrant
     const int m = q * 32 + lane;                 // weight row of this thread
     const uint32_t lane_q = (uint32_t)(q * 32) << 16;
     const uint32_t swz = (uint32_t)(m & 7);
@@ -259,44 +292,34 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
       const TileInfo cur = queue_pop_warp(Q, qp, abort_flag, a.status);
       if (cur.rows == 0) break;
       for (int kr = 0; kr < kraw && ok; ++kr) {
-        if (!wait_or_abort(R.bar(kBarRawFull + rs), rphase, abort_flag, a.status)) {
+        // the packed slot has landed and the TMEM slot's previous MMAs are done
+        if (!wait_or_abort(R.bar(kBarRawFull + rs), rphase, abort_flag, a.status) ||
+            !wait_or_abort(R.bar(kBarAFree + slot), aphase ^ 1, abort_flag, a.status)) {
           ok = false;
           break;
         }
+        tc_fence_after();
         const uint32_t rb = smem_u32(raw_ring + rs * kRawSlotBytes);
+        const uint32_t acol = tmem + lane_q + a_base + slot * kACols;
+#pragma unroll
         for (int h = 0; h < 2; ++h) {
-          // the TMEM slot's previous MMAs are done
-          if (!wait_or_abort(R.bar(kBarAFree + slot), aphase ^ 1, abort_flag, a.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
           // row m's 8 block scales of this half: atoms 2h and 2h+1
           const uint32_t s03 = lds32(rb + kRawBytes + (2 * h) * kAtom + (m & 31) * 16 + (m >> 5) * 4);
           const uint32_t s47 =
               lds32(rb + kRawBytes + (2 * h + 1) * kAtom + (m & 31) * 16 + (m >> 5) * 4);
-          const uint32_t acol = tmem + lane_q + a_base + slot * kACols;
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {       // 32 elements per 16-byte chunk
-            const int c = 2 * wpair + cc;        // chunk within the half
+          for (int cc = 0; cc < kChunksPerWarp; ++cc) {  // 32 elements per 16-byte chunk
+            const int c = kChunksPerWarp * wq + cc;        // chunk within the half
             const uint4 raw = lds128(rb + m * 128 + (((uint32_t)(4 * h + c) ^ swz) << 4));
             const uint32_t sw = c < 2 ? s03 : s47;
-            const uint32_t sc0 = e4m3_to_f16x2_bcast(sw >> (16 * (c & 1)));
-            const uint32_t sc1 = e4m3_to_f16x2_bcast(sw >> (16 * (c & 1) + 8));
+            const uint32_t sc0 = e4m3_scale_bf16x2((sw >> (16 * (c & 1))) & 0xFFu);
+            const uint32_t sc1 = e4m3_scale_bf16x2((sw >> (16 * (c & 1) + 8)) & 0xFFu);
             uint32_t o[16];
             decode8_bf16(raw.x, sc0, o);
             decode8_bf16(raw.y, sc0, o + 4);
             decode8_bf16(raw.z, sc1, o + 8);
             decode8_bf16(raw.w, sc1, o + 12);
-            tmem_st16(acol + 16 * c, o);
-          }
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(R.bar(kBarAReady + slot));
-          if (++slot == n_aslots) {
-            slot = 0;
-            aphase ^= 1;
+            tmem_st16(acol + 64 * h + 16 * c, o);
           }
         }
         // this warp has read its part of the packed slot
@@ -306,11 +329,23 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
           rs = 0;
           rphase ^= 1;
         }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(R.bar(kBarAReady + slot));
+        if (++slot == n_aslots) {
+          slot = 0;
+          aphase ^= 1;
+        }
       }
       ok = __all_sync(0xFFFFFFFFu, ok);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == kIssuerWarp1) {
+    // ------------------------------------------------------------ MMA issuers
+    // Issuer `part` (warp 1: 0, the last warp: 1) issues the K steps of its
+    // parity into its partial sum; one thread issues an MMA about every 60 ns
+    // whatever its shape, so two issuers double the rate for small token tiles.
+    const int part = warp == 1 ? 0 : 1;
     if (lane == 0) {
       int stage = 0, slot = 0, local = 0;
       uint32_t phase = 0, aphase = 0;
@@ -322,6 +357,7 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
         if (cur.rows == 0) break;
         const int n16 = (cur.rows + 15) & ~15;
         const uint32_t idesc = idesc_bf16(128, n16);
+        const int chunk_bytes = box_rows(n16) * kChunkRowBytes;  // this tile's chunk stride
         const int buf = local % nbuf;
         const uint32_t acc_par = ((uint32_t)(local / nbuf) & 1u) ^ 1u;
         if (!wait_or_abort(R.bar(kBarAccEmpty + buf), acc_par, abort_flag, a.status)) {
@@ -340,11 +376,11 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
           const uint8_t* sb = stage_ring + stage * stage_bytes;
           const uint32_t acol = tmem + a_base + slot * kACols;
 #pragma unroll
-          for (int ks = 0; ks < kBK / 16; ++ks) {
+          for (int kp = 0; kp < kBK / 32; ++kp) {
+            const int ks = 2 * kp + part;
             const uint64_t bdesc = smem_desc(
                 smem_u32(sb + (ks >> 2) * chunk_bytes + (ks & 3) * 32), 16, 1024, 2);
-            const int part = nacc == 2 ? (ks & 1) : 0;
-            const uint32_t first = (kb == 0 && ks < nacc) ? 1u : 0u;
+            const uint32_t first = (kb == 0 && kp == 0) ? 1u : 0u;
             mma_bf16_ts(acc + part * acc_cols, acol + 8 * ks, bdesc, idesc, first ? 0u : 1u);
           }
           issued = true;
@@ -364,8 +400,8 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
         ++local;
       }
       if ((!ok || *abort_flag) && issued) {
-        tc_commit(R.bar(kBarDrain));
-        mbar_wait(R.bar(kBarDrain), 0);
+        tc_commit(R.bar(kBarDrain + part));
+        mbar_wait(R.bar(kBarDrain + part), 0);
       }
     }
   } else {
@@ -384,7 +420,8 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
       const int row0 = cur.tt * kTileRows;
       const int buf = local % nbuf;
       const uint32_t acc_par = (uint32_t)(local / nbuf) & 1u;
-      const float alpha = rows ? a.alpha[cur.e] : 0.0f;
+      // the decoded weights carry a factor 2^-8 (exactly undone here)
+      const float alpha = rows ? a.alpha[cur.e] * kDecodeUnscale : 0.0f;
       if (rows == 0 || !wait_or_abort(R.bar(kBarAccFull + buf), acc_par, abort_flag, a.status))
         *epi_stop = 1;
       named_bar_sync(1, 128);
@@ -479,7 +516,7 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
 }
 
 template <int MODE>
-static cudaError_t launch_w4a16_mode(const CUtensorMap& tmA, const CUtensorMap& tmB,
+static cudaError_t launch_w4a16_mode(const CUtensorMap& tmA, const TokenMaps& tmB,
                                      const GemmArgs& a, int grid, cudaStream_t s) {
   static bool configured = false;
   if (!configured) {
@@ -493,7 +530,7 @@ static cudaError_t launch_w4a16_mode(const CUtensorMap& tmA, const CUtensorMap& 
                     (size_t)w4a16::kSmemBytes, s, tmA, tmB, a);
 }
 
-cudaError_t launch_gemm_w4a16(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+cudaError_t launch_gemm_w4a16(const CUtensorMap& tmA, const TokenMaps& tmB, const GemmArgs& a,
                               int grid, cudaStream_t s) {
   switch (a.mode) {
     case kFc1Relu2: return launch_w4a16_mode<kFc1Relu2>(tmA, tmB, a, grid, s);

@@ -172,7 +172,7 @@ cudaError_t launch_selftest_wait(const int32_t* never_set, int32_t* status, cuda
 // W4A16: tmA over packed weights (128-byte boxes, 128-byte swizzle), tmB over bf16
 // token rows (128-byte boxes, 128-byte swizzle); route_out receives the bf16
 // activated rows (FC1, row stride I) or the bf16 route rows (FC2, stride H).
-cudaError_t launch_gemm_w4a16(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+cudaError_t launch_gemm_w4a16(const CUtensorMap& tmA, const TokenMaps& tmB, const GemmArgs& a,
                               int grid, cudaStream_t s);
 
 }  // namespace moe

@@ -173,6 +173,26 @@ bool make_token_maps(TokenMaps* t, const void* base, uint64_t row_bytes, uint64_
   return true;
 }
 
+// The four token-stage maps of a bf16 [rows][row_bytes] buffer for the W4A16
+// GEMM: a 3-D view (128-byte chunk of a row, row, chunk index) whose box
+// (128 B, 16 << i rows, 4 chunks) lands chunk-major in shared memory, i.e. four
+// 128-byte-swizzled K-major chunks (256 K) of box-height rows, in one copy.
+bool make_token_maps_3d(TokenMaps* t, const void* base, uint64_t row_bytes, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  for (int i = 0; i < 4; ++i) {
+    cuuint64_t dims[3] = {128, rows, row_bytes / 128};
+    cuuint64_t strides[2] = {row_bytes, 128};
+    cuuint32_t box[3] = {128, 16u << i, 4};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(&t->box[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+  }
+  return true;
+}
+
 moe_status check_weights(const moe_nvfp4_weights* w) {
   if (!w || !w->fc1_codes || !w->fc1_sf || !w->fc1_alpha || !w->fc2_codes || !w->fc2_sf ||
       !w->fc2_alpha)
@@ -527,11 +547,12 @@ static moe_status forward_w4a16_impl(const moe_dims* d, const moe_nvfp4_weights*
   // padded sizes: stored weights, token rows and every workspace row
   const int H = (int)hp_of(d), I = (int)ip_of(d), N1 = (int)n1p_of(d);
 
-  CUtensorMap tmA1, tmB1, tmA2, tmB2;
+  CUtensorMap tmA1, tmA2;
+  TokenMaps tmB1, tmB2;
   if (!make_tmap_bytes(&tmA1, w->fc1_codes, H / 2, (uint64_t)d->E * N1, 128) ||
-      !make_tmap_bytes(&tmB1, at<uint8_t>(ws, L.x_perm), 2 * (uint64_t)H, L.rows_cap, 16) ||
+      !make_token_maps_3d(&tmB1, at<uint8_t>(ws, L.x_perm), 2 * (uint64_t)H, L.rows_cap) ||
       !make_tmap_bytes(&tmA2, w->fc2_codes, I / 2, (uint64_t)d->E * H, 128) ||
-      !make_tmap_bytes(&tmB2, at<uint8_t>(ws, L.act_bf16), 2 * (uint64_t)I, L.rows_cap, 16))
+      !make_token_maps_3d(&tmB2, at<uint8_t>(ws, L.act_bf16), 2 * (uint64_t)I, L.rows_cap))
     return MOE_ERR_CUDA;
 
   mark(0, s);

@@ -121,6 +121,15 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "l"(policy)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar, int32_t c0, int32_t c1, int32_t c2,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
                                           uint32_t bar) {
   asm volatile(
@@ -340,36 +349,49 @@ __device__ __forceinline__ uint32_t cvt_e4m3(float v) {
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(out) : "f"(v), "f"(v));
   return out & 0xFFu;
 }
-// E4M3 byte -> f16x2 holding that value in both halves (exact).
-__device__ __forceinline__ uint32_t e4m3_to_f16x2_bcast(uint32_t b) {
+// Decoding NVFP4 weights to bf16 without conversion instructions (the
+// conversion pipe is a small fraction of the integer and FMA pipes):
+//   * an E2M1 code c = s e1 e0 m0 written as the bf16 bits s<<15 | (c & 7)<<6
+//     reads as its E2M1 value x 2^-126 -- the exponent field is e1e0 and the top
+//     mantissa bit m0, and E2M1's subnormal (0.5) lands on a bf16 subnormal of
+//     the same relative step;
+//   * a UE4M3 block scale shifted into fp32's exponent/mantissa fields reads as
+//     its value x 2^-120 (again subnormals included); two exact power-of-two
+//     products make it scale x 2^118, a normal bf16 for every scale;
+//   * their bf16 product is code x scale x 2^-8: at most 6 significant bits and
+//     within bf16's normal range, so exact.  The GEMM epilogue multiplies the
+//     accumulator by alpha x 2^8 (exact) to undo the factor.
+constexpr float kDecodeUnscale = 256.0f;  // 2^8
+
+// UE4M3 byte -> bf16x2 holding (its value x 2^118) in both halves.
+__device__ __forceinline__ uint32_t e4m3_scale_bf16x2(uint32_t b) {
+  const float v = __uint_as_float((b & 0x7Fu) << 20);  // value x 2^-120
+  float t, u;
+  asm("mul.rn.f32 %0, %1, 0f7B000000;" : "=f"(t) : "f"(v));  // x 2^119
+  asm("mul.rn.f32 %0, %1, 0f7B000000;" : "=f"(u) : "f"(t));  // x 2^119
   uint32_t out;
-  const uint16_t pair = (uint16_t)((b & 0xFFu) | ((b & 0xFFu) << 8));
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(out) : "h"(pair));
+  asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(out) : "f"(u));
   return out;
 }
 
-// 8 E2M1 codes (one 32-bit word, element 0 in the low nibble) times a block
-// scale given as f16x2 -> 4 bf16x2 words (element 0 in the low half).  Every
-// E2M1 x E4M3 product has at most 5 significant bits and lies in [2^-10, 2688],
-// so the f16 multiply and the f16 -> f32 -> bf16 conversions are exact.
-__device__ __forceinline__ void decode8_bf16(uint32_t w, uint32_t scale_f16x2, uint32_t* o) {
-  uint32_t h[4];
-  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
-      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
-      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
-      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
-      : "r"(w));
+// 8 E2M1 codes (one 32-bit word, element 0 in the low nibble) -> 4 bf16x2 words
+// (element 0 in the low half) of code x scale x 2^-8, the scale given by
+// e4m3_scale_bf16x2.  Per pair of codes: a byte permute puts them 16 bits apart
+// (the sign-replicating selector of a byte below 0x80 yields zero), one
+// multiply by 4160 = 2^6 + 2^12 makes the shifted copies that hold the
+// magnitude bits (<< 6) and the sign bit (<< 12), a mask keeps those bits, and
+// one bf16x2 multiply applies the scale.
+__device__ __forceinline__ void decode8_bf16(uint32_t w, uint32_t scale, uint32_t* o) {
+  const uint32_t ev = w & 0x0F0F0F0Fu;         // codes 0, 2, 4, 6 (one per byte)
+  const uint32_t od = (w >> 4) & 0x0F0F0F0Fu;  // codes 1, 3, 5, 7
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint32_t p;
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(p) : "r"(h[i]), "r"(scale_f16x2));
-    float lo, hi;
-    asm("{\n .reg .b16 l, u;\n mov.b32 {l, u}, %2;\n cvt.f32.f16 %0, l;\n cvt.f32.f16 %1, u;\n}"
-        : "=f"(lo), "=f"(hi)
-        : "r"(p));
-    uint32_t b;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(b) : "f"(hi), "f"(lo));
-    o[i] = b;
+  for (int j = 0; j < 4; ++j) {
+    // result bytes: [code 2j, 0, code 2j+1, 0]
+    const uint32_t sel = (uint32_t)j | ((8u | j) << 4) | ((4u + j) << 8) | ((8u | j) << 12);
+    uint32_t y;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(y) : "r"(ev), "r"(od), "r"(sel));
+    const uint32_t x = (y * 4160u) & 0x81C081C0u;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[j]) : "r"(x), "r"(scale));
   }
 }
 
