@@ -55,8 +55,7 @@ constexpr int kChunks = kBK / 64;           // 64-element (128-byte) K chunks pe
 constexpr int kChunkRowBytes = 128;         // 64 bf16 per row per K chunk
 constexpr int kACols = kBK / 2;             // TMEM columns of one decoded A slot
 constexpr int kMaxRaw = 6;                  // packed-weight slots (released after decode)
-constexpr int kMaxStages = 12;              // token stages (released by the MMAs)
-constexpr int kMaxASlots = 3;               // TMEM slots of decoded weights
+constexpr int kMaxRing = 3;                 // blocks in flight: token stage + TMEM slot of decoded A
 constexpr int kMaxAcc = 2;
 constexpr int kTmemCols = 512;
 constexpr int kXchgFloats = 2 * 64 * 33;
@@ -71,14 +70,14 @@ constexpr int kIssuers = 2;                 // MMA issuers: even and odd K steps
 constexpr int kIssuerWarp1 = 6 + kDecodeWarps;      // warp of the second issuer
 constexpr int kTokenWarp = 7 + kDecodeWarps;        // token-stage producer
 constexpr int kThreads = (8 + kDecodeWarps) * 32;
-static_assert(kDecodePerQuad * 4 == kDecodeWarps && kChunksPerWarp * kDecodePerQuad == 4, "decode");
+static_assert(kDecodePerQuad * 4 == kDecodeWarps && kChunksPerWarp * kDecodePerQuad == 4 &&
+                  kChunksPerWarp <= 2, "decode: a warp's chunks share one scale atom");
 constexpr int kBarRawFull = 0;
 constexpr int kBarRawEmpty = kBarRawFull + kMaxRaw;
-constexpr int kBarFull = kBarRawEmpty + kMaxRaw;          // token stages
-constexpr int kBarEmpty = kBarFull + kMaxStages;
-constexpr int kBarAReady = kBarEmpty + kMaxStages;        // per TMEM A slot
-constexpr int kBarAFree = kBarAReady + kMaxASlots;
-constexpr int kBarAccFull = kBarAFree + kMaxASlots;
+constexpr int kBarFull = kBarRawEmpty + kMaxRaw;          // token stage landed (TMA bytes)
+constexpr int kBarReady = kBarFull + kMaxRing;            // A decoded and token stage landed
+constexpr int kBarFree = kBarReady + kMaxRing;            // the block's MMAs are done
+constexpr int kBarAccFull = kBarFree + kMaxRing;
 constexpr int kBarAccEmpty = kBarAccFull + kMaxAcc;
 constexpr int kBarItemFull = kBarAccEmpty + kMaxAcc;
 constexpr int kBarItemEmpty = kBarItemFull + kItemSlots;
@@ -117,13 +116,10 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
       mbar_init(R.bar(kBarRawFull + s), 1);
       mbar_init(R.bar(kBarRawEmpty + s), kDecodeWarps);
     }
-    for (int s = 0; s < kMaxStages; ++s) {
-      mbar_init(R.bar(kBarFull + s), 1);
-      mbar_init(R.bar(kBarEmpty + s), kIssuers);
-    }
-    for (int j = 0; j < kMaxASlots; ++j) {
-      mbar_init(R.bar(kBarAReady + j), kDecodeWarps);
-      mbar_init(R.bar(kBarAFree + j), kIssuers);
+    for (int j = 0; j < kMaxRing; ++j) {
+      mbar_init(R.bar(kBarFull + j), 1);
+      mbar_init(R.bar(kBarReady + j), kDecodeWarps);
+      mbar_init(R.bar(kBarFree + j), kIssuers);
     }
     for (int b = 0; b < kMaxAcc; ++b) {
       mbar_init(R.bar(kBarAccFull + b), kIssuers);
@@ -166,13 +162,14 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
   const int acc_stride = nacc * acc_cols;                  // TMEM columns per item
   const int nbuf = max_n16 <= 64 ? 2 : 1;                  // accumulator buffers
   const int a_base = nbuf * acc_stride;                    // decoded A slots follow the accumulators
-  int n_aslots = (kTmemCols - a_base) / kACols;
-  if (n_aslots > kMaxASlots) n_aslots = kMaxASlots;
   const int n_raw = max_n16 <= 64 ? kMaxRaw : 4;
   uint8_t* raw_ring = rings;
   uint8_t* stage_ring = rings + n_raw * kRawSlotBytes;     // multiple of 1024 past rings
-  int n_stages = (kRingBudget - n_raw * kRawSlotBytes) / stage_bytes;
-  if (n_stages > kMaxStages) n_stages = kMaxStages;
+  // Block ring: block b of the CTA's K stream uses token stage and TMEM A slot
+  // b % n_ring, so one barrier says "ready" (decoded and landed) and one "free".
+  int n_ring = (kTmemCols - a_base) / kACols;
+  n_ring = min(n_ring, (kRingBudget - n_raw * kRawSlotBytes) / stage_bytes);
+  n_ring = min(n_ring, kMaxRing);
 
   const int kraw = a.K / kRawK;                        // packed-weight slots per item
   const int atoms = a.K / 64;
@@ -238,9 +235,9 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
     // One 3-D tiled copy per token stage: the kChunks 64-K chunks of the tile's
     // rows, in the smallest of the 16/32/64/128-row boxes that covers them.
     if (lane == 0) {
-      int last_stg[kMaxStages];
+      int last_stg[kMaxRing];
 #pragma unroll
-      for (int s = 0; s < kMaxStages; ++s) last_stg[s] = -1;
+      for (int s = 0; s < kMaxRing; ++s) last_stg[s] = -1;
       const uint64_t pol_x = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
@@ -253,7 +250,7 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
         const uint32_t tx = (uint32_t)kChunks * (16u << bl) * kChunkRowBytes;
         const int b_row = cur.tt * kTileRows;
         for (int kb = 0; kb < a.K / kBK; ++kb) {
-          if (!wait_or_abort(R.bar(kBarEmpty + stage), phase ^ 1, abort_flag, a.status)) {
+          if (!wait_or_abort(R.bar(kBarFree + stage), phase ^ 1, abort_flag, a.status)) {
             ok = false;
             break;
           }
@@ -262,14 +259,14 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
           tma_load_3d_hint(smem_u32(stage_ring + stage * stage_bytes), &tmB.box[bl], full, 0,
                            b_row, kChunks * kb, pol_x);
           last_stg[stage] = (int)phase;
-          if (++stage == n_stages) {
+          if (++stage == n_ring) {
             stage = 0;
             phase ^= 1;
           }
         }
       }
       if (!ok || *abort_flag) {
-        for (int s = 0; s < kMaxStages; ++s)
+        for (int s = 0; s < kMaxRing; ++s)
           if (last_stg[s] >= 0) mbar_wait(R.bar(kBarFull + s), (uint32_t)last_stg[s]);
       }
     }
@@ -294,7 +291,7 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
       for (int kr = 0; kr < kraw && ok; ++kr) {
         // the packed slot has landed and the TMEM slot's previous MMAs are done
         if (!wait_or_abort(R.bar(kBarRawFull + rs), rphase, abort_flag, a.status) ||
-            !wait_or_abort(R.bar(kBarAFree + slot), aphase ^ 1, abort_flag, a.status)) {
+            !wait_or_abort(R.bar(kBarFree + slot), aphase ^ 1, abort_flag, a.status)) {
           ok = false;
           break;
         }
@@ -303,17 +300,16 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
         const uint32_t acol = tmem + lane_q + a_base + slot * kACols;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          // row m's 8 block scales of this half: atoms 2h and 2h+1
-          const uint32_t s03 = lds32(rb + kRawBytes + (2 * h) * kAtom + (m & 31) * 16 + (m >> 5) * 4);
-          const uint32_t s47 =
-              lds32(rb + kRawBytes + (2 * h + 1) * kAtom + (m & 31) * 16 + (m >> 5) * 4);
+          // row m's block scales of this warp's chunks: one 4-scale word of atom
+          // 2h (chunks 0-1) or 2h+1 (chunks 2-3)
+          const int atom = 2 * h + (kChunksPerWarp * wq >= 2 ? 1 : 0);
+          const uint32_t sw = lds32(rb + kRawBytes + atom * kAtom + (m & 31) * 16 + (m >> 5) * 4);
 #pragma unroll
           for (int cc = 0; cc < kChunksPerWarp; ++cc) {  // 32 elements per 16-byte chunk
             const int c = kChunksPerWarp * wq + cc;        // chunk within the half
             const uint4 raw = lds128(rb + m * 128 + (((uint32_t)(4 * h + c) ^ swz) << 4));
-            const uint32_t sw = c < 2 ? s03 : s47;
-            const uint32_t sc0 = e4m3_scale_bf16x2((sw >> (16 * (c & 1))) & 0xFFu);
-            const uint32_t sc1 = e4m3_scale_bf16x2((sw >> (16 * (c & 1) + 8)) & 0xFFu);
+            uint32_t sc0, sc1;
+            e4m3x2_scale_bf16x2(sw >> (16 * (c & 1)), sc0, sc1);
             uint32_t o[16];
             decode8_bf16(raw.x, sc0, o);
             decode8_bf16(raw.y, sc0, o + 4);
@@ -331,9 +327,15 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
         }
         tmem_wait_st();
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(R.bar(kBarAReady + slot));
-        if (++slot == n_aslots) {
+        // warp 6 also waits for the block's token stage, so that "ready"
+        // covers both operands and the MMA issuers wait on one barrier
+        if (warp == 6 && lane == 0 &&
+            !wait_or_abort(R.bar(kBarFull + slot), aphase, abort_flag, a.status))
+          ok = false;
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0) && ok;
+        if (!ok) break;
+        if (lane == 0) mbar_arrive(R.bar(kBarReady + slot));
+        if (++slot == n_ring) {
           slot = 0;
           aphase ^= 1;
         }
@@ -343,66 +345,56 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
   } else if (warp == 1 || warp == kIssuerWarp1) {
     // ------------------------------------------------------------ MMA issuers
     // Issuer `part` (warp 1: 0, the last warp: 1) issues the K steps of its
-    // parity into its partial sum; one thread issues an MMA about every 60 ns
-    // whatever its shape, so two issuers double the rate for small token tiles.
+    // parity into its partial sum.  The whole warp runs the loop (waits and
+    // descriptors are warp-uniform) and elect.sync picks the lane that issues
+    // each MMA and commit: that keeps the MMA rate near the tensor pipe's even
+    // for 16-token tiles, where a single-lane loop is bound by issue latency.
     const int part = warp == 1 ? 0 : 1;
-    if (lane == 0) {
-      int stage = 0, slot = 0, local = 0;
-      uint32_t phase = 0, aphase = 0;
-      QueuePos qp;
-      bool ok = true, issued = false;
-      const int kblocks = a.K / kBK;
-      while (ok) {
-        const TileInfo cur = queue_pop_thread(Q, qp, abort_flag, a.status);
-        if (cur.rows == 0) break;
-        const int n16 = (cur.rows + 15) & ~15;
-        const uint32_t idesc = idesc_bf16(128, n16);
-        const int chunk_bytes = box_rows(n16) * kChunkRowBytes;  // this tile's chunk stride
-        const int buf = local % nbuf;
-        const uint32_t acc_par = ((uint32_t)(local / nbuf) & 1u) ^ 1u;
-        if (!wait_or_abort(R.bar(kBarAccEmpty + buf), acc_par, abort_flag, a.status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t acc = tmem + buf * acc_stride;
-        for (int kb = 0; kb < kblocks; ++kb) {
-          if (!wait_or_abort(R.bar(kBarAReady + slot), aphase, abort_flag, a.status) ||
-              !wait_or_abort(R.bar(kBarFull + stage), phase, abort_flag, a.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint8_t* sb = stage_ring + stage * stage_bytes;
-          const uint32_t acol = tmem + a_base + slot * kACols;
-#pragma unroll
-          for (int kp = 0; kp < kBK / 32; ++kp) {
-            const int ks = 2 * kp + part;
-            const uint64_t bdesc = smem_desc(
-                smem_u32(sb + (ks >> 2) * chunk_bytes + (ks & 3) * 32), 16, 1024, 2);
-            const uint32_t first = (kb == 0 && kp == 0) ? 1u : 0u;
-            mma_bf16_ts(acc + part * acc_cols, acol + 8 * ks, bdesc, idesc, first ? 0u : 1u);
-          }
-          issued = true;
-          tc_commit(R.bar(kBarEmpty + stage));
-          tc_commit(R.bar(kBarAFree + slot));
-          if (++stage == n_stages) {
-            stage = 0;
-            phase ^= 1;
-          }
-          if (++slot == n_aslots) {
-            slot = 0;
-            aphase ^= 1;
-          }
-        }
+    int slot = 0, local = 0;
+    uint32_t aphase = 0;
+    QueuePos qp;
+    bool ok = true, issued = false;
+    const int kblocks = a.K / kBK;
+    while (ok) {
+      const TileInfo cur = queue_pop_warp(Q, qp, abort_flag, a.status);
+      if (cur.rows == 0) break;
+      const int n16 = (cur.rows + 15) & ~15;
+      const uint32_t idesc = idesc_bf16(128, n16);
+      const int chunk_bytes = box_rows(n16) * kChunkRowBytes;  // this tile's chunk stride
+      const int buf = local % nbuf;
+      const uint32_t acc_par = ((uint32_t)(local / nbuf) & 1u) ^ 1u;
+      ok = __all_sync(0xFFFFFFFFu,
+                      wait_or_abort(R.bar(kBarAccEmpty + buf), acc_par, abort_flag, a.status));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t acc = tmem + buf * acc_stride + part * acc_cols;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        ok = __all_sync(0xFFFFFFFFu,
+                        wait_or_abort(R.bar(kBarReady + slot), aphase, abort_flag, a.status));
         if (!ok) break;
-        tc_commit(R.bar(kBarAccFull + buf));
-        ++local;
+        tc_fence_after();
+        const uint32_t sb = smem_u32(stage_ring + slot * stage_bytes);
+        const uint32_t acol = tmem + a_base + slot * kACols;
+#pragma unroll
+        for (int kp = 0; kp < kBK / 32; ++kp) {
+          const int ks = 2 * kp + part;
+          const uint64_t bdesc = smem_desc(sb + (ks >> 2) * chunk_bytes + (ks & 3) * 32, 16, 1024, 2);
+          mma_bf16_ts_warp(acc, acol + 8 * ks, bdesc, idesc, (kb == 0 && kp == 0) ? 0u : 1u);
+        }
+        issued = true;
+        tc_commit_warp(R.bar(kBarFree + slot));
+        if (++slot == n_ring) {
+          slot = 0;
+          aphase ^= 1;
+        }
       }
-      if ((!ok || *abort_flag) && issued) {
-        tc_commit(R.bar(kBarDrain + part));
-        mbar_wait(R.bar(kBarDrain + part), 0);
-      }
+      if (!ok) break;
+      tc_commit_warp(R.bar(kBarAccFull + buf));
+      ++local;
+    }
+    if ((!ok || *abort_flag) && issued) {
+      tc_commit_warp(R.bar(kBarDrain + part));
+      mbar_wait(R.bar(kBarDrain + part), 0);
     }
   } else {
     // ------------------------------------------------------------ epilogue

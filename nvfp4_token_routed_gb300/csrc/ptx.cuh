@@ -276,6 +276,25 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// Whole-warp forms: every lane of a converged warp executes them with the same
+// (warp-uniform) operands and elect.sync picks the one lane that issues.  Run
+// this way, the descriptor arithmetic stays on the uniform datapath and a warp
+// issues an MMA every ~13 ns, against ~25-70 ns from a single-lane branch.
+__device__ __forceinline__ void mma_bf16_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_warp(uint32_t bar) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(bar)
+      : "memory");
+}
+
 // Copy one 512-byte scale-factor atom (32 rows x 16 bytes) from shared memory to
 // 4 TMEM columns of lanes 0..31, replicated to the four 32-lane quadrants.
 __device__ __forceinline__ void tc_cp_sf_atom(uint32_t taddr, uint64_t sdesc) {
@@ -355,28 +374,29 @@ __device__ __forceinline__ uint32_t cvt_e4m3(float v) {
 //     reads as its E2M1 value x 2^-126 -- the exponent field is e1e0 and the top
 //     mantissa bit m0, and E2M1's subnormal (0.5) lands on a bf16 subnormal of
 //     the same relative step;
-//   * a UE4M3 block scale shifted into fp32's exponent/mantissa fields reads as
-//     its value x 2^-120 (again subnormals included); two exact power-of-two
-//     products make it scale x 2^118, a normal bf16 for every scale;
+//   * two UE4M3 block scales become an exact f16x2 (E4M3 subnormals are f16
+//     normals); shifting each half right by 3 moves the f16 fields onto bf16's
+//     and adding 230 to each exponent field makes scale x 2^118, a normal bf16
+//     (a zero scale gives 2^103 instead of 0, harmless: every code of an
+//     all-zero block is +-0, and +-0 times a finite scale is +-0);
 //   * their bf16 product is code x scale x 2^-8: at most 6 significant bits and
 //     within bf16's normal range, so exact.  The GEMM epilogue multiplies the
 //     accumulator by alpha x 2^8 (exact) to undo the factor.
 constexpr float kDecodeUnscale = 256.0f;  // 2^8
 
-// UE4M3 byte -> bf16x2 holding (its value x 2^118) in both halves.
-__device__ __forceinline__ uint32_t e4m3_scale_bf16x2(uint32_t b) {
-  const float v = __uint_as_float((b & 0x7Fu) << 20);  // value x 2^-120
-  float t, u;
-  asm("mul.rn.f32 %0, %1, 0f7B000000;" : "=f"(t) : "f"(v));  // x 2^119
-  asm("mul.rn.f32 %0, %1, 0f7B000000;" : "=f"(u) : "f"(t));  // x 2^119
-  uint32_t out;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(out) : "f"(u));
-  return out;
+// Two UE4M3 bytes (low 16 bits of b, first in the low byte) -> bf16x2 words
+// holding (first x 2^118) and (second x 2^118) in both halves.
+__device__ __forceinline__ void e4m3x2_scale_bf16x2(uint32_t b, uint32_t& s0, uint32_t& s1) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((uint16_t)(b & 0xFFFFu)));
+  const uint32_t t = (h >> 3) + 0x73007300u;
+  s0 = __byte_perm(t, 0, 0x1010);
+  s1 = __byte_perm(t, 0, 0x3232);
 }
 
 // 8 E2M1 codes (one 32-bit word, element 0 in the low nibble) -> 4 bf16x2 words
 // (element 0 in the low half) of code x scale x 2^-8, the scale given by
-// e4m3_scale_bf16x2.  Per pair of codes: a byte permute puts them 16 bits apart
+// e4m3x2_scale_bf16x2.  Per pair of codes: a byte permute puts them 16 bits apart
 // (the sign-replicating selector of a byte below 0x80 yields zero), one
 // multiply by 4160 = 2^6 + 2^12 makes the shifted copies that hold the
 // magnitude bits (<< 6) and the sign bit (<< 12), a mask keeps those bits, and
