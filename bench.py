@@ -451,9 +451,10 @@ def run_ours(args, rank, world, local_rank):
     fc1_bytes, U, R = algorithmic_fc1_bytes(wl, ids, args.w4a16)
     fc1_mean = statistics.fmean(fc1_ms)
     fc2_mean = statistics.fmean(fc2_ms)
-    # the library runs FC1, the FC2-input requant and FC2 as one launch for small
-    # batches (its FC2 marker interval is then empty): the roofline is that launch's
-    fused = fc2_mean < 0.02 * fc1_mean
+    # the W4A4 forward runs FC1, the FC2-input requant and FC2 as one launch when
+    # T*K <= min(2048, 8*E) (moe_nvfp4.h): the roofline is then that launch's,
+    # FC1 and FC2 bytes over the FC1 marker interval (the FC2 one is empty)
+    fused = (not args.w4a16) and T * K <= min(2048, 8 * wl.E)
     kernel_bytes = fc1_bytes + (algorithmic_fc2_bytes(wl, U, R, args.w4a16) if fused else 0)
     hbm, src = peaks()
     achieved = kernel_bytes / (fc1_mean * 1e-3) / 1e9
