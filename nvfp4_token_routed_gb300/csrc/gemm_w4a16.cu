@@ -9,29 +9,31 @@
 //
 // Structure (swap-AB as in the W4A4 kernel; weights are the M=128 operand and
 // are decoded on chip, never written back to global or shared memory):
-//   * warp 0: TMA producer -- packed E2M1 weight slots (128 rows x 128 B = 256 K
-//     elements, 128-byte swizzle, so each row is read in 128-byte runs) with
-//     their E4M3 scale atoms (bulk copy), and bf16 token stages (two 64-element
-//     K chunks, 128-byte swizzle, 16-row boxes) -- two token stages per slot
+//   * warp 0: weight producer -- claims items and streams packed E2M1 weight
+//     slots (128 rows x 128 B = 256 K elements, 128-byte swizzle, so each row is
+//     read in 128-byte runs) with their E4M3 scale atoms (bulk copy)
+//   * the last warp: token producer -- one 3-D tiled copy per 256-K block: four
+//     64-element K chunks of the tile's bf16 rows (128-byte swizzle), chunk-major,
+//     in the smallest 16/32/64/128-row box that covers the tile
 //   * warps 6..5+kDecodeWarps: decode -- kDecodeWarps/4 warps per TMEM lane
 //     quadrant; thread r of quadrant q owns weight row 32q+r: for each 128-K
 //     half of a packed slot its warps read the packed bytes and their scales
 //     from shared memory, form exact bf16 values of code x scale x 2^-8 with
 //     integer and bf16x2 instructions only (decode8_bf16; the epilogue's alpha
 //     carries the 2^8) and write them into a TMEM A slot (lane = row, 2 K
-//     elements per column); the packed slot is released once both halves are
-//     decoded
-//   * warp 1 (also the TMEM allocator) and the last warp: MMA issuers, one
-//     thread each -- tcgen05.mma.kind::f16 with A from TMEM and B from shared
-//     memory, K = 16 per instruction, N = the tile's token count rounded up to
-//     16; the first issues the even K steps into one partial sum, the second
-//     the odd ones into another (a thread issues one MMA about every 60 ns
-//     whatever its shape, so small token tiles are bound by issue, not math)
+//     elements per column); the packed slot is released once read
+//   * warp 1 (also the TMEM allocator) and warp 6+kDecodeWarps: MMA issuers --
+//     tcgen05.mma.kind::f16 with A from TMEM and B from shared memory, K = 16
+//     per instruction, N = the tile's token count rounded up to 16; the first
+//     issues the even K steps into one partial sum, the second the odd ones
+//     into another, each from a whole warp with elect.sync (a single-lane loop
+//     is bound by issue latency at small N)
 //   * warps 2-5: epilogue (alpha, activation, bf16 rounding), one TMEM lane per
 //     thread; SwiGLU pairs gate and up rows through shared memory as in W4A4
-//   * three rings: packed-weight slots (4-6), token stages (up to 12) and TMEM
-//     slots of decoded weights (4-6); each item's accumulator is split into
-//     even / odd K-step partial sums; 1-2 items in flight; every wait bounded.
+//   * rings: packed-weight slots (4-6) and a ring of 2-3 blocks of 256 K, each
+//     a token stage plus a TMEM slot of decoded weights; each item's
+//     accumulator is split into even / odd K-step partial sums; 1-2 items in
+//     flight; every wait bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
