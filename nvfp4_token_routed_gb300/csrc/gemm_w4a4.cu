@@ -31,7 +31,7 @@
 //     memory into that stage's TMEM scale slot with tcgen05.st, in the layout the
 //     block-scaled MMA reads (row r of a 128-row atom at lane r%32, column r/32,
 //     replicated in all four lane quadrants)
-//   * warp 1: TMEM allocator and single-thread MMA issuer:
+//   * warp 1: TMEM allocator and MMA issuer (whole warp, elect.sync issues):
 //     tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X, K = 64 per
 //     instruction, N = the tile's token count rounded up to 16
 //   * warps 2-5: epilogue, one TMEM lane (= one weight row) per thread; each
@@ -421,60 +421,59 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      int stage = 0, local = 0;
-      uint32_t phase = 0;
-      QueuePos qp;
-      bool ok = true, issued = false;
-      while (ok) {
-        const TileInfo cur = queue_pop_thread(Q, qp, abort_flag, a.status);
-        if (cur.rows == 0) break;
-        if ((cur.mt >> 16) == kPhaseRequant) continue;
-        const int kblocks = a.ph[cur.mt >> 16].K / kBK;
-        const int n16 = (cur.rows + 15) & ~15;
-        const uint32_t idesc = idesc_mxf4nvf4(128, n16);
-        const int buf = local % nbuf;
-        const uint32_t acc_par = ((uint32_t)(local / nbuf) & 1u) ^ 1u;
-        if (!wait_or_abort(R.bar(kBarAccEmpty + buf), acc_par, abort_flag, a.status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t acc = tmem + buf * acc_stride;
-        for (int kb = 0; kb < kblocks; ++kb) {
-          // scales staged (which implies the stage's copies landed); the full
-          // barrier is re-checked so this thread observes the TMA writes itself
-          if (!wait_or_abort(R.bar(kBarSfReady + stage), phase, abort_flag, a.status) ||
-              !wait_or_abort(R.bar(kBarFull + stage), phase, abort_flag, a.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint8_t* sb = stages + stage * stage_bytes;
-          const uint32_t col0 = tmem + sf_base + stage * slot_cols;
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t adesc = smem_desc(smem_u32(sb + ks * 32), 16, 1024, 2);
-            const uint64_t bdesc = smem_desc(smem_u32(sb + off_b + ks * 32), 16, 1024, 2);
-            mma_mxf4nvf4(acc, adesc, bdesc, idesc, col0 + 4 * ks, col0 + 16 + 4 * ks,
-                         (kb | ks) != 0 ? 1u : 0u);
-          }
-          issued = true;
-          tc_commit(R.bar(kBarEmpty + stage));
-          if (++stage == n_stages) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
+    // The whole warp runs the loop (waits and descriptors are warp-uniform) and
+    // elect.sync picks the lane that issues each MMA and commit: a single-lane
+    // loop pays ~60 ns of issue latency per MMA, the warp form ~13 ns.
+    int stage = 0, local = 0;
+    uint32_t phase = 0;
+    QueuePos qp;
+    bool ok = true, issued = false;
+    while (ok) {
+      const TileInfo cur = queue_pop_warp(Q, qp, abort_flag, a.status);
+      if (cur.rows == 0) break;
+      if ((cur.mt >> 16) == kPhaseRequant) continue;
+      const int kblocks = a.ph[cur.mt >> 16].K / kBK;
+      const int n16 = (cur.rows + 15) & ~15;
+      const uint32_t idesc = idesc_mxf4nvf4(128, n16);
+      const int buf = local % nbuf;
+      const uint32_t acc_par = ((uint32_t)(local / nbuf) & 1u) ^ 1u;
+      ok = __all_sync(0xFFFFFFFFu,
+                      wait_or_abort(R.bar(kBarAccEmpty + buf), acc_par, abort_flag, a.status));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t acc = tmem + buf * acc_stride;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        // scales staged (which implies the stage's copies landed); the full
+        // barrier is re-checked so this warp observes the TMA writes itself
+        ok = __all_sync(0xFFFFFFFFu,
+                        wait_or_abort(R.bar(kBarSfReady + stage), phase, abort_flag, a.status) &&
+                            wait_or_abort(R.bar(kBarFull + stage), phase, abort_flag, a.status));
         if (!ok) break;
-        tc_commit(R.bar(kBarAccFull + buf));
-        ++local;
+        tc_fence_after();
+        const uint32_t sb = smem_u32(stages + stage * stage_bytes);
+        const uint32_t col0 = tmem + sf_base + stage * slot_cols;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t adesc = smem_desc(sb + ks * 32, 16, 1024, 2);
+          const uint64_t bdesc = smem_desc(sb + off_b + ks * 32, 16, 1024, 2);
+          mma_mxf4nvf4_warp(acc, adesc, bdesc, idesc, col0 + 4 * ks, col0 + 16 + 4 * ks,
+                            (kb | ks) != 0 ? 1u : 0u);
+        }
+        issued = true;
+        tc_commit_warp(R.bar(kBarEmpty + stage));
+        if (++stage == n_stages) {
+          stage = 0;
+          phase ^= 1;
+        }
       }
-      if ((!ok || *abort_flag) && issued) {
-        // drain the tensor-core work issued so far before TMEM is released
-        tc_commit(R.bar(kBarDrain));
-        mbar_wait(R.bar(kBarDrain), 0);
-      }
+      if (!ok) break;
+      tc_commit_warp(R.bar(kBarAccFull + buf));
+      ++local;
+    }
+    if ((!ok || *abort_flag) && issued) {
+      // drain the tensor-core work issued so far before TMEM is released
+      tc_commit_warp(R.bar(kBarDrain));
+      mbar_wait(R.bar(kBarDrain), 0);
     }
   } else {
     // ------------------------------------------------------------ epilogue
