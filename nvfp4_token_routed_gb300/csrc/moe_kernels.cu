@@ -328,6 +328,108 @@ __global__ void __launch_bounds__(kChunk) route_scatter_kernel(
   if (idx < TK) inv[idx] = p;
 }
 
+// Small batches (TK <= kSmallRoutes): count, scan and scatter in one block of
+// 1024 threads, saving two launches.  Same outputs as the three kernels: the
+// histogram and the tile table as the scan writes them, then the stable
+// scatter in 1024-route chunks (earlier warps of the chunk, then the lane's
+// rank among earlier lanes with the same expert, on top of a running
+// per-expert cursor).  Dynamic shared memory: hist[E], cursor[E], wcnt[32][E].
+constexpr int kSmallRoutes = 2048;  // measured: one block is slower than three kernels at 4096
+__global__ void __launch_bounds__(1024) route_small_kernel(
+    const int32_t* __restrict__ ids, int ids64, int TK, int E, int32_t* __restrict__ counts,
+    int32_t* __restrict__ group_row0, int4* __restrict__ tiles, int32_t* __restrict__ status,
+    int32_t* __restrict__ tile_sync, int tile_sync_words, int32_t* __restrict__ inv,
+    int32_t* __restrict__ perm) {
+  extern __shared__ int s_small[];
+  int* hist = s_small;
+  int* cursor = s_small + E;
+  int* wcnt = s_small + 2 * E;  // [32][E]
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  for (int i = tid; i < tile_sync_words; i += blockDim.x) tile_sync[i] = 0;
+  for (int i = tid; i < E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  // (1) histogram of valid ids, and the invalid-id flag
+  int bad = 0;
+  for (int i = tid; i < TK; i += blockDim.x) {
+    const int e = load_id(ids, i, ids64);
+    if (e >= 0 && e < E)
+      atomicAdd(&hist[e], 1);
+    else if (e != -1)
+      bad = 1;
+  }
+  bad = __syncthreads_or(bad);
+  // (2) exclusive scan of the 128-row-padded group sizes, the tile table and
+  // the largest tile (thread e owns expert e, E <= 1024)
+  const int total = tid < E ? hist[tid] : 0;
+  const int ntiles = (total + kTileRows - 1) / kTileRows;
+  __shared__ int warp_sum[32];
+  __shared__ int max_rows;
+  if (tid == 0) max_rows = 0;
+  int incl = ntiles;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sum[wid] = incl;
+  __syncthreads();
+  if (total > 0) atomicMax(&max_rows, min(kTileRows, total));
+  if (wid == 0) {
+    int v = (lane < (int)(blockDim.x >> 5)) ? warp_sum[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, v, o);
+      if (lane >= o) v += y;
+    }
+    warp_sum[lane] = v;  // inclusive over warps
+  }
+  __syncthreads();
+  const int base = incl - ntiles + (wid > 0 ? warp_sum[wid - 1] : 0);
+  if (tid < E) {
+    counts[tid] = total;
+    group_row0[tid] = base * kTileRows;
+    cursor[tid] = base * kTileRows;
+    for (int j = 0; j < ntiles; ++j) tiles[base + j] = make_int4(tid, base, ntiles, total);
+  }
+  if (tid == (int)blockDim.x - 1) {
+    status[kStatusFlags] = bad ? kFlagBadExpertId : 0;
+    status[kStatusTiles] = base + ntiles;
+    status[kStatusRows] = (base + ntiles) * kTileRows;
+    status[kStatusMaxRows] = max_rows;
+    status[kStatusItemCtr] = 0;
+    status[kStatusItemCtr + 1] = 0;
+  }
+  // (3) stable scatter, one 1024-route chunk after another
+  for (int c0 = 0; c0 < TK; c0 += blockDim.x) {
+    for (int i = tid; i < 32 * E; i += blockDim.x) wcnt[i] = 0;
+    __syncthreads();
+    const int idx = c0 + tid;
+    const int e = idx < TK ? load_id(ids, idx, ids64) : -1;
+    const bool valid = e >= 0 && e < E;
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, valid ? e : -1);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (valid && rank == 0) wcnt[wid * E + e] = __popc(peers);
+    __syncthreads();
+    int p = -1;
+    if (valid) {
+      int before = 0;
+      for (int v = 0; v < wid; ++v) before += wcnt[v * E + e];
+      p = cursor[e] + before + rank;
+      perm[p] = idx;
+    }
+    if (idx < TK) inv[idx] = p;
+    __syncthreads();
+    for (int i = tid; i < E; i += blockDim.x) {
+      int n = 0;
+      for (int v = 0; v < 32; ++v) n += wcnt[v * E + i];
+      cursor[i] += n;
+    }
+    __syncthreads();  // the next chunk clears wcnt only after every thread has read it
+  }
+}
+
 // Gather: one warp per route copies its token's row to the route's permuted row.
 // W4A4 rows are already padded to Hp by the quantizer; W4A16 copies H bf16
 // values and zero-fills the Hp - H padding columns.
@@ -363,15 +465,28 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(
 }
 
 void launch_route(const RouteArgs& a, cudaStream_t s) {
-  const int nchunks = (a.TK + kChunk - 1) / kChunk;
-  launch_pdl(route_count_kernel, dim3(nchunks), dim3(kChunk), sizeof(int) * a.E, s, a.ids,
-             a.ids64, a.TK, a.E, a.chunk_counts);
-  launch_pdl(route_scan_kernel, dim3(1), dim3(1024), 0, s, nchunks, a.E,
-             (const int32_t*)a.chunk_counts, a.chunk_prefix, a.counts, a.group_row0, a.tiles,
-             a.status, a.tile_sync, a.tile_sync_words);
-  const size_t smem = sizeof(int) * (kChunk / 32) * a.E;
-  launch_pdl(route_scatter_kernel, dim3(nchunks), dim3(kChunk), smem, s, a.ids, a.ids64, a.TK, a.E,
-             (const int32_t*)a.chunk_prefix, (const int32_t*)a.group_row0, a.inv, a.perm);
+  if (a.TK <= kSmallRoutes) {
+    const size_t smem = sizeof(int) * 34 * (size_t)a.E;  // hist, cursor, 32 warp rows
+    static bool configured = false;
+    if (!configured) {
+      cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)(sizeof(int) * 34 * 1024));
+      configured = true;
+    }
+    launch_pdl(route_small_kernel, dim3(1), dim3(1024), smem, s, a.ids, a.ids64, a.TK, a.E,
+               a.counts, a.group_row0, a.tiles, a.status, a.tile_sync, a.tile_sync_words, a.inv,
+               a.perm);
+  } else {
+    const int nchunks = (a.TK + kChunk - 1) / kChunk;
+    launch_pdl(route_count_kernel, dim3(nchunks), dim3(kChunk), sizeof(int) * a.E, s, a.ids,
+               a.ids64, a.TK, a.E, a.chunk_counts);
+    launch_pdl(route_scan_kernel, dim3(1), dim3(1024), 0, s, nchunks, a.E,
+               (const int32_t*)a.chunk_counts, a.chunk_prefix, a.counts, a.group_row0, a.tiles,
+               a.status, a.tile_sync, a.tile_sync_words);
+    const size_t smem = sizeof(int) * (kChunk / 32) * a.E;
+    launch_pdl(route_scatter_kernel, dim3(nchunks), dim3(kChunk), smem, s, a.ids, a.ids64, a.TK,
+               a.E, (const int32_t*)a.chunk_prefix, (const int32_t*)a.group_row0, a.inv, a.perm);
+  }
   const int gblocks = (a.TK + 7) / 8;
   if (a.w4a16)
     launch_pdl(gather_rows_kernel<true>, dim3(gblocks), dim3(256), 0, s, a.TK, a.K, a.H, a.Hp,
