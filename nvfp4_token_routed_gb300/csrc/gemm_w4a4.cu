@@ -256,7 +256,6 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
   const ItemSpace sp{a.run_fc1 ? n_tiles * a.ph[0].m_tiles : 0, a.fused ? n_tiles : 0,
                      a.run_fc2 ? n_tiles * a.ph[1].m_tiles : 0, a.ph[0].m_tiles,
                      a.ph[1].m_tiles};
-  const int n_items = sp.n1 + sp.nr + sp.n2;
 
   // ---- geometry from the largest token tile (<= 128 rows) of this launch
   const int max_n16 = (a.status[kStatusMaxRows] + 15) & ~15;
