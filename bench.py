@@ -32,7 +32,6 @@ import nvfp4_token_routed_gb300 as M  # noqa: E402
 from nvfp4_token_routed_gb300 import workloads as W  # noqa: E402
 
 METRIC = "MoE-layer tokens/s and µs/layer at 1 GB300"
-KERNELS_PER_STEP = 9  # quantize, route count/scan/scatter/gather, FC1, requant, FC2, finalize
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -481,8 +480,10 @@ def run_ours(args, rank, world, local_rank):
                                "over a second pass of the same K steps"},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": (KERNELS_PER_STEP - (2 if args.w4a16 else 0) + (1 if args.with_router else 0))
-                        * args.steps,
+        # the forward's own count (moe_nvfp4_forward_kernel_count) plus the token
+        # quantization (W4A4) and the router, when the step runs them
+        "gpu_launches": (M.moe_nvfp4_forward_kernel_count(w.dims, T, K, args.w4a16)
+                         + (0 if args.w4a16 else 1) + (1 if args.with_router else 0)) * args.steps,
         "clocks": clocks,
         "wall_s": t_wall,
     }

@@ -75,6 +75,8 @@ def lib():
         L.moe_nvfp4_quantize_tokens.argtypes = [i32, i32, vp, vp, vp, vp, vp]
         L.moe_nvfp4_workspace_bytes.restype = sz
         L.moe_nvfp4_workspace_bytes.argtypes = [C.POINTER(moe_dims), i32, i32, i32]
+        L.moe_nvfp4_forward_kernel_count.restype = i32
+        L.moe_nvfp4_forward_kernel_count.argtypes = [C.POINTER(moe_dims), i32, i32, i32]
         L.moe_nvfp4_workspace_layout.argtypes = [C.POINTER(moe_dims), i32, i32, i32,
                                                  C.POINTER(moe_ws_layout)]
         L.moe_nvfp4_forward.argtypes = [C.POINTER(moe_dims), C.POINTER(moe_nvfp4_weights), i32,
@@ -218,6 +220,10 @@ def moe_nvfp4_route_topk(logits, topk_ids, topk_w, stream=None):
 
 def moe_nvfp4_workspace_bytes(d, T_max, K, w4a16=False):
     return int(lib().moe_nvfp4_workspace_bytes(C.byref(d), T_max, K, int(bool(w4a16))))
+
+
+def moe_nvfp4_forward_kernel_count(d, T, K, w4a16=False):
+    return int(lib().moe_nvfp4_forward_kernel_count(C.byref(d), T, K, int(bool(w4a16))))
 
 
 def moe_nvfp4_workspace_layout(d, T, K, w4a16=False):

@@ -236,6 +236,10 @@ T* at(void* ws, size_t off) {
 
 }  // namespace
 
+namespace moe {
+int route_kernel_launches(int64_t TK);  // defined next to the routing kernels
+}  // namespace moe
+
 extern "C" {
 
 int32_t moe_nvfp4_abi_version(void) { return MOE_NVFP4_ABI_VERSION; }
@@ -332,6 +336,15 @@ moe_status moe_nvfp4_quantize_tokens_static(int32_t T, int32_t H, const void* x_
                                             moe_stream_t stream) {
   if (T > 0 && !a1_scale) return MOE_ERR_INVALID_ARG;
   return quantize_impl(T, H, x_bf16, codes, sf, nullptr, a1_scale, stream);
+}
+
+int32_t moe_nvfp4_forward_kernel_count(const moe_dims* d, int32_t T, int32_t K, int32_t w4a16) {
+  if (check_dims(d) != MOE_OK || check_tk(d, T, K) != MOE_OK) return -1;
+  if (T == 0) return 0;
+  const int64_t TK = (int64_t)T * K;
+  const bool fused = !w4a16 && TK <= kFusedMaxRoutes && TK <= kFusedRoutesPerExpert * d->E;
+  const int gemms = w4a16 ? 2 : fused ? 1 : 3;  // W4A4 three: FC1, requant, FC2
+  return route_kernel_launches(TK) + 1 + gemms + 1;  // routing, gather, GEMMs, finalize
 }
 
 size_t moe_nvfp4_workspace_bytes(const moe_dims* d, int32_t T_max, int32_t K, int32_t w4a16) {

@@ -464,6 +464,9 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(
   }
 }
 
+// Kernels launch_route issues for TK routes (before the gather).
+int route_kernel_launches(int64_t TK) { return TK <= kSmallRoutes ? 1 : 3; }
+
 void launch_route(const RouteArgs& a, cudaStream_t s) {
   if (a.TK <= kSmallRoutes) {
     const size_t smem = sizeof(int) * 34 * (size_t)a.E;  // hist, cursor, 32 warp rows
