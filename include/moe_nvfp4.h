@@ -167,8 +167,8 @@ size_t moe_nvfp4_workspace_bytes(const moe_dims* d, int32_t T_max, int32_t K, in
 
 /* Number of kernels one moe_nvfp4_forward (w4a16 = 0) or
  * moe_nvfp4_forward_w4a16 (w4a16 = 1) call launches for T tokens with top-K:
- * routing (one kernel up to 2048 routes, three beyond), the row gather, the
- * grouped GEMMs (W4A4: one launch when T*K <= min(2048, 8*E), else FC1, the
+ * routing and the row gather (one kernel up to 32 routes, two up to 2048,
+ * four beyond), the grouped GEMMs (W4A4: one launch when T*K <= min(2048, 8*E), else FC1, the
  * FC2-input requant and FC2; W4A16: FC1 and FC2) and the finalize; 0 for
  * T == 0.  Host only, no device work.  Returns -1 for invalid arguments. */
 int32_t moe_nvfp4_forward_kernel_count(const moe_dims* d, int32_t T, int32_t K, int32_t w4a16);

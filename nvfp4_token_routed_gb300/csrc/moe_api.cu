@@ -237,7 +237,7 @@ T* at(void* ws, size_t off) {
 }  // namespace
 
 namespace moe {
-int route_kernel_launches(int64_t TK);  // defined next to the routing kernels
+int route_kernel_launches(int64_t TK);  // routing + gather launches; next to those kernels
 }  // namespace moe
 
 extern "C" {
@@ -344,7 +344,7 @@ int32_t moe_nvfp4_forward_kernel_count(const moe_dims* d, int32_t T, int32_t K, 
   const int64_t TK = (int64_t)T * K;
   const bool fused = !w4a16 && TK <= kFusedMaxRoutes && TK <= kFusedRoutesPerExpert * d->E;
   const int gemms = w4a16 ? 2 : fused ? 1 : 3;  // W4A4 three: FC1, requant, FC2
-  return route_kernel_launches(TK) + 1 + gemms + 1;  // routing, gather, GEMMs, finalize
+  return route_kernel_launches(TK) + gemms + 1;  // routing and gather, GEMMs, finalize
 }
 
 size_t moe_nvfp4_workspace_bytes(const moe_dims* d, int32_t T_max, int32_t K, int32_t w4a16) {

@@ -328,18 +328,55 @@ __global__ void __launch_bounds__(kChunk) route_scatter_kernel(
   if (idx < TK) inv[idx] = p;
 }
 
+// Row gather of one route (one warp): the token's quantized row and its block
+// scales (W4A4; rows already padded to Hp by the quantizer) or its bf16 row
+// with the Hp - H padding columns zeroed (W4A16) into permuted row p.
+struct GatherArgs {
+  int K, H, Hp;
+  const uint8_t* xc;
+  const uint8_t* xsf;
+  const float* xs;
+  uint8_t* pc;
+  uint8_t* psf;
+  float* ps;
+  const uint4* xb;
+  uint4* pb;
+};
+template <bool kW4A16>
+__device__ __forceinline__ void gather_route_row(const GatherArgs& g, int idx, int p, int lane) {
+  const int t = idx / g.K;
+  if constexpr (kW4A16) {
+    const uint4* src = g.xb + (size_t)t * (g.H / 8);
+    uint4* dst = g.pb + (size_t)p * (g.Hp / 8);
+    for (int i = lane; i < g.H / 8; i += 32) dst[i] = __ldg(src + i);
+    for (int i = g.H / 8 + lane; i < g.Hp / 8; i += 32) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+  } else {
+    const uint4* src = reinterpret_cast<const uint4*>(g.xc + (size_t)t * (g.Hp / 2));
+    uint4* dst = reinterpret_cast<uint4*>(g.pc + (size_t)p * (g.Hp / 2));
+    for (int i = lane; i < g.Hp / 32; i += 32) dst[i] = __ldg(src + i);
+    const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(g.xsf + (size_t)t * (g.Hp / 16));
+    const uint32_t c16 = (uint32_t)(g.Hp / 16);
+    for (int j = lane; j < g.Hp / 64; j += 32)
+      *reinterpret_cast<uint32_t*>(g.psf + sf_offset(p, 4 * j, c16)) = __ldg(ssrc + j);
+    if (lane == 0) g.ps[p] = g.xs ? g.xs[t] : 1.0f;  // per-tensor tokens carry no row scale
+  }
+}
+
 // Small batches (TK <= kSmallRoutes): count, scan and scatter in one block of
 // 1024 threads, saving two launches.  Same outputs as the three kernels: the
 // histogram and the tile table as the scan writes them, then the stable
 // scatter in 1024-route chunks (earlier warps of the chunk, then the lane's
 // rank among earlier lanes with the same expert, on top of a running
 // per-expert cursor).  Dynamic shared memory: hist[E], cursor[E], wcnt[32][E].
+// Up to kInlineGatherRoutes routes it also gathers the rows (one warp per
+// route), saving the gather launch.
 constexpr int kSmallRoutes = 2048;  // measured: one block is slower than three kernels at 4096
+constexpr int kInlineGatherRoutes = 32;
 __global__ void __launch_bounds__(1024) route_small_kernel(
     const int32_t* __restrict__ ids, int ids64, int TK, int E, int32_t* __restrict__ counts,
     int32_t* __restrict__ group_row0, int4* __restrict__ tiles, int32_t* __restrict__ status,
     int32_t* __restrict__ tile_sync, int tile_sync_words, int32_t* __restrict__ inv,
-    int32_t* __restrict__ perm) {
+    int32_t* __restrict__ perm, const GatherArgs ga, int gather, int w4a16) {
   extern __shared__ int s_small[];
   int* hist = s_small;
   int* cursor = s_small + E;
@@ -428,17 +465,24 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
     }
     __syncthreads();  // the next chunk clears wcnt only after every thread has read it
   }
+  // (4) tiny batches: the row gather too, warp w copying route w's row
+  if (gather && wid < TK) {
+    const int p = inv[wid];
+    if (p >= 0) {
+      if (w4a16)
+        gather_route_row<true>(ga, wid, p, lane);
+      else
+        gather_route_row<false>(ga, wid, p, lane);
+    }
+  }
 }
 
 // Gather: one warp per route copies its token's row to the route's permuted row.
 // W4A4 rows are already padded to Hp by the quantizer; W4A16 copies H bf16
 // values and zero-fills the Hp - H padding columns.
 template <bool kW4A16>
-__global__ void __launch_bounds__(256) gather_rows_kernel(
-    int TK, int K, int H, int Hp, const int32_t* __restrict__ inv, const uint8_t* __restrict__ xc,
-    const uint8_t* __restrict__ xsf, const float* __restrict__ xs, uint8_t* __restrict__ pc,
-    uint8_t* __restrict__ psf, float* __restrict__ ps, const uint4* __restrict__ xb,
-    uint4* __restrict__ pb) {
+__global__ void __launch_bounds__(256) gather_rows_kernel(int TK, const int32_t* __restrict__ inv,
+                                                          const GatherArgs g) {
   pdl_wait();
   pdl_trigger();
   const int idx = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -446,26 +490,18 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(
   if (idx >= TK) return;
   const int p = inv[idx];
   if (p < 0) return;
-  const int t = idx / K;
-  if constexpr (kW4A16) {
-    const uint4* src = xb + (size_t)t * (H / 8);
-    uint4* dst = pb + (size_t)p * (Hp / 8);
-    for (int i = lane; i < H / 8; i += 32) dst[i] = __ldg(src + i);
-    for (int i = H / 8 + lane; i < Hp / 8; i += 32) dst[i] = make_uint4(0u, 0u, 0u, 0u);
-  } else {
-    const uint4* src = reinterpret_cast<const uint4*>(xc + (size_t)t * (Hp / 2));
-    uint4* dst = reinterpret_cast<uint4*>(pc + (size_t)p * (Hp / 2));
-    for (int i = lane; i < Hp / 32; i += 32) dst[i] = __ldg(src + i);
-    const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(xsf + (size_t)t * (Hp / 16));
-    const uint32_t c16 = (uint32_t)(Hp / 16);
-    for (int g = lane; g < Hp / 64; g += 32)
-      *reinterpret_cast<uint32_t*>(psf + sf_offset(p, 4 * g, c16)) = __ldg(ssrc + g);
-    if (lane == 0) ps[p] = xs ? xs[t] : 1.0f;  // per-tensor tokens carry no row scale
-  }
+  gather_route_row<kW4A16>(g, idx, p, lane);
 }
 
-// Kernels launch_route issues for TK routes (before the gather).
-int route_kernel_launches(int64_t TK) { return TK <= kSmallRoutes ? 1 : 3; }
+// Kernels launch_route issues for TK routes: routing and the row gather.
+int route_kernel_launches(int64_t TK) {
+  return TK <= kInlineGatherRoutes ? 1 : TK <= kSmallRoutes ? 2 : 4;
+}
+
+static GatherArgs gather_args(const RouteArgs& a) {
+  return GatherArgs{a.K,  a.H,  a.Hp, a.xc, a.xsf, a.xs, a.pc, a.psf, a.ps,
+                    static_cast<const uint4*>(a.xb), static_cast<uint4*>(a.pb)};
+}
 
 void launch_route(const RouteArgs& a, cudaStream_t s) {
   if (a.TK <= kSmallRoutes) {
@@ -478,7 +514,8 @@ void launch_route(const RouteArgs& a, cudaStream_t s) {
     }
     launch_pdl(route_small_kernel, dim3(1), dim3(1024), smem, s, a.ids, a.ids64, a.TK, a.E,
                a.counts, a.group_row0, a.tiles, a.status, a.tile_sync, a.tile_sync_words, a.inv,
-               a.perm);
+               a.perm, gather_args(a), a.TK <= kInlineGatherRoutes ? 1 : 0, a.w4a16);
+    if (a.TK <= kInlineGatherRoutes) return;  // rows gathered by the same block
   } else {
     const int nchunks = (a.TK + kChunk - 1) / kChunk;
     launch_pdl(route_count_kernel, dim3(nchunks), dim3(kChunk), sizeof(int) * a.E, s, a.ids,
@@ -492,14 +529,11 @@ void launch_route(const RouteArgs& a, cudaStream_t s) {
   }
   const int gblocks = (a.TK + 7) / 8;
   if (a.w4a16)
-    launch_pdl(gather_rows_kernel<true>, dim3(gblocks), dim3(256), 0, s, a.TK, a.K, a.H, a.Hp,
-               (const int32_t*)a.inv, (const uint8_t*)nullptr, (const uint8_t*)nullptr,
-               (const float*)nullptr, (uint8_t*)nullptr, (uint8_t*)nullptr, (float*)nullptr,
-               static_cast<const uint4*>(a.xb), static_cast<uint4*>(a.pb));
+    launch_pdl(gather_rows_kernel<true>, dim3(gblocks), dim3(256), 0, s, a.TK,
+               (const int32_t*)a.inv, gather_args(a));
   else
-    launch_pdl(gather_rows_kernel<false>, dim3(gblocks), dim3(256), 0, s, a.TK, a.K, a.H, a.Hp,
-               (const int32_t*)a.inv, a.xc, a.xsf, a.xs, a.pc, a.psf, a.ps,
-               (const uint4*)nullptr, (uint4*)nullptr);
+    launch_pdl(gather_rows_kernel<false>, dim3(gblocks), dim3(256), 0, s, a.TK,
+               (const int32_t*)a.inv, gather_args(a));
 }
 
 // ============================================================== FC2-input requant

@@ -173,18 +173,20 @@ def test_binding_rejects_cpu_tensors():
 
 
 def test_forward_kernel_count(lib):
-    """Launches of one forward call: routing (one kernel up to 2048 routes,
-    three beyond), gather, GEMMs (W4A4: one launch when T*K <= min(2048, 8E),
-    else FC1, requant, FC2; W4A16: FC1, FC2), finalize."""
+    """Launches of one forward call: routing and gather (one kernel up to 32
+    routes, two up to 2048, four beyond), GEMMs (W4A4: one launch when
+    T*K <= min(2048, 8E), else FC1, requant, FC2; W4A16: FC1, FC2), finalize."""
     e64 = M.dims(64, 2048, 1024, "swiglu")
     e256 = M.dims(256, 7168, 2048, "relu2")
     count = M.moe_nvfp4_forward_kernel_count
-    assert count(e64, 128, 8) == 1 + 1 + 3 + 1          # 1024 routes > 8 per expert
-    assert count(e64, 128, 8, True) == 1 + 1 + 2 + 1
-    assert count(e64, 64, 8) == 1 + 1 + 1 + 1           # 512 routes = 8 per expert: one launch
-    assert count(e256, 1, 8) == 1 + 1 + 1 + 1
-    assert count(e256, 256, 8) == 1 + 1 + 1 + 1         # 2048 routes
-    assert count(e256, 257, 8) == 3 + 1 + 3 + 1         # 2056 routes: three routing kernels
-    assert count(e256, 4096, 8, True) == 3 + 1 + 2 + 1
+    assert count(e64, 128, 8) == 2 + 3 + 1              # 1024 routes > 8 per expert
+    assert count(e64, 128, 8, True) == 2 + 2 + 1
+    assert count(e64, 64, 8) == 2 + 1 + 1               # 512 routes = 8 per expert: one launch
+    assert count(e256, 1, 8) == 1 + 1 + 1               # 8 routes: rows gathered by the routing block
+    assert count(e256, 4, 8) == 1 + 1 + 1               # 32 routes
+    assert count(e256, 5, 8) == 2 + 1 + 1               # 40 routes: separate gather
+    assert count(e256, 256, 8) == 2 + 1 + 1             # 2048 routes
+    assert count(e256, 257, 8) == 4 + 3 + 1             # 2056 routes: three routing kernels
+    assert count(e256, 4096, 8, True) == 4 + 2 + 1
     assert count(e256, 0, 8) == 0
     assert count(e256, 4, 0) == -1 and count(e256, 4, 33) == -1 and count(e256, -1, 8) == -1
