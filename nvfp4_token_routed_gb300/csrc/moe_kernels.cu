@@ -481,7 +481,7 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
 // W4A4 rows are already padded to Hp by the quantizer; W4A16 copies H bf16
 // values and zero-fills the Hp - H padding columns.
 template <bool kW4A16>
-__global__ void __launch_bounds__(256) gather_rows_kernel(int TK, const int32_t* __restrict__ inv,
+__global__ void __launch_bounds__(128) gather_rows_kernel(int TK, const int32_t* __restrict__ inv,
                                                           const GatherArgs g) {
   pdl_wait();
   pdl_trigger();
@@ -527,12 +527,14 @@ void launch_route(const RouteArgs& a, cudaStream_t s) {
     launch_pdl(route_scatter_kernel, dim3(nchunks), dim3(kChunk), smem, s, a.ids, a.ids64, a.TK,
                a.E, (const int32_t*)a.chunk_prefix, (const int32_t*)a.group_row0, a.inv, a.perm);
   }
-  const int gblocks = (a.TK + 7) / 8;
+  // 4-warp blocks: small enough in registers to share an SM with a GEMM CTA,
+  // which can then start (programmatic launch) before the gather is done
+  const int gblocks = (a.TK + 3) / 4;
   if (a.w4a16)
-    launch_pdl(gather_rows_kernel<true>, dim3(gblocks), dim3(256), 0, s, a.TK,
+    launch_pdl(gather_rows_kernel<true>, dim3(gblocks), dim3(128), 0, s, a.TK,
                (const int32_t*)a.inv, gather_args(a));
   else
-    launch_pdl(gather_rows_kernel<false>, dim3(gblocks), dim3(256), 0, s, a.TK,
+    launch_pdl(gather_rows_kernel<false>, dim3(gblocks), dim3(128), 0, s, a.TK,
                (const int32_t*)a.inv, gather_args(a));
 }
 
