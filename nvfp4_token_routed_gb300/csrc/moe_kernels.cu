@@ -562,7 +562,11 @@ __global__ void __launch_bounds__(256) requant_kernel(int TK, int I, const int32
 
 void launch_requant(int TK, int I, const int32_t* inv, const float* act, uint8_t* qc, uint8_t* qsf,
                     float* qs, const float* static_enc, cudaStream_t s) {
-  const int warps = 8;
+  // Large batches: 2-warp blocks (91 registers a thread), small enough to share
+  // an SM with a GEMM CTA, so FC2 can start (programmatic launch) before the
+  // long pass is done (ReLU2 H7168 E256 T=4096: -11 us); small batches keep
+  // 8-warp blocks (the many tiny blocks cost more than they overlap there).
+  const int warps = TK > kSmallRoutes ? 2 : 8;
   launch_pdl(requant_kernel, dim3((TK + warps - 1) / warps), dim3(warps * 32), 0, s, TK, I, inv,
              act, qc, qsf, qs, static_enc);
 }
