@@ -155,9 +155,8 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
   // A token stage is one 3-D box: kChunks 64-K chunks of box_rows(n16) rows
   // each, chunk-major, so chunk c of a tile starts c x box_rows x 128 bytes in.
   const int stage_bytes = kChunks * box_rows(max_n16) * kChunkRowBytes;  // multiple of 1024
-  // Each item accumulates into two partial sums (even and odd K steps, so
-  // consecutive MMAs do not wait on one another), added in a fixed order in the
-  // epilogue.  The split never depends on the batch, so results stay bitwise
+  // Each item accumulates into two partial sums (even and odd K steps, each
+  // issued by its own warp), added in a fixed order in the epilogue.  The split never depends on the batch, so results stay bitwise
   // batch invariant.  nbuf items are in flight (one when tiles exceed 64 tokens).
   const int acc_cols = (max_n16 + 31) & ~31;
   const int nacc = kIssuers;
