@@ -307,6 +307,7 @@ int64_t orc_sf_swizzle_offset(int64_t r, int64_t j, int64_t ncols16) {
  * This equals softmax over all experts renormalised over the selected K. */
 void orc_route_topk(int64_t T, int64_t E, int64_t K, const float* logits, int32_t* ids,
                     float* w) {
+    if (K < 1 || K > E) return; /* no K distinct experts to select */
     for (int64_t t = 0; t < T; ++t) {
         const float* l = logits + t * E;
         unsigned char* taken = (unsigned char*)calloc((size_t)E, 1);
@@ -319,7 +320,7 @@ void orc_route_topk(int64_t T, int64_t E, int64_t K, const float* logits, int32_
             taken[best] = 1;
             ids[t * K + k] = (int32_t)best;
         }
-        double ex[64];
+        double* ex = (double*)malloc(sizeof(double) * (size_t)K);
         double m = (double)l[ids[t * K]];
         double sum = 0.0;
         for (int64_t k = 0; k < K; ++k) {
@@ -327,6 +328,7 @@ void orc_route_topk(int64_t T, int64_t E, int64_t K, const float* logits, int32_
             sum += ex[k];
         }
         for (int64_t k = 0; k < K; ++k) w[t * K + k] = (float)(ex[k] / sum);
+        free(ex);
         free(taken);
     }
 }

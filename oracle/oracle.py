@@ -196,6 +196,8 @@ def route_topk(logits, K):
     id) and fp32 softmax scores over the selected logits."""
     lg = np.ascontiguousarray(logits, dtype=np.float32)
     T, E = lg.shape
+    if not 1 <= K <= E:
+        raise ValueError(f"top-K router needs 1 <= K <= E, got K={K}, E={E}")
     ids = np.empty((T, K), np.int32)
     w = np.empty((T, K), np.float32)
     lib().orc_route_topk(C.c_int64(T), C.c_int64(E), C.c_int64(K), _p(lg), _p(ids), _p(w))

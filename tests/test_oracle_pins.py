@@ -273,6 +273,63 @@ def test_sanity_against_unquantized_fp64_moe(act):
     assert cos16.min() > cos.min() - 1e-3 and cos16.mean() > 0.98
 
 
+def _f32_alpha(w_bf16_expert):
+    """alpha = 1 / w_scale with w_scale = 2688 / amax, each one binary32 operation,
+    written here with numpy scalars (How to extend: alpha = 1 / w_scale)."""
+    amax = np.float32(np.abs(w_bf16_expert.float().numpy()).max())
+    return np.float32(np.float32(1.0) / np.float32(np.float32(2688.0) / amax))
+
+
+def _bf16_of(a):
+    """Nearest bf16 of fp64 values, through torch's float32 -> bfloat16 conversion."""
+    t = torch.from_numpy(np.asarray(a, np.float64).astype(np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _mismatches_within_one_ulp(got_u16, want_u16):
+    """Count of differing bf16 elements; fails if any differs by more than one ulp."""
+    g = got_u16.astype(np.int64)
+    w = want_u16.astype(np.int64)
+    sg = np.where(g & 0x8000, -(g & 0x7FFF), g & 0x7FFF)
+    sw = np.where(w & 0x8000, -(w & 0x7FFF), w & 0x7FFF)
+    assert np.abs(sg - sw).max(initial=0) <= 1
+    return int((g != w).sum())
+
+
+@pytest.mark.parametrize("act", ["relu2", "swiglu"])
+def test_w4a16_expert_matches_a_direct_dequantized_matmul(act):
+    """W4A16 compute order (Tensor and numerical contract): FC1 over the bf16 token
+    row with weights decoded from the oracle's codes and scales, times alpha1;
+    activation; a bf16 handoff; FC2 over the handoff times alpha2; bf16 route
+    rows.  Computed here with numpy from the bf16 weights' own amax, so a dropped
+    or doubled alpha1 / alpha2, or an FC2 fed with the unrounded activation,
+    moves hundreds of elements."""
+    wl, x, w1, w2, ids, wts = _tiny(act, I=256 if act == "swiglu" else 512)
+    Wt = O.Weights(W.bf16_bits(w1), W.bf16_bits(w2))
+    res = O.forward_w4a16(Wt, W.bf16_bits(x), ids, wts, wl.E, wl.H, wl.I, act)
+    xf = x.float().numpy().astype(np.float64)          # bf16 values, exact
+    act_miss = route_miss = n_act = n_route = 0
+    for q in range(res["R"]):
+        r = int(res["perm"][q]); t, e = r // wl.K, int(ids[r // wl.K, r % wl.K])
+        a1, a2 = _f32_alpha(w1[e]), _f32_alpha(w2[e])
+        assert a1 == Wt.a1[e] and a2 == Wt.a2[e]
+        y = (O.dequant(Wt.w1c[e], Wt.w1sf[e]) @ xf[t]) * np.float64(a1)
+        if act == "relu2":
+            a = np.maximum(y, 0) ** 2
+        else:
+            g, u = y[: wl.I], y[wl.I:]
+            a = g / (1 + np.exp(-g)) * u
+        a_h = _bf16_of(a)                                  # the handoff
+        act_miss += _mismatches_within_one_ulp(res["act"][q], a_h)
+        n_act += a_h.size
+        z = (O.dequant(Wt.w2c[e], Wt.w2sf[e]) @ O.bf16_to_f32(a_h).astype(np.float64))
+        route = _bf16_of(z * np.float64(a2))
+        route_miss += _mismatches_within_one_ulp(res["route"][q], route)
+        n_route += route.size
+    # only values within rounding-order noise of a bf16 midpoint may round apart
+    assert act_miss <= 2 and route_miss <= 2, (act_miss, n_act, route_miss, n_route)
+
+
 def test_swiglu_gate_up_split():
     """up rows zero -> output 0; gate rows zero -> output 0; swapping the halves
     changes the output (canonical FC1 = [gate; up], Tensor and numerical contract)."""
