@@ -376,6 +376,19 @@ static inline double dq(const uint8_t* codes, const uint8_t* sf, int64_t i) {
     return orc_e2m1_decode(code) * orc_e4m3_decode(sf[i >> 4]);
 }
 
+/* A whole decoded row (D elements); the dot products below read decoded values
+ * from such rows, so each element is decoded once per row instead of once per
+ * product (the same values, multiplied and summed in the same order). */
+static void dq_row(const uint8_t* codes, const uint8_t* sf, int64_t D, double* out) {
+    for (int64_t b = 0; b < D / 16; ++b) {
+        const double scale = orc_e4m3_decode(sf[b]); /* one block scale per 16 elements */
+        for (int64_t i = 16 * b; i < 16 * b + 16; ++i) {
+            uint8_t byte = codes[i >> 1];
+            out[i] = orc_e2m1_decode((i & 1) ? (byte >> 4) : (byte & 15)) * scale;
+        }
+    }
+}
+
 static double silu(double g) { return g / (1.0 + exp(-g)); }
 
 /* Activation of one FC1 output row in fp64 (R8).  y has N1 entries (I for
@@ -418,12 +431,15 @@ static void expert_w4a4(const orc_dims* d, int64_t e, const uint8_t* w1c, const 
     int64_t H = d->H, I = d->I, N1 = d->act ? 2 * I : I;
     double* y = (double*)malloc(sizeof(double) * (size_t)N1);
     double* a = (double*)malloc(sizeof(double) * (size_t)I);
+    double* xd = (double*)malloc(sizeof(double) * (size_t)(H > I ? H : I));
+    double* wd = (double*)malloc(sizeof(double) * (size_t)(H > I ? H : I));
     const uint8_t* c1 = w1c + e * N1 * (H / 2);
     const uint8_t* s1 = w1sf + e * N1 * (H / 16);
+    dq_row(xc, xsf, H, xd);
     for (int64_t n = 0; n < N1; ++n) {
+        dq_row(c1 + n * (H / 2), s1 + n * (H / 16), H, wd);
         double acc = 0.0;
-        for (int64_t h = 0; h < H; ++h)
-            acc += dq(c1 + n * (H / 2), s1 + n * (H / 16), h) * dq(xc, xsf, h);
+        for (int64_t h = 0; h < H; ++h) acc += wd[h] * xd[h];
         y[n] = acc * (double)a1[e] * (double)xs;
     }
     activation(d->act, d->limit, I, y, a);
@@ -438,14 +454,17 @@ static void expert_w4a4(const orc_dims* d, int64_t e, const uint8_t* w1c, const 
     *s2_out = s2;
     const uint8_t* c2 = w2c + e * H * (I / 2);
     const uint8_t* sc2 = w2sf + e * H * (I / 16);
+    dq_row(fc2c, fc2sf, I, xd);
     for (int64_t h = 0; h < H; ++h) {
+        dq_row(c2 + h * (I / 2), sc2 + h * (I / 16), I, wd);
         double acc = 0.0;
-        for (int64_t n = 0; n < I; ++n)
-            acc += dq(c2 + h * (I / 2), sc2 + h * (I / 16), n) * dq(fc2c, fc2sf, n);
+        for (int64_t n = 0; n < I; ++n) acc += wd[n] * xd[n];
         route_out[h] = orc_f64_to_bf16(acc * (double)a2[e] * (double)s2);
     }
     free(y);
     free(a);
+    free(xd);
+    free(wd);
 }
 
 /* One route of the W4A16 expert (R7; Tensor and numerical contract: compute
@@ -456,12 +475,13 @@ static void expert_w4a16(const orc_dims* d, int64_t e, const uint8_t* w1c, const
     int64_t H = d->H, I = d->I, N1 = d->act ? 2 * I : I;
     double* y = (double*)malloc(sizeof(double) * (size_t)N1);
     double* a = (double*)malloc(sizeof(double) * (size_t)I);
+    double* wd = (double*)malloc(sizeof(double) * (size_t)(H > I ? H : I));
     const uint8_t* c1 = w1c + e * N1 * (H / 2);
     const uint8_t* s1 = w1sf + e * N1 * (H / 16);
     for (int64_t n = 0; n < N1; ++n) {
+        dq_row(c1 + n * (H / 2), s1 + n * (H / 16), H, wd);
         double acc = 0.0;
-        for (int64_t h = 0; h < H; ++h)
-            acc += dq(c1 + n * (H / 2), s1 + n * (H / 16), h) * (double)bf16_to_f32(x[h]);
+        for (int64_t h = 0; h < H; ++h) acc += wd[h] * (double)bf16_to_f32(x[h]);
         y[n] = acc * (double)a1[e];
     }
     activation(d->act, d->limit, I, y, a);
@@ -469,13 +489,14 @@ static void expert_w4a16(const orc_dims* d, int64_t e, const uint8_t* w1c, const
     const uint8_t* c2 = w2c + e * H * (I / 2);
     const uint8_t* sc2 = w2sf + e * H * (I / 16);
     for (int64_t h = 0; h < H; ++h) {
+        dq_row(c2 + h * (I / 2), sc2 + h * (I / 16), I, wd);
         double acc = 0.0;
-        for (int64_t n = 0; n < I; ++n)
-            acc += dq(c2 + h * (I / 2), sc2 + h * (I / 16), n) * (double)bf16_to_f32(act_out[n]);
+        for (int64_t n = 0; n < I; ++n) acc += wd[n] * (double)bf16_to_f32(act_out[n]);
         route_out[h] = orc_f64_to_bf16(acc * (double)a2[e]);
     }
     free(y);
     free(a);
+    free(wd);
 }
 
 /* Deterministic two-stage finalize (stage 6; What is added: "reduces each
