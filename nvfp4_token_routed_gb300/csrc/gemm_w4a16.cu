@@ -511,14 +511,10 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
 template <int MODE>
 static cudaError_t launch_w4a16_mode(const CUtensorMap& tmA, const TokenMaps& tmB,
                                      const GemmArgs& a, int grid, cudaStream_t s) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t err = cudaFuncSetAttribute(gemm_w4a16_kernel<MODE>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           w4a16::kSmemBytes);
-    if (err != cudaSuccess) return err;
-    configured = true;
-  }
+  static std::atomic<uint64_t> configured{0};  // per device
+  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(gemm_w4a16_kernel<MODE>),
+                                      w4a16::kSmemBytes, configured);
+  if (err != cudaSuccess) return err;
   return launch_pdl(gemm_w4a16_kernel<MODE>, dim3(grid), dim3(w4a16::kThreads),
                     (size_t)w4a16::kSmemBytes, s, tmA, tmB, a);
 }

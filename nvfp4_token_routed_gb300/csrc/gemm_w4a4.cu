@@ -718,14 +718,10 @@ cudaError_t launch_selftest_wait(const int32_t* never_set, int32_t* status, cuda
 
 template <int ACT>
 static cudaError_t launch_act(const W4A4Maps& maps, const W4A4Args& a, int grid, cudaStream_t s) {
-  static bool configured = false;  // the attribute is per function
-  if (!configured) {
-    cudaError_t err = cudaFuncSetAttribute(gemm_w4a4_kernel<ACT>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           w4a4::kSmemBytes);
-    if (err != cudaSuccess) return err;
-    configured = true;
-  }
+  static std::atomic<uint64_t> configured{0};  // per device
+  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(gemm_w4a4_kernel<ACT>),
+                                      w4a4::kSmemBytes, configured);
+  if (err != cudaSuccess) return err;
   return launch_pdl(gemm_w4a4_kernel<ACT>, dim3(grid), dim3(w4a4::kThreads),
                     (size_t)w4a4::kSmemBytes, s, maps, a);
 }

@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <utility>
@@ -100,6 +101,23 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current device,
+// once per device: the attribute belongs to the function on each device, so a
+// process that uses several devices sets it on each.  `done` holds one bit per
+// device (devices 0-63) and is only set after the call succeeded; two threads
+// racing on the first launch both make the (idempotent) call.
+inline cudaError_t ensure_smem_limit(const void* fn, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const uint64_t bit = uint64_t(1) << dev;
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
 // static_enc: null for the per-token recipe, else the device encode scale a1 of
 // the per-tensor recipe (scale is then not written).
 void launch_quantize_tokens(int T, int H, int Hp, const void* x, uint8_t* codes, uint8_t* sf,
@@ -108,7 +126,7 @@ void launch_quantize_tokens(int T, int H, int Hp, const void* x, uint8_t* codes,
 void launch_prepare_fc(int E, int N, int D, int Np, int Dp, int swiglu_I, const void* w,
                        uint8_t* codes, uint8_t* sf, float* alpha, const float* a_scale,
                        cudaStream_t s);
-void launch_route(const RouteArgs& a, cudaStream_t s);
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 void launch_route_topk(int T, int E, int K, const float* logits, int32_t* ids, float* w,
                        cudaStream_t s);
 void launch_requant(int TK, int I, const int32_t* inv, const float* act, uint8_t* qc, uint8_t* qsf,

@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 #include <nvtx3/nvToolsExt.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -21,7 +22,9 @@ namespace {
 constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
-  int checked = 0;  // 0 unknown, 1 ok, -1 unsupported
+  // 0 unknown, 1 ok, -1 unsupported; published with release after `sms` is set,
+  // so a thread that reads it with acquire also sees `sms`
+  std::atomic<int> checked{0};
   int sms = 0;
 };
 DeviceInfo g_dev[kMaxDevices];
@@ -31,19 +34,22 @@ moe_status check_device(int* sms_out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
   DeviceInfo& di = g_dev[dev];
-  if (di.checked == 0) {
+  int state = di.checked.load(std::memory_order_acquire);
+  if (state == 0) {
     std::lock_guard<std::mutex> lock(g_mu);
-    if (di.checked == 0) {
+    state = di.checked.load(std::memory_order_acquire);
+    if (state == 0) {
       int major = 0, minor = 0, sms = 0;
       if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
           cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
           cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return MOE_ERR_CUDA;
       di.sms = sms;
-      di.checked = (major == 10 && minor == 3) ? 1 : -1;
+      state = (major == 10 && minor == 3) ? 1 : -1;
+      di.checked.store(state, std::memory_order_release);
     }
   }
-  if (di.checked < 0) return MOE_ERR_UNSUPPORTED_DEVICE;
+  if (state < 0) return MOE_ERR_UNSUPPORTED_DEVICE;
   if (sms_out) *sms_out = di.sms;
   return MOE_OK;
 }
@@ -119,16 +125,19 @@ void compute_layout(const moe_dims* d, int32_t T, int32_t K, int32_t w4a16, moe_
 }
 
 // ---------------------------------------------------------------- tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 lookup_encode_fn() {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                       &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  return nullptr;
+}
+// looked up once per process (a function-local static is initialised once,
+// thread-safely)
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = lookup_encode_fn();
   return fn;
 }
 
@@ -462,7 +471,7 @@ static moe_status forward_w4a4_impl(const moe_dims* d, const moe_nvfp4_weights* 
     r.tile_sync = at<int32_t>(ws, L.tile_sync);
     r.tile_sync_words = (int)(2 * tiles_cap + L.rows_cap);
   }
-  launch_route(r, s);
+  if (launch_route(r, s) != cudaSuccess) return MOE_ERR_CUDA;
   mark(1, s);
 
   W4A4Args g{};
@@ -572,7 +581,7 @@ static moe_status forward_w4a16_impl(const moe_dims* d, const moe_nvfp4_weights*
   RouteArgs r = route_args(d, T, K, topk_ids, o.ids_int64, ws, L, 1);
   r.xb = x_bf16;
   r.pb = at<uint8_t>(ws, L.x_perm);
-  launch_route(r, s);
+  if (launch_route(r, s) != cudaSuccess) return MOE_ERR_CUDA;
   mark(1, s);
 
   const int64_t tiles_cap = L.rows_cap / kTileRows;

@@ -503,19 +503,17 @@ static GatherArgs gather_args(const RouteArgs& a) {
                     static_cast<const uint4*>(a.xb), static_cast<uint4*>(a.pb)};
 }
 
-void launch_route(const RouteArgs& a, cudaStream_t s) {
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
   if (a.TK <= kSmallRoutes) {
     const size_t smem = sizeof(int) * 34 * (size_t)a.E;  // hist, cursor, 32 warp rows
-    static bool configured = false;
-    if (!configured) {
-      cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)(sizeof(int) * 34 * 1024));
-      configured = true;
-    }
+    static std::atomic<uint64_t> configured{0};  // per device
+    cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(route_small_kernel),
+                                        (int)(sizeof(int) * 34 * 1024), configured);
+    if (err != cudaSuccess) return err;
     launch_pdl(route_small_kernel, dim3(1), dim3(1024), smem, s, a.ids, a.ids64, a.TK, a.E,
                a.counts, a.group_row0, a.tiles, a.status, a.tile_sync, a.tile_sync_words, a.inv,
                a.perm, gather_args(a), a.TK <= kInlineGatherRoutes ? 1 : 0, a.w4a16);
-    if (a.TK <= kInlineGatherRoutes) return;  // rows gathered by the same block
+    if (a.TK <= kInlineGatherRoutes) return cudaGetLastError();  // rows gathered by the same block
   } else {
     const int nchunks = (a.TK + kChunk - 1) / kChunk;
     launch_pdl(route_count_kernel, dim3(nchunks), dim3(kChunk), sizeof(int) * a.E, s, a.ids,
@@ -536,6 +534,7 @@ void launch_route(const RouteArgs& a, cudaStream_t s) {
   else
     launch_pdl(gather_rows_kernel<false>, dim3(gblocks), dim3(128), 0, s, a.TK,
                (const int32_t*)a.inv, gather_args(a));
+  return cudaGetLastError();
 }
 
 // ============================================================== FC2-input requant
