@@ -312,6 +312,9 @@ moe_status moe_nvfp4_read_status(const void* ws, moe_stream_t stream);
  *     is rejected with MOE_ERR_WORKSPACE_TOO_SMALL before anything runs.
  *   - The first call on each device looks up the array's device address (with
  *     that device current); make that first call outside any stream capture.
+ *     The address is kept until the process exits: do not call cudaDeviceReset
+ *     on a device where this entry point has been used (the array would move).
+ *   - Shape errors are reported exactly as by moe_nvfp4_forward.
  *   - Nothing is allocated or freed, by the library or any routine it calls.
  *   - All calls on a device share the one array.  The forward clears the
  *     status words it needs zeroed; the rest is written before it is read, so

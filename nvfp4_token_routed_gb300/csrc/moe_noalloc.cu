@@ -32,7 +32,10 @@ void* g_scratch_ptr[kMaxDevices] = {};
 std::mutex g_scratch_mu;
 
 // Per-device set-up, run on the first call on each device with that device
-// current: look up the device address of the scratch array.
+// current: look up the device address of the scratch array.  The address is
+// kept for the life of the process; a cudaDeviceReset on that device makes it
+// stale (the array is re-created at a new address), so callers must not reset a
+// device on which they use this entry point.
 moe_status scratch_for_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
@@ -53,9 +56,12 @@ extern "C" moe_status moe_nvfp4_forward_noalloc(const moe_dims* d, const moe_nvf
                                                 const uint8_t* sf, const float* scale,
                                                 const int32_t* topk_ids, const float* topk_w,
                                                 void* out_bf16, moe_stream_t stream) {
-  const size_t need = moe_nvfp4_workspace_bytes(d, T, K, 0);
-  if (need == 0) return d ? MOE_ERR_UNSUPPORTED_SHAPE : MOE_ERR_INVALID_ARG;
-  if (need > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  // the shape checks of moe_nvfp4_forward first, so a bad shape gets the same
+  // status code here as there; then the size of the fixed scratch
+  moe_ws_layout L;
+  const moe_status shape = moe_nvfp4_workspace_layout(d, T, K, 0, &L);
+  if (shape != MOE_OK) return shape;
+  if (L.total > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;
   moe_status st = scratch_for_current_device(&scratch);
   if (st != MOE_OK) return st;

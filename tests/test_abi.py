@@ -154,6 +154,15 @@ def test_forward_validation_without_a_gpu(lib):
     rc = L.moe_nvfp4_forward_noalloc(C.byref(big), C.byref(wb.c), 4096, 8, vp(4096), vp(4096),
                                      vp(4096), vp(4096), vp(4096), vp(4096), None)
     assert rc == 4
+    # ... and reports a bad shape with the status moe_nvfp4_forward gives it
+    for T, K, want in ((4, 0, 1), (-1, 2, 1), (4, 33, 2)):
+        args = (C.byref(d), C.byref(w.c), T, K, vp(4096), vp(4096), vp(4096), vp(4096),
+                vp(4096), vp(4096))
+        assert L.moe_nvfp4_forward(*args, vp(4096), 1 << 30, None) == want
+        assert L.moe_nvfp4_forward_noalloc(*args, None) == want
+    bad_act = M.moe_dims(8, 256, 512, 7)
+    assert L.moe_nvfp4_forward_noalloc(C.byref(bad_act), C.byref(w.c), 4, 2, vp(4096), vp(4096),
+                                       vp(4096), vp(4096), vp(4096), vp(4096), None) == 1
 
 
 def test_profile_events_argument_checks(lib):
