@@ -7,6 +7,10 @@ deterministic finalize) over one batch of T synthetic tokens, replayed from a
 CUDA graph.  Inputs are resident in HBM; L2 is flushed (a 256 MB write)
 between timed steps, outside the per-step CUDA events.
 
+Default workload: the MoE layer of the pages' benchmark shape on one GPU
+(FlashInfer fork PR #1, "Performance and reproduction": hidden 7168,
+intermediate 3072, 384 experts, top-6, SwiGLU) at 4096 tokens.
+
 Prints one JSON line (rank 0).  --impl reference times the CPU oracle instead
 (bounded samples on the host cores).  Multi-GPU runs (torchrun) are replicas:
 every rank runs the same workload on its own GPU, no collective on the data
@@ -33,6 +37,11 @@ from nvfp4_token_routed_gb300 import workloads as W  # noqa: E402
 
 METRIC = "MoE-layer tokens/s and µs/layer at 1 GB300"
 FALLBACK_HBM_GBS = 6800.0
+DEFAULT_WORKLOAD = W.PAGES_E384.name
+DEFAULT_T = 4096
+# the oracle's samples of large workloads use at most this many distinct experts
+# (its weight preparation, outside the timed region, grows with the experts)
+ORACLE_MAX_EXPERTS = 24
 
 
 def parse():
@@ -41,8 +50,10 @@ def parse():
     p.add_argument("--steps", type=int, default=3000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default=W.SWIGLU_E64.name, choices=list(W.ALL))
-    p.add_argument("--T", type=int, default=0, help="override the workload's token count")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(W.ALL))
+    p.add_argument("--T", type=int, default=-1,
+                   help="token count (default: 4096 for the default workload, else the "
+                        "workload's own)")
     p.add_argument("--E", type=int, default=0, help="override the expert count (profiling cases)")
     p.add_argument("--no-graph", action="store_true")
     p.add_argument("--w4a16", action="store_true", help="time the BF16-activation variant")
@@ -131,6 +142,16 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
+def workload_of(args):
+    wl = W.ALL[args.workload]
+    T = args.T if args.T >= 0 else (DEFAULT_T if args.workload == DEFAULT_WORKLOAD else 0)
+    if T:
+        wl = wl.with_T(T)
+    if getattr(args, "E", 0):
+        wl = wl.with_E(args.E)
+    return wl
+
+
 def make_inputs(wl, device):
     big = wl.E * (wl.N1 + wl.I) * wl.H > 2e9
     gen_dev = device if big else "cpu"
@@ -140,112 +161,122 @@ def make_inputs(wl, device):
     return x, w1, w2, ids, wts
 
 
-def algorithmic_fc1_bytes(wl, ids, w4a16=False):
-    """Algorithmic DRAM bytes of one FC1 launch: each touched expert's FC1 codes
-    and scales once (9/16 byte per weight); W4A4: the permuted token codes and
-    scales, the fp32 activated rows and the per-row scales; W4A16: the permuted
-    bf16 token rows and the bf16 activated rows."""
+def routes_and_experts(wl, ids):
     idsn = ids.cpu().numpy().ravel()
     valid = idsn[(idsn >= 0) & (idsn < wl.E)]
-    U = int(np.unique(valid).size)
-    R = int(valid.size)
-    Hp, Ip = M.padded(wl.H), M.padded(wl.I)
-    N1p = 2 * Ip if wl.act == "swiglu" else Ip
-    weights = U * N1p * Hp * 9 / 16
-    if w4a16:
-        return weights + 2 * R * Hp + 2 * R * Ip, U, R
-    return weights + R * Hp * 9 / 16 + 4 * R * Ip + 4 * R, U, R
+    return int(valid.size), int(np.unique(valid).size)
 
 
-def algorithmic_fc2_bytes(wl, U, R, w4a16=False):
-    """Algorithmic DRAM bytes of one FC2 launch: each touched expert's FC2 codes
-    and scales once, the FC2 input rows (NVFP4, or bf16 for W4A16), the bf16
-    route rows written."""
-    Hp, Ip = M.padded(wl.H), M.padded(wl.I)
-    weights = U * Hp * Ip * 9 / 16
+def algorithmic_bytes(wl, R, U, w4a16=False):
+    """Algorithmic DRAM bytes of the layer and of its two GEMM launches, as the
+    scope table defines them: each touched expert's codes and E4M3 scales once
+    (9/16 byte per weight), the tokens (bf16 in, NVFP4 out of the quantizer and
+    into FC1), the FC2 input (NVFP4 written by the FC1 stage, read by FC2), the
+    bf16 route rows (written by FC2, read by the finalize), the output and the
+    routing ids and scores.  Workspace-only traffic (the permuted token copy, the
+    fp32 activated rows) is not algorithmic; `workspace_bytes` reports it.
+    W4A16 has no token or FC2-input quantization: its GEMMs read bf16 rows."""
+    T, H, I, K = wl.T, wl.H, wl.I, wl.K
+    N1 = 2 * I if wl.act == "swiglu" else I
+    w1 = U * N1 * H * 9 / 16
+    w2 = U * H * I * 9 / 16
     if w4a16:
-        return weights + 2 * R * Ip + 2 * R * Hp
-    return weights + R * Ip * 9 / 16 + 4 * R + 2 * R * Hp
+        fc1 = w1 + 2 * T * H + 2 * R * I
+        fc2 = w2 + 2 * R * I + 2 * R * H
+        layer = w1 + w2 + 2 * T * H + 2 * 2 * R * I + 4 * R * H + 2 * T * H + 8 * T * K
+        ws = 2 * 2 * R * H                               # permuted bf16 rows: written, read
+    else:
+        fc1 = w1 + T * H * 9 / 16 + R * I * 9 / 16
+        fc2 = w2 + R * I * 9 / 16 + 2 * R * H
+        layer = (w1 + w2 + 2 * T * H + 2 * T * H * 9 / 16 + 2 * R * I * 9 / 16 + 4 * R * H
+                 + 2 * T * H + 8 * T * K)
+        ws = 2 * R * H * 9 / 16 + 2 * 4 * R * I + 8 * R  # permuted copy; fp32 rows, row scales
+    return {"fc1": fc1, "fc2": fc2, "layer": layer, "workspace": ws}
 
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def oracle_sample_runner(wl, x, w1, w2, ids, wts):
-    """Build a function that runs the oracle (quantize + W4A4 forward) on the
-    first n tokens of the workload, with only the experts those tokens use."""
+def oracle_sample(wl, ids, max_tokens):
+    """Token indices of the oracle's bounded sample: a prefix of the batch, cut
+    where it would need more than ORACLE_MAX_EXPERTS distinct experts (small
+    layers: every expert is prepared once and the prefix is only cut at
+    max_tokens)."""
+    idsn = ids.cpu().numpy()
+    full = wl.E * (wl.N1 + wl.I) * wl.H <= 1e9
+    n, used = 0, set()
+    while n < min(wl.T, max_tokens):
+        new = used | {int(e) for e in idsn[n] if 0 <= e < wl.E}
+        if not full and n > 0 and len(new) > ORACLE_MAX_EXPERTS:
+            break
+        used, n = new, n + 1
+    return np.arange(n)
+
+
+def oracle_sample_runner(wl, x, w1, w2, ids, wts, sample):
+    """Prepare the oracle's weights for the experts the sample tokens use (outside
+    any timing) and return a function that runs the oracle (quantize + W4A4
+    forward) on a sub-range of the sample and returns its seconds."""
     from oracle import oracle as O
 
-    idsn = ids.cpu().numpy().astype(np.int32)
-    wtn = wts.cpu().numpy().astype(np.float32)
-    xs = W.bf16_bits(x.cpu())
-    cache = {}
+    idsn = ids.cpu().numpy().astype(np.int32)[sample]
+    wtn = wts.cpu().numpy().astype(np.float32)[sample]
+    xs = W.bf16_bits(x[torch.as_tensor(sample, device=x.device)].cpu())
+    used = np.unique(idsn[(idsn >= 0) & (idsn < wl.E)])
+    idx = torch.as_tensor(used, dtype=torch.long, device=w1.device)
+    Wt = O.Weights(W.bf16_bits(w1.index_select(0, idx).cpu()),
+                   W.bf16_bits(w2.index_select(0, idx).cpu()))
+    remap = np.full(wl.E, -1, np.int32)
+    remap[used] = np.arange(used.size, dtype=np.int32)
+    sub_ids = np.where(idsn >= 0, remap[np.clip(idsn, 0, None)], -1).astype(np.int32)
 
     def run(start, n):
         sl = slice(start, start + n)
-        Wt, remap, Eu = prepared_for(sl)
-        sub_ids = np.where(idsn[sl] >= 0, remap[np.clip(idsn[sl], 0, None)], -1).astype(np.int32)
         t0 = time.perf_counter()
         c, f, s = O.quantize_tokens(xs[sl])
-        O.forward_w4a4(Wt, c, f, s, sub_ids, wtn[sl], Eu, wl.H, wl.I, wl.act)
+        O.forward_w4a4(Wt, c, f, s, sub_ids[sl], wtn[sl], used.size, wl.H, wl.I, wl.act)
         return time.perf_counter() - t0
 
-    full = wl.E * (wl.N1 + wl.I) * wl.H <= 1e9   # small enough to prepare every expert once
-
-    def prepared_for(sl):
-        if full:
-            if "all" not in cache:
-                cache["all"] = O.Weights(W.bf16_bits(w1.cpu()), W.bf16_bits(w2.cpu()))
-            return cache["all"], np.arange(wl.E, dtype=np.int32), wl.E
-        used = np.unique(idsn[sl][idsn[sl] >= 0])
-        key = tuple(used.tolist())
-        if key not in cache:
-            cache.clear()
-            idx = torch.as_tensor(used, dtype=torch.long, device=w1.device)
-            cache[key] = O.Weights(W.bf16_bits(w1.index_select(0, idx).cpu()),
-                                   W.bf16_bits(w2.index_select(0, idx).cpu()))
-        remap = np.full(wl.E, -1, np.int32)
-        remap[used] = np.arange(used.size, dtype=np.int32)
-        return cache[key], remap, used.size
-
-    return run, O.num_threads()
+    return run, O.num_threads(), int(used.size)
 
 
 def cpu_baseline(wl, x, w1, w2, ids, wts, seconds):
-    run, cores = oracle_sample_runner(wl, x, w1, w2, ids, wts)
-    # the sample: a prefix of the batch's tokens, all their routes; grown until
-    # it holds about `seconds` of oracle work
-    n = 1
-    t1 = run(0, 1)
-    n = int(max(1, min(wl.T, seconds / max(t1, 1e-6))))
-    t = run(0, n) if n > 1 else t1
-    return {"value": n / t, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"first {n} of {wl.T} tokens of {wl.name} (all their routes; only the "
-                      f"experts they use), quantize + W4A4 forward, {t:.1f} s"}
+    """The oracle as it stands on the host cores, on a bounded sample of the
+    workload: the sample is run whole, repeatedly, until about `seconds` of
+    oracle work have been timed."""
+    sample = oracle_sample(wl, ids, max_tokens=256)
+    run, cores, n_exp = oracle_sample_runner(wl, x, w1, w2, ids, wts, sample)
+    n = sample.size
+    total, reps = 0.0, 0
+    while total < seconds or reps == 0:
+        total += run(0, n)
+        reps += 1
+    return {"value": n * reps / total, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {n} of {wl.T} tokens of {wl.name} (all their routes, {n_exp} "
+                      f"experts prepared outside the timing), quantize + W4A4 forward, "
+                      f"run {reps}x, {total:.1f} s"}
 
 
 def run_reference(args, rank, world):
-    wl = W.ALL[args.workload]
-    if args.T:
-        wl = wl.with_T(args.T)
     if rank != 0:
         return
-    x, w1, w2, ids, wts = make_inputs(wl, "cpu")
-    run, cores = oracle_sample_runner(wl, x, w1, w2, ids, wts)
-    t1 = run(0, 1)
+    wl = workload_of(args)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"  # input generation only
+    x, w1, w2, ids, wts = make_inputs(wl, dev)
+    sample = oracle_sample(wl, ids, max_tokens=64)
+    run, cores, n_exp = oracle_sample_runner(wl, x, w1, w2, ids, wts, sample)
+    del w1, w2
     budget = 150.0  # seconds for warmup + timed steps
-    n = 1
-    per_step = t1
     steps = args.steps
-    # each step is a bounded sample: one token (all its routes) at a time, cycling
+    # each step is a bounded sample: one token (all its routes), cycling over the sample
     times = []
     for i in range(args.warmup):
-        run(i % wl.T, 1)
+        run(i % sample.size, 1)
     for i in range(steps):
-        times.append(run(i % wl.T, n))
+        times.append(run(i % sample.size, 1))
         if sum(times) > budget:
             break
     mean = sum(times) / len(times)
-    value = n / mean
+    value = 1 / mean
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": len(times), "warmup": args.warmup,
             "ms_per_step": mean * 1e3, "higher_is_better": True, "scaling": "weak",
@@ -253,9 +284,10 @@ def run_reference(args, rank, world):
             "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
                        "K": wl.K, "act": wl.act},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                             "sample": f"{n} token per step (all its routes), cycling over the "
-                                       f"{wl.T} tokens; {len(times)} steps run of {steps} asked "
-                                       f"(150 s budget)"},
+                             "sample": f"1 token per step (all its routes), cycling over the "
+                                       f"first {sample.size} of the {wl.T} tokens ({n_exp} "
+                                       f"experts prepared outside the timing); {len(times)} "
+                                       f"steps run of {steps} asked (150 s budget)"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -284,11 +316,7 @@ def replica_throughput(world, tokens_per_step, steps, max_total_ms):
 def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    wl = W.ALL[args.workload]
-    if args.T:
-        wl = wl.with_T(args.T)
-    if args.E:
-        wl = wl.with_E(args.E)
+    wl = workload_of(args)
     x, w1, w2, ids, wts = make_inputs(wl, dev)
     x_d, ids_d, wts_d = x.to(dev), ids.to(dev), wts.to(dev)
     w = M.prepare_weights(w1.to(dev), w2.to(dev), wl.act)
@@ -447,16 +475,18 @@ def run_ours(args, rank, world, local_rank):
 
     if rank != 0:
         return
-    fc1_bytes, U, R = algorithmic_fc1_bytes(wl, ids, args.w4a16)
+    R, U = routes_and_experts(wl, ids)
+    B = algorithmic_bytes(wl, R, U, args.w4a16)
     fc1_mean = statistics.fmean(fc1_ms)
     fc2_mean = statistics.fmean(fc2_ms)
     # the W4A4 forward runs FC1, the FC2-input requant and FC2 as one launch when
     # T*K <= min(2048, 8*E) (moe_nvfp4.h): the roofline is then that launch's,
     # FC1 and FC2 bytes over the FC1 marker interval (the FC2 one is empty)
     fused = (not args.w4a16) and T * K <= min(2048, 8 * wl.E)
-    kernel_bytes = fc1_bytes + (algorithmic_fc2_bytes(wl, U, R, args.w4a16) if fused else 0)
+    kernel_bytes = B["fc1"] + (B["fc2"] if fused else 0)
     hbm, src = peaks()
     achieved = kernel_bytes / (fc1_mean * 1e-3) / 1e9
+    layer_gbs = B["layer"] / (ms_per_step * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -475,9 +505,15 @@ def run_ours(args, rank, world, local_rank):
                      "frac": achieved / hbm, "peak_source": src,
                      "traffic": None if fused else traffic_for(wl.name),
                      "algorithmic_bytes": kernel_bytes,
+                     "workspace_bytes": B["workspace"],
                      "kernel_us": fc1_mean * 1e3, "fc2_kernel_us": fc2_mean * 1e3,
+                     "fc2_frac": (None if fused else
+                                  B["fc2"] / (fc2_mean * 1e-3) / 1e9 / hbm),
                      "timing": "CUDA events recorded by the library around the FC1 launch, "
                                "over a second pass of the same K steps"},
+        "layer_roofline": {"bound": "hbm", "algorithmic_bytes": B["layer"],
+                           "achieved": layer_gbs, "peak": hbm, "unit": "GB/s",
+                           "frac": layer_gbs / hbm},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         # the forward's own count (moe_nvfp4_forward_kernel_count) plus the token
