@@ -24,8 +24,10 @@ DEV = "cuda"
 CASES = {
     # 160 routes over 32 experts: the one-launch FC1 -> FC2 path
     "fused": W.Workload("swiglu_T40_H512_I512_E32_K4", 40, 512, 512, 32, 4, "swiglu"),
-    # 600 routes over 4 experts: three launches
+    # 600 routes over 4 experts: three launches, two to three token tiles per expert
     "separate": W.Workload("swiglu_T300_H512_I256_E4_K2", 300, 512, 256, 4, 2, "swiglu"),
+    # 1024 routes over 64 experts: three launches, 16-row tiles read by route
+    "wide": W.Workload("swiglu_T256_H512_I1024_E64_K4", 256, 512, 1024, 64, 4, "swiglu"),
 }
 LIMIT = 0.05
 
