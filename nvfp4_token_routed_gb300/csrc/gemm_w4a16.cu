@@ -30,8 +30,11 @@
 //     is bound by issue latency at small N)
 //   * warps 2-5: epilogue (alpha, activation, bf16 rounding), one TMEM lane per
 //     thread; SwiGLU pairs gate and up rows through shared memory as in W4A4
-//   * rings: packed-weight slots (4-6) and a ring of 2-3 blocks of 256 K, each
-//     a token stage plus a TMEM slot of decoded weights; each item's
+//   * rings: packed-weight slots (4-9 of 18 KB, as many as shared memory holds
+//     next to a few token stages, each released as soon as the decode warps have
+//     read it into registers), TMEM slots of decoded weights (3 blocks of 256 K)
+//     and token stages (2-8 blocks of 256 K, loaded ahead of the MMAs
+//     independently of the decode); each item's
 //     accumulator is split into even / odd K-step partial sums; 1-2 items in
 //     flight; every wait bounded.
 #include <cuda.h>
@@ -56,8 +59,9 @@ constexpr int kBK = kRawK;                  // K elements per token stage / deco
 constexpr int kChunks = kBK / 64;           // 64-element (128-byte) K chunks per token stage
 constexpr int kChunkRowBytes = 128;         // 64 bf16 per row per K chunk
 constexpr int kACols = kBK / 2;             // TMEM columns of one decoded A slot
-constexpr int kMaxRaw = 6;                  // packed-weight slots (released after decode)
-constexpr int kMaxRing = 3;                 // blocks in flight: token stage + TMEM slot of decoded A
+constexpr int kMaxRaw = 10;                 // packed-weight slots (released once read)
+constexpr int kMaxRing = 3;                 // TMEM slots of decoded A (blocks being decoded / multiplied)
+constexpr int kMaxTok = 8;                  // token stages (each one 256-K block of the token tile)
 constexpr int kMaxAcc = 2;
 constexpr int kTmemCols = 512;
 constexpr int kXchgFloats = 2 * 64 * 33;
@@ -77,8 +81,9 @@ static_assert(kDecodePerQuad * 4 == kDecodeWarps && kChunksPerWarp * kDecodePerQ
 constexpr int kBarRawFull = 0;
 constexpr int kBarRawEmpty = kBarRawFull + kMaxRaw;
 constexpr int kBarFull = kBarRawEmpty + kMaxRaw;          // token stage landed (TMA bytes)
-constexpr int kBarReady = kBarFull + kMaxRing;            // A decoded and token stage landed
-constexpr int kBarFree = kBarReady + kMaxRing;            // the block's MMAs are done
+constexpr int kBarTokEmpty = kBarFull + kMaxTok;          // token stage's MMAs are done
+constexpr int kBarReady = kBarTokEmpty + kMaxTok;         // A slot decoded
+constexpr int kBarFree = kBarReady + kMaxRing;            // A slot's MMAs are done
 constexpr int kBarAccFull = kBarFree + kMaxRing;
 constexpr int kBarAccEmpty = kBarAccFull + kMaxAcc;
 constexpr int kBarItemFull = kBarAccEmpty + kMaxAcc;
@@ -118,8 +123,11 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
       mbar_init(R.bar(kBarRawFull + s), 1);
       mbar_init(R.bar(kBarRawEmpty + s), kDecodeWarps);
     }
-    for (int j = 0; j < kMaxRing; ++j) {
+    for (int j = 0; j < kMaxTok; ++j) {
       mbar_init(R.bar(kBarFull + j), 1);
+      mbar_init(R.bar(kBarTokEmpty + j), kIssuers);
+    }
+    for (int j = 0; j < kMaxRing; ++j) {
       mbar_init(R.bar(kBarReady + j), kDecodeWarps);
       mbar_init(R.bar(kBarFree + j), kIssuers);
     }
@@ -163,14 +171,18 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
   const int acc_stride = nacc * acc_cols;                  // TMEM columns per item
   const int nbuf = max_n16 <= 64 ? 2 : 1;                  // accumulator buffers
   const int a_base = nbuf * acc_stride;                    // decoded A slots follow the accumulators
-  const int n_raw = max_n16 <= 64 ? kMaxRaw : 4;
+  // Shared memory goes first to packed-weight slots: the weight stream needs
+  // its bytes in flight to cover the memory latency under load (measured on
+  // GB300: with 6 slots of 18 KB the decode warps waited for weights 80% of the
+  // time), then to token stages (at least 4, or 2 for 128-row tiles).
+  const int tok_min = max_n16 <= 64 ? 4 : 2;
+  const int n_raw = min(kMaxRaw, (kRingBudget - tok_min * stage_bytes) / kRawSlotBytes);
   uint8_t* raw_ring = rings;
   uint8_t* stage_ring = rings + n_raw * kRawSlotBytes;     // multiple of 1024 past rings
-  // Block ring: block b of the CTA's K stream uses token stage and TMEM A slot
-  // b % n_ring, so one barrier says "ready" (decoded and landed) and one "free".
-  int n_ring = (kTmemCols - a_base) / kACols;
-  n_ring = min(n_ring, (kRingBudget - n_raw * kRawSlotBytes) / stage_bytes);
-  n_ring = min(n_ring, kMaxRing);
+  // Block b of the CTA's K stream uses TMEM A slot b % n_ring and token stage
+  // b % n_tok, so token loads run ahead of the MMAs independently of the decode.
+  const int n_ring = min(kMaxRing, (kTmemCols - a_base) / kACols);
+  const int n_tok = min(kMaxTok, (kRingBudget - n_raw * kRawSlotBytes) / stage_bytes);
 
   const int kraw = a.K / kRawK;                        // packed-weight slots per item
   const int atoms = a.K / 64;
@@ -234,11 +246,12 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
   } else if (warp == kTokenWarp) {
     // ------------------------------------------------------------ token producer
     // One 3-D tiled copy per token stage: the kChunks 64-K chunks of the tile's
-    // rows, in the smallest of the 16/32/64/128-row boxes that covers them.
+    // rows, in the smallest of the 16/32/64/128-row boxes that covers them.  A
+    // stage is refilled once both MMA issuers have finished with it.
     if (lane == 0) {
-      int last_stg[kMaxRing];
+      int last_stg[kMaxTok];
 #pragma unroll
-      for (int s = 0; s < kMaxRing; ++s) last_stg[s] = -1;
+      for (int s = 0; s < kMaxTok; ++s) last_stg[s] = -1;
       const uint64_t pol_x = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
@@ -251,7 +264,7 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
         const uint32_t tx = (uint32_t)kChunks * (16u << bl) * kChunkRowBytes;
         const int b_row = cur.tt * kTileRows;
         for (int kb = 0; kb < a.K / kBK; ++kb) {
-          if (!wait_or_abort(R.bar(kBarFree + stage), phase ^ 1, abort_flag, a.status)) {
+          if (!wait_or_abort(R.bar(kBarTokEmpty + stage), phase ^ 1, abort_flag, a.status)) {
             ok = false;
             break;
           }
@@ -260,14 +273,14 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
           tma_load_3d_hint(smem_u32(stage_ring + stage * stage_bytes), &tmB.box[bl], full, 0,
                            b_row, kChunks * kb, pol_x);
           last_stg[stage] = (int)phase;
-          if (++stage == n_ring) {
+          if (++stage == n_tok) {
             stage = 0;
             phase ^= 1;
           }
         }
       }
       if (!ok || *abort_flag) {
-        for (int s = 0; s < kMaxRing; ++s)
+        for (int s = 0; s < kMaxTok; ++s)
           if (last_stg[s] >= 0) mbar_wait(R.bar(kBarFull + s), (uint32_t)last_stg[s]);
       }
     }
@@ -290,27 +303,49 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
       const TileInfo cur = queue_pop_warp(Q, qp, abort_flag, a.status);
       if (cur.rows == 0) break;
       for (int kr = 0; kr < kraw && ok; ++kr) {
-        // the packed slot has landed and the TMEM slot's previous MMAs are done
-        if (!wait_or_abort(R.bar(kBarRawFull + rs), rphase, abort_flag, a.status) ||
-            !wait_or_abort(R.bar(kBarFree + slot), aphase ^ 1, abort_flag, a.status)) {
+        // the packed slot has landed: read this warp's part of it into
+        // registers (row m's chunks and their block-scale words) and release it
+        // at once, before waiting for a TMEM slot
+        if (!wait_or_abort(R.bar(kBarRawFull + rs), rphase, abort_flag, a.status)) {
           ok = false;
           break;
         }
-        tc_fence_after();
         const uint32_t rb = smem_u32(raw_ring + rs * kRawSlotBytes);
-        const uint32_t acol = tmem + lane_q + a_base + slot * kACols;
+        uint32_t sw[2];
+        uint4 raws[2][kChunksPerWarp];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           // row m's block scales of this warp's chunks: one 4-scale word of atom
           // 2h (chunks 0-1) or 2h+1 (chunks 2-3)
           const int atom = 2 * h + (kChunksPerWarp * wq >= 2 ? 1 : 0);
-          const uint32_t sw = lds32(rb + kRawBytes + atom * kAtom + (m & 31) * 16 + (m >> 5) * 4);
+          sw[h] = lds32(rb + kRawBytes + atom * kAtom + (m & 31) * 16 + (m >> 5) * 4);
+#pragma unroll
+          for (int cc = 0; cc < kChunksPerWarp; ++cc) {
+            const int c = kChunksPerWarp * wq + cc;
+            raws[h][cc] = lds128(rb + m * 128 + (((uint32_t)(4 * h + c) ^ swz) << 4));
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(R.bar(kBarRawEmpty + rs));
+        if (++rs == n_raw) {
+          rs = 0;
+          rphase ^= 1;
+        }
+        // the TMEM slot's previous MMAs are done
+        if (!wait_or_abort(R.bar(kBarFree + slot), aphase ^ 1, abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t acol = tmem + lane_q + a_base + slot * kACols;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
 #pragma unroll
           for (int cc = 0; cc < kChunksPerWarp; ++cc) {  // 32 elements per 16-byte chunk
             const int c = kChunksPerWarp * wq + cc;        // chunk within the half
-            const uint4 raw = lds128(rb + m * 128 + (((uint32_t)(4 * h + c) ^ swz) << 4));
+            const uint4 raw = raws[h][cc];
             uint32_t sc0, sc1;
-            e4m3x2_scale_bf16x2(sw >> (16 * (c & 1)), sc0, sc1);
+            e4m3x2_scale_bf16x2(sw[h] >> (16 * (c & 1)), sc0, sc1);
             uint32_t o[16];
             decode8_bf16(raw.x, sc0, o);
             decode8_bf16(raw.y, sc0, o + 4);
@@ -319,22 +354,9 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
             tmem_st16(acol + 64 * h + 16 * c, o);
           }
         }
-        // this warp has read its part of the packed slot
-        __syncwarp();
-        if (lane == 0) mbar_arrive(R.bar(kBarRawEmpty + rs));
-        if (++rs == n_raw) {
-          rs = 0;
-          rphase ^= 1;
-        }
         tmem_wait_st();
         tc_fence_before();
-        // warp 6 also waits for the block's token stage, so that "ready"
-        // covers both operands and the MMA issuers wait on one barrier
-        if (warp == 6 && lane == 0 &&
-            !wait_or_abort(R.bar(kBarFull + slot), aphase, abort_flag, a.status))
-          ok = false;
-        ok = __shfl_sync(0xFFFFFFFFu, ok, 0) && ok;
-        if (!ok) break;
+        __syncwarp();
         if (lane == 0) mbar_arrive(R.bar(kBarReady + slot));
         if (++slot == n_ring) {
           slot = 0;
@@ -351,8 +373,8 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
     // each MMA and commit: that keeps the MMA rate near the tensor pipe's even
     // for 16-token tiles, where a single-lane loop is bound by issue latency.
     const int part = warp == 1 ? 0 : 1;
-    int slot = 0, local = 0;
-    uint32_t aphase = 0;
+    int slot = 0, local = 0, ts = 0;
+    uint32_t aphase = 0, tphase = 0;
     QueuePos qp;
     bool ok = true, issued = false;
     const int kblocks = a.K / kBK;
@@ -370,11 +392,13 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
       tc_fence_after();
       const uint32_t acc = tmem + buf * acc_stride + part * acc_cols;
       for (int kb = 0; kb < kblocks; ++kb) {
+        // the block's decoded weights and its token stage
         ok = __all_sync(0xFFFFFFFFu,
-                        wait_or_abort(R.bar(kBarReady + slot), aphase, abort_flag, a.status));
+                        wait_or_abort(R.bar(kBarReady + slot), aphase, abort_flag, a.status) &&
+                            wait_or_abort(R.bar(kBarFull + ts), tphase, abort_flag, a.status));
         if (!ok) break;
         tc_fence_after();
-        const uint32_t sb = smem_u32(stage_ring + slot * stage_bytes);
+        const uint32_t sb = smem_u32(stage_ring + ts * stage_bytes);
         const uint32_t acol = tmem + a_base + slot * kACols;
 #pragma unroll
         for (int kp = 0; kp < kBK / 32; ++kp) {
@@ -384,9 +408,14 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
         }
         issued = true;
         tc_commit_warp(R.bar(kBarFree + slot));
+        tc_commit_warp(R.bar(kBarTokEmpty + ts));
         if (++slot == n_ring) {
           slot = 0;
           aphase ^= 1;
+        }
+        if (++ts == n_tok) {
+          ts = 0;
+          tphase ^= 1;
         }
       }
       if (!ok) break;
