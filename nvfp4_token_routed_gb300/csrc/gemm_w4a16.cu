@@ -455,6 +455,7 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
       if constexpr (MODE == kFc1Swiglu) {
         const bool gate = q < 2;
         const int f = mt * 64 + (r & 63);
+        const int fo = (f & ~7) | k8_pos(f & 7);  // FC2 meets it in the decode's K order
         for (int c0 = 0; c0 < n16; c0 += 32, xb ^= 1) {
           float v[32];
           tmem_ld16(acc + c0, *reinterpret_cast<float(*)[16]>(v));
@@ -487,7 +488,7 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
                 yu = fmaxf(fminf(yu, a.swiglu_limit), -a.swiglu_limit);
               }
               const float act = __fmul_rn(__fdiv_rn(yg, __fadd_rn(1.0f, expf(-yg))), yu);
-              a.route_out[p * a.I + f] = __bfloat16_as_ushort(__float2bfloat16_rn(act));
+              a.route_out[p * a.I + fo] = __bfloat16_as_ushort(__float2bfloat16_rn(act));
             }
           }
         }
@@ -511,7 +512,7 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
             const float y = __fmul_rn(v[j], alpha);
             if constexpr (MODE == kFc1Relu2) {
               const float t = fmaxf(y, 0.0f);
-              a.route_out[p * a.I + mt * 128 + r] =
+              a.route_out[p * a.I + mt * 128 + (r & ~7) + k8_pos(r & 7)] =
                   __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(t, t)));
             } else {
               a.route_out[p * a.H + mt * 128 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(y));

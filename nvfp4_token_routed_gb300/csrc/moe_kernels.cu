@@ -8,6 +8,7 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "ptx.cuh"
 #include "quant.cuh"
 
 namespace moe {
@@ -330,7 +331,8 @@ __global__ void __launch_bounds__(kChunk) route_scatter_kernel(
 
 // Row gather of one route (one warp): the token's quantized row and its block
 // scales (W4A4; rows already padded to Hp by the quantizer) or its bf16 row
-// with the Hp - H padding columns zeroed (W4A16) into permuted row p.
+// with the Hp - H padding columns zeroed (W4A16, each group of 8 values in the
+// K order 0,4,1,5,2,6,3,7 of the decoded weights) into permuted row p.
 struct GatherArgs {
   int K, H, Hp;
   const uint8_t* xc;
@@ -348,7 +350,8 @@ __device__ __forceinline__ void gather_route_row(const GatherArgs& g, int idx, i
   if constexpr (kW4A16) {
     const uint4* src = g.xb + (size_t)t * (g.H / 8);
     uint4* dst = g.pb + (size_t)p * (g.Hp / 8);
-    for (int i = lane; i < g.H / 8; i += 32) dst[i] = __ldg(src + i);
+    // in the K order of the decoded weights it meets in the W4A16 GEMM
+    for (int i = lane; i < g.H / 8; i += 32) dst[i] = k8_order(__ldg(src + i));
     for (int i = g.H / 8 + lane; i < g.Hp / 8; i += 32) dst[i] = make_uint4(0u, 0u, 0u, 0u);
   } else {
     const uint4* src = reinterpret_cast<const uint4*>(g.xc + (size_t)t * (g.Hp / 2));

@@ -404,25 +404,35 @@ __device__ __forceinline__ void e4m3x2_scale_bf16x2(uint32_t b, uint32_t& s0, ui
   s1 = __byte_perm(t, 0, 0x3232);
 }
 
-// 8 E2M1 codes (one 32-bit word, element 0 in the low nibble) -> 4 bf16x2 words
-// (element 0 in the low half) of code x scale x 2^-8, the scale given by
-// e4m3x2_scale_bf16x2.  Per pair of codes: a byte permute puts them 16 bits apart
-// (the sign-replicating selector of a byte below 0x80 yields zero), one
-// multiply by 4160 = 2^6 + 2^12 makes the shifted copies that hold the
-// magnitude bits (<< 6) and the sign bit (<< 12), a mask keeps those bits, and
-// one bf16x2 multiply applies the scale.
+// 8 E2M1 codes (one 32-bit word, code j in nibble j) -> 4 bf16x2 words of
+// code x scale x 2^-8, the scale given by e4m3x2_scale_bf16x2.  Word i holds
+// codes i (low half) and i + 4 (high half): the two nibbles sit 16 bits apart
+// in the word already, so one mask isolates a pair, one multiply makes the
+// shifted copies that hold the magnitude bits (at bits 6-8) and the sign bit
+// (at bit 15), a mask keeps those bits, and one bf16x2 multiply applies the
+// scale.  (Pairs 2 and 3 come from the word shifted right by 8; pair 1 is
+// already 4 bits up, so its multiplier is 4160 / 16.)  The K order of the
+// decoded operand is therefore 0, 4, 1, 5, 2, 6, 3, 7 within each group of 8,
+// and the bf16 operand it meets in the MMA is stored in that order too.
 __device__ __forceinline__ void decode8_bf16(uint32_t w, uint32_t scale, uint32_t* o) {
-  const uint32_t ev = w & 0x0F0F0F0Fu;         // codes 0, 2, 4, 6 (one per byte)
-  const uint32_t od = (w >> 4) & 0x0F0F0F0Fu;  // codes 1, 3, 5, 7
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    // result bytes: [code 2j, 0, code 2j+1, 0]
-    const uint32_t sel = (uint32_t)j | ((8u | j) << 4) | ((4u + j) << 8) | ((8u | j) << 12);
-    uint32_t y;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(y) : "r"(ev), "r"(od), "r"(sel));
-    const uint32_t x = (y * 4160u) & 0x81C081C0u;
-    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[j]) : "r"(x), "r"(scale));
-  }
+  const uint32_t w8 = w >> 8;
+  const uint32_t x0 = ((w & 0x000F000Fu) * 4160u) & 0x81C081C0u;   // codes 0, 4
+  const uint32_t x1 = ((w & 0x00F000F0u) * 260u) & 0x81C081C0u;    // codes 1, 5
+  const uint32_t x2 = ((w8 & 0x000F000Fu) * 4160u) & 0x81C081C0u;  // codes 2, 6
+  const uint32_t x3 = ((w8 & 0x00F000F0u) * 260u) & 0x81C081C0u;   // codes 3, 7
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[0]) : "r"(x0), "r"(scale));
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[1]) : "r"(x1), "r"(scale));
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[2]) : "r"(x2), "r"(scale));
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[3]) : "r"(x3), "r"(scale));
+}
+
+// Position of element i (0..7) of a group of 8 in the K order that decode8_bf16
+// gives the decoded weights: 0, 4, 1, 5, 2, 6, 3, 7.
+__device__ __forceinline__ int k8_pos(int i) { return i < 4 ? 2 * i : 2 * i - 7; }
+// 8 bf16 values in natural order (one 16-byte vector) -> the same in that order.
+__device__ __forceinline__ uint4 k8_order(const uint4& v) {
+  return make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.x, v.z, 0x7632),
+                    __byte_perm(v.y, v.w, 0x5410), __byte_perm(v.y, v.w, 0x7632));
 }
 
 // E4M3 byte -> fp32, exact (bias 7, subnormal step 2^-9).

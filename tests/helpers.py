@@ -49,6 +49,21 @@ def unpack_codes(packed):
     return np.stack([packed & 15, packed >> 4], axis=-1).reshape(*packed.shape[:-1], -1)
 
 
+# K order of each group of 8 values in the W4A16 GEMM's bf16 operands (the order
+# in which the GEMM decodes a 32-bit word of eight E2M1 codes): the permuted
+# token rows (x_perm) and the bf16 activated rows (act_bf16) are stored so.
+K8_ORDER = np.array([0, 4, 1, 5, 2, 6, 3, 7])
+
+
+def from_k8_order(rows):
+    """Rows stored with each group of 8 values in K8_ORDER -> natural order."""
+    r = np.asarray(rows)
+    g = r.reshape(*r.shape[:-1], r.shape[-1] // 8, 8)
+    nat = np.empty_like(g)
+    nat[..., K8_ORDER] = g
+    return nat.reshape(r.shape)
+
+
 def rel_l2(a, b):
     a = np.asarray(a, np.float64)
     b = np.asarray(b, np.float64)

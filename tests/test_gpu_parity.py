@@ -13,8 +13,8 @@ import nvfp4_token_routed_gb300 as M
 from nvfp4_token_routed_gb300 import workloads as W
 from oracle import oracle as O
 
-from helpers import (TILE_ROWS, OracleRun, bf16_np, rel_l2, signed_step, stored_fc1_rows, to_np_u16,
-                     unpack_codes, unswizzle)
+from helpers import (TILE_ROWS, OracleRun, bf16_np, from_k8_order, rel_l2, signed_step,
+                     stored_fc1_rows, to_np_u16, unpack_codes, unswizzle)
 
 pytestmark = pytest.mark.gpu
 
@@ -209,7 +209,7 @@ def test_w4a16_permuted_rows_and_routing(name):
     perm = g.view("perm", torch.int32, (g.L["rows_cap"],))
     assert np.array_equal(perm[rmap], o.res["perm"])
     xp = g.view("x_perm", torch.int16, (g.L["rows_cap"], wl.H))[rmap].view(np.uint16)
-    assert np.array_equal(xp, to_np_u16(x)[o.res["perm"] // wl.K])
+    assert np.array_equal(from_k8_order(xp), to_np_u16(x)[o.res["perm"] // wl.K])
 
 
 @pytest.mark.parametrize("name", list(CASES))
@@ -217,7 +217,7 @@ def test_w4a16_handoff_route_rows_and_output(name):
     wl, g, o, x = _run16(name)
     rmap = _rows_map(g, o)
     act = g.view("act_bf16", torch.int16, (g.L["rows_cap"], wl.I))[rmap].view(np.uint16)
-    a_g, a_o = bf16_np(act), bf16_np(o.res["act"])
+    a_g, a_o = bf16_np(from_k8_order(act)), bf16_np(o.res["act"])
     assert rel_l2(a_g, a_o) <= 4e-3
     # bf16 rounding of an fp32-accumulated vs an fp64 value: one bf16 step apart
     # at most, except where cancellation leaves a value near zero (at most 0.1%)
