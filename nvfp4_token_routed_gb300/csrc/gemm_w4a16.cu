@@ -331,13 +331,8 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
           rs = 0;
           rphase ^= 1;
         }
-        // the TMEM slot's previous MMAs are done
-        if (!wait_or_abort(R.bar(kBarFree + slot), aphase ^ 1, abort_flag, a.status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t acol = tmem + lane_q + a_base + slot * kACols;
+        // decode into registers while the TMEM slot may still be in use
+        uint32_t o[2][kChunksPerWarp][16];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
 #pragma unroll
@@ -346,14 +341,24 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
             const uint4 raw = raws[h][cc];
             uint32_t sc0, sc1;
             e4m3x2_scale_bf16x2(sw[h] >> (16 * (c & 1)), sc0, sc1);
-            uint32_t o[16];
-            decode8_bf16(raw.x, sc0, o);
-            decode8_bf16(raw.y, sc0, o + 4);
-            decode8_bf16(raw.z, sc1, o + 8);
-            decode8_bf16(raw.w, sc1, o + 12);
-            tmem_st16(acol + 64 * h + 16 * c, o);
+            decode8_bf16(raw.x, sc0, o[h][cc]);
+            decode8_bf16(raw.y, sc0, o[h][cc] + 4);
+            decode8_bf16(raw.z, sc1, o[h][cc] + 8);
+            decode8_bf16(raw.w, sc1, o[h][cc] + 12);
           }
         }
+        // the TMEM slot's previous MMAs are done
+        if (!wait_or_abort(R.bar(kBarFree + slot), aphase ^ 1, abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t acol = tmem + lane_q + a_base + slot * kACols;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int cc = 0; cc < kChunksPerWarp; ++cc)
+            tmem_st16(acol + 64 * h + 16 * (kChunksPerWarp * wq + cc), o[h][cc]);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
