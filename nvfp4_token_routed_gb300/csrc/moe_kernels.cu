@@ -24,6 +24,9 @@ namespace moe {
 // With `static_enc` (the per-tensor recipe, Megatron-LM PR #8262, "How to
 // extend": nvfp4_quantize(x, a1_scale) with a fixed scale tensor) every row uses
 // that encode scale and no per-token scale is written.
+// Rows of up to 512 * NB values (NB blocks of 16 per lane) are loaded once into
+// registers, all their loads in flight together; longer rows are read twice.
+template <int NB>
 __global__ void __launch_bounds__(256) quantize_tokens_kernel(int T, int H, int Hp,
                                                               const uint4* __restrict__ x,
                                                               uint8_t* __restrict__ codes,
@@ -36,6 +39,49 @@ __global__ void __launch_bounds__(256) quantize_tokens_kernel(int T, int H, int 
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
   const uint4* row = x + (size_t)t * (H / 8);
+  const int nb = H / 16;
+  if (NB > 0 && nb <= 32 * NB) {
+    // lane l holds blocks l, l + 32, ...: two 16-byte vectors each
+    uint4 r[NB > 0 ? NB : 1][2];
+    float m = 0.0f;
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      const int b = lane + 32 * j;
+      if (b < nb) {
+        r[j][0] = __ldcs(row + 2 * b);
+        r[j][1] = __ldcs(row + 2 * b + 1);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+      if (lane + 32 * j < nb) m = fmaxf(m, fmaxf(bf16x8_absmax(r[j][0]), bf16x8_absmax(r[j][1])));
+    if (static_enc) m = 1.0f;  // any non-zero value: the static path quantizes every real block
+    m = warp_max(m);
+    uint2* crow = reinterpret_cast<uint2*>(codes + (size_t)t * (Hp / 2));
+    uint8_t* srow = sf + (size_t)t * (Hp / 16);
+    for (int b = (m == 0.0f ? 0 : nb) + lane; b < Hp / 16; b += 32) {
+      crow[b] = make_uint2(0u, 0u);
+      srow[b] = 0;
+    }
+    if (m == 0.0f) {
+      if (lane == 0) scale[t] = 0.0f;
+      return;
+    }
+    const float enc = static_enc ? *static_enc : __fdiv_rn(kRecipeMax, m);
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      const int b = lane + 32 * j;
+      if (b < nb) {
+        float v[16];
+        bf16x16_to_f32(r[j][0], r[j][1], v);
+        uint2 q;
+        srow[b] = (uint8_t)quant_block16(v, enc, q);
+        crow[b] = q;
+      }
+    }
+    if (lane == 0 && !static_enc) scale[t] = __fmul_rn(m, kRecipeInv);
+    return;
+  }
   float m = 1.0f;  // any non-zero value: the static path quantizes every real block
   if (!static_enc) {
     m = 0.0f;
@@ -67,8 +113,10 @@ void launch_quantize_tokens(int T, int H, int Hp, const void* x, uint8_t* codes,
                             float* scale, const float* static_enc, cudaStream_t s) {
   const int warps = 8;
   const int blocks = (T + warps - 1) / warps;
-  launch_pdl(quantize_tokens_kernel, dim3(blocks), dim3(warps * 32), 0, s, T, H, Hp,
-             static_cast<const uint4*>(x), codes, sf, scale, static_enc);
+  auto* k = H <= 2048 ? quantize_tokens_kernel<4> : H <= 8192 ? quantize_tokens_kernel<16>
+                                                              : quantize_tokens_kernel<0>;
+  launch_pdl(k, dim3(blocks), dim3(warps * 32), 0, s, T, H, Hp, static_cast<const uint4*>(x),
+             codes, sf, scale, static_enc);
 }
 
 // ============================================================== weight preparation
@@ -546,6 +594,8 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
 // route reads the fp32 activated row written by the FC1 epilogue.
 // With `static_enc` (per-tensor recipe: fc2_input_scale = a2_scale) every row
 // uses that encode scale and its row scale is 1.
+// G: rows of up to G * 2048 values are read once, into registers.
+template <int G>
 __global__ void __launch_bounds__(256) requant_kernel(int TK, int I, const int32_t* __restrict__ inv,
                                                       const float* __restrict__ act,
                                                       uint8_t* __restrict__ qc,
@@ -559,7 +609,7 @@ __global__ void __launch_bounds__(256) requant_kernel(int TK, int I, const int32
   if (idx >= TK) return;
   const int p = inv[idx];
   if (p < 0) return;
-  requant_row_warp(act + (size_t)p * I, I, (uint64_t)p, qc, qsf, qs, static_enc, lane);
+  requant_row_warp<G>(act + (size_t)p * I, I, (uint64_t)p, qc, qsf, qs, static_enc, lane);
 }
 
 void launch_requant(int TK, int I, const int32_t* inv, const float* act, uint8_t* qc, uint8_t* qsf,
@@ -569,8 +619,12 @@ void launch_requant(int TK, int I, const int32_t* inv, const float* act, uint8_t
   // long pass is done (ReLU2 H7168 E256 T=4096: -11 us); small batches keep
   // 8-warp blocks (the many tiny blocks cost more than they overlap there).
   const int warps = TK > kSmallRoutes ? 2 : 8;
-  launch_pdl(requant_kernel, dim3((TK + warps - 1) / warps), dim3(warps * 32), 0, s, TK, I, inv,
-             act, qc, qsf, qs, static_enc);
+  if (I <= 2048)
+    launch_pdl(requant_kernel<1>, dim3((TK + warps - 1) / warps), dim3(warps * 32), 0, s, TK, I,
+               inv, act, qc, qsf, qs, static_enc);
+  else
+    launch_pdl(requant_kernel<2>, dim3((TK + warps - 1) / warps), dim3(warps * 32), 0, s, TK, I,
+               inv, act, qc, qsf, qs, static_enc);
 }
 
 // ============================================================== finalize

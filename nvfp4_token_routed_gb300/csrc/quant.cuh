@@ -88,19 +88,20 @@ __device__ __forceinline__ float warp_max(float v) {
 // per-tensor recipe: fc2_input_scale = a2_scale, row scale 1).  Writes the I/2
 // code bytes of permuted row p, its block scales into the 128x4-swizzled plane
 // and its row scale.  Lane l owns blocks l, l+32, ... (16 consecutive values
-// each, 64 contiguous bytes); a row of up to 2048 values is loaded once into
-// registers (one round trip), longer rows in groups of 128 blocks read twice.
-// The fused GEMM's requant uses the same quant_block16 and amax, so both give
-// the same bits.
+// each, 64 contiguous bytes).  A row of up to G * 2048 values is loaded once
+// into registers (all its loads in flight together); longer rows are read in
+// groups of 128 blocks, twice.  The fused GEMM's requant uses the same
+// quant_block16 and amax, so both give the same bits.
+template <int G>
 __device__ __forceinline__ void requant_group_load(const float4* __restrict__ r4, int b0, int nb,
-                                                   int lane, float (&v)[4][16]) {
+                                                   int lane, float (&v)[4 * G][16]) {
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
+  for (int k = 0; k < 4 * G; ++k) {
     const int b = b0 + lane + 32 * k;
     if (b < nb) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float4 f = r4[4 * b + i];
+        const float4 f = __ldcs(r4 + 4 * b + i);  // streamed: read once
         v[k][4 * i] = f.x;
         v[k][4 * i + 1] = f.y;
         v[k][4 * i + 2] = f.z;
@@ -109,22 +110,24 @@ __device__ __forceinline__ void requant_group_load(const float4* __restrict__ r4
     }
   }
 }
+template <int G>
 __device__ __forceinline__ void requant_row_warp(const float* __restrict__ row, int I, uint64_t p,
                                                  uint8_t* __restrict__ qc,
                                                  uint8_t* __restrict__ qsf,
                                                  float* __restrict__ qs,
                                                  const float* __restrict__ static_enc, int lane) {
+  constexpr int kGroup = 128 * G;  // blocks held in registers at once
   const float4* r4 = reinterpret_cast<const float4*>(row);
   const int nb = I / 16;  // a multiple of 16: lanes come in groups of four in range
   const uint32_t c16 = (uint32_t)nb;
-  float v[4][16];
+  float v[4 * G][16];
   float m = 1.0f;
   if (!static_enc) {
     m = 0.0f;
-    for (int b0 = 0; b0 < nb; b0 += 128) {
-      requant_group_load(r4, b0, nb, lane, v);
+    for (int b0 = 0; b0 < nb; b0 += kGroup) {
+      requant_group_load<G>(r4, b0, nb, lane, v);
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
+      for (int k = 0; k < 4 * G; ++k)
         if (b0 + lane + 32 * k < nb) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[k][i]));
@@ -142,11 +145,11 @@ __device__ __forceinline__ void requant_row_warp(const float* __restrict__ row, 
     return;
   }
   const float enc = static_enc ? *static_enc : __fdiv_rn(kRecipeMax, m);
-  for (int b0 = 0; b0 < nb; b0 += 128) {
-    // rows of up to 2048 values (and the static-scale path) are still in registers
-    if (nb > 128 || static_enc) requant_group_load(r4, b0, nb, lane, v);
+  for (int b0 = 0; b0 < nb; b0 += kGroup) {
+    // a row of one group (and the static-scale path) is still in registers
+    if (nb > kGroup || static_enc) requant_group_load<G>(r4, b0, nb, lane, v);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < 4 * G; ++k) {
       const int b = b0 + lane + 32 * k;
       uint32_t sfb = 0;
       if (b < nb) {
