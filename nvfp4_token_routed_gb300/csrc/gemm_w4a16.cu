@@ -437,7 +437,6 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
     const int r = q * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
     int local = 0;
-    int xb = 0;
     QueuePos qp;
     while (true) {
       const TileInfo cur = queue_pop_warp(Q, qp, abort_flag, a.status);
@@ -458,10 +457,20 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
       tc_fence_after();
       const uint32_t acc = tmem + lane_addr + buf * acc_stride;
       if constexpr (MODE == kFc1Swiglu) {
-        const bool gate = q < 2;
-        const int f = mt * 64 + (r & 63);
+        // Rows 0-63 of the weight tile are the gate rows and 64-127 the up rows
+        // of the same 64 features.  For each chunk of 32 tokens every thread
+        // publishes its row's alpha-scaled sums in shared memory; then thread r
+        // forms the activations of feature r % 64 for tokens 16 (r / 64) ..
+        // 16 (r / 64) + 15 of the chunk, so that all 128 threads share the
+        // activation work.
+        const int fl = r & 63;
+        const int j0 = 16 * (r >> 6);
+        const int f = mt * 64 + fl;
         const int fo = (f & ~7) | k8_pos(f & 7);  // FC2 meets it in the decode's K order
-        for (int c0 = 0; c0 < n16; c0 += 32, xb ^= 1) {
+        const float* xg = xchg + fl * 33;             // gate sums of feature fl
+        const float* xu = xchg + (64 + fl) * 33;      // up sums of feature fl
+        float* mine = xchg + r * 33;
+        for (int c0 = 0; c0 < n16; c0 += 32) {
           float v[32];
           tmem_ld16(acc + c0, *reinterpret_cast<float(*)[16]>(v));
           if (c0 + 16 < n16) tmem_ld16(acc + c0 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
@@ -475,27 +484,24 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
             for (int j = 0; j < 32; ++j) v[j] = __fadd_rn(v[j], w[j]);
           }
           tmem_wait_ld();
-          float* xrow = xchg + xb * (64 * 33) + (r & 63) * 33;
           const int ncol = min(32, n16 - c0);
-          if (!gate) {
-            for (int j = 0; j < ncol; ++j) xrow[j] = __fmul_rn(v[j], alpha);
-          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < ncol) mine[j] = __fmul_rn(v[j], alpha);
           named_bar_sync(1, 128);
-          if (gate) {
-            for (int j = 0; j < ncol; ++j) {
-              const int col = c0 + j;
-              if (col >= rows) break;
-              const size_t p = (size_t)row0 + col;
-              float yg = __fmul_rn(v[j], alpha);
-              float yu = xrow[j];
-              if (a.swiglu_limit > 0.0f) {  // clamped SwiGLU: cap the gate, clip the up value
-                yg = fminf(yg, a.swiglu_limit);
-                yu = fmaxf(fminf(yu, a.swiglu_limit), -a.swiglu_limit);
-              }
-              const float act = __fmul_rn(__fdiv_rn(yg, __fadd_rn(1.0f, expf(-yg))), yu);
-              a.route_out[p * a.I + fo] = __bfloat16_as_ushort(__float2bfloat16_rn(act));
+          const int jend = min(j0 + 16, min(ncol, rows - c0));
+          for (int j = j0; j < jend; ++j) {
+            const size_t p = (size_t)row0 + c0 + j;
+            float yg = xg[j];
+            float yu = xu[j];
+            if (a.swiglu_limit > 0.0f) {  // clamped SwiGLU: cap the gate, clip the up value
+              yg = fminf(yg, a.swiglu_limit);
+              yu = fmaxf(fminf(yu, a.swiglu_limit), -a.swiglu_limit);
             }
+            const float act = __fmul_rn(__fdiv_rn(yg, __fadd_rn(1.0f, expf(-yg))), yu);
+            a.route_out[p * a.I + fo] = __bfloat16_as_ushort(__float2bfloat16_rn(act));
           }
+          named_bar_sync(1, 128);  // the chunk's sums are read before the next one lands
         }
       } else {
         for (int c0 = 0; c0 < n16; c0 += 16) {
