@@ -75,6 +75,29 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+# Nominal dense tensor rates relative to bf16 (2.25 PFLOP/s): FP4 13.5, so x6.
+FP4_OVER_BF16 = 6.0
+FALLBACK_BF16_SUSTAINED_TFLOPS = 1700.0
+
+
+def fp4_peak():
+    """Dense NVFP4 tensor peak in TFLOP/s: the measured sustained bf16 GEMM rate
+    (the GEMMs run inside a step of several launches) times the nominal
+    FP4 / bf16 ratio."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops_sustained"]) * FP4_OVER_BF16, "measured bf16 sustained x 6"
+    return FALLBACK_BF16_SUSTAINED_TFLOPS * FP4_OVER_BF16, "fallback bf16 sustained x 6"
+
+
+def algorithmic_flops(wl, R):
+    """Routed work of the two grouped GEMMs: 2 R H N1 (FC1) and 2 R I H (FC2)."""
+    N1 = 2 * wl.I if wl.act == "swiglu" else wl.I
+    return {"fc1": 2.0 * R * wl.H * N1, "fc2": 2.0 * R * wl.I * wl.H}
+
+
 def kernel_hash():
     h = hashlib.sha256()
     for f in ("gemm_w4a4.cu", "gemm_common.cuh", "ptx.cuh", "internal.h"):
@@ -487,6 +510,18 @@ def run_ours(args, rank, world, local_rank):
     hbm, src = peaks()
     achieved = kernel_bytes / (fc1_mean * 1e-3) / 1e9
     layer_gbs = B["layer"] / (ms_per_step * 1e-3) / 1e9
+    # Bound of the kernel (and of the layer): the larger of its FLOPs at the
+    # dense tensor peak of its input type and its bytes at the HBM rate.
+    F = algorithmic_flops(wl, R)
+    tpeak, tsrc = fp4_peak()
+    if args.w4a16:
+        tpeak, tsrc = tpeak / FP4_OVER_BF16, tsrc.replace(" x 6", "")
+    kernel_flops = F["fc1"] + (F["fc2"] if fused else 0)
+    layer_flops = F["fc1"] + F["fc2"]
+    kernel_tensor = kernel_flops / (tpeak * 1e12) > kernel_bytes / (hbm * 1e9)
+    layer_tensor = layer_flops / (tpeak * 1e12) > B["layer"] / (hbm * 1e9)
+    kernel_tflops = kernel_flops / (fc1_mean * 1e-3) / 1e12
+    layer_tflops = layer_flops / (ms_per_step * 1e-3) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -501,19 +536,31 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"kernel": ("fc1 grouped GEMM (gemm_w4a16_kernel<SwiGLU|ReLU2>)" if args.w4a16
                                 else "fused FC1 + requant + FC2 (gemm_w4a4_kernel, one launch)"
                                 if fused else "fc1 grouped GEMM (gemm_w4a4_kernel<SwiGLU|ReLU2>)"),
-                     "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "peak_source": src,
+                     **({"bound": "tensor", "achieved": kernel_tflops, "peak": tpeak,
+                         "unit": "TFLOP/s", "frac": kernel_tflops / tpeak, "peak_source": tsrc,
+                         "hbm_gbs": achieved, "hbm_frac": achieved / hbm}
+                        if kernel_tensor else
+                        {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "peak_source": src,
+                         "tflops": kernel_tflops, "tensor_frac": kernel_tflops / tpeak}),
+                     "algorithmic_flops": kernel_flops,
                      "traffic": None if fused else traffic_for(wl.name),
                      "algorithmic_bytes": kernel_bytes,
                      "workspace_bytes": B["workspace"],
                      "kernel_us": fc1_mean * 1e3, "fc2_kernel_us": fc2_mean * 1e3,
                      "fc2_frac": (None if fused else
                                   B["fc2"] / (fc2_mean * 1e-3) / 1e9 / hbm),
+                     "fc2_tensor_frac": (None if fused else
+                                         F["fc2"] / (fc2_mean * 1e-3) / 1e12 / tpeak),
                      "timing": "CUDA events recorded by the library around the FC1 launch, "
                                "over a second pass of the same K steps"},
-        "layer_roofline": {"bound": "hbm", "algorithmic_bytes": B["layer"],
-                           "achieved": layer_gbs, "peak": hbm, "unit": "GB/s",
-                           "frac": layer_gbs / hbm},
+        "layer_roofline": ({"bound": "tensor", "algorithmic_flops": layer_flops,
+                            "achieved": layer_tflops, "peak": tpeak, "unit": "TFLOP/s",
+                            "frac": layer_tflops / tpeak, "hbm_frac": layer_gbs / hbm}
+                           if layer_tensor else
+                           {"bound": "hbm", "algorithmic_bytes": B["layer"],
+                            "achieved": layer_gbs, "peak": hbm, "unit": "GB/s",
+                            "frac": layer_gbs / hbm, "tensor_frac": layer_tflops / tpeak}),
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         # the forward's own count (moe_nvfp4_forward_kernel_count) plus the token

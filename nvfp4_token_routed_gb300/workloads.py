@@ -61,8 +61,15 @@ PAGES_E384 = Workload("swiglu_H7168_I3072_E384_K6", 512, 7168, 3072, 384, 6, "sw
 PAGES_GB300_RELU2 = Workload("relu2_H7168_I2048_E256_K8", 128, 7168, 2048, 256, 8, "relu2",
                              x_dist="normal")
 
+# A compute-regime probe outside the pages' workloads: 8 experts of the
+# H7168 / I2048 SwiGLU layer, top-2 of uniform routing over 65536 tokens gives
+# ~16k routes per expert, far past the ~530 at which the grouped GEMMs stop
+# being weight-streaming bound, so it measures the tensor pipe.
+COMPUTE_PROBE = Workload("swiglu_H7168_I2048_E8_K2_compute", 65536, 7168, 2048, 8, 2, "swiglu",
+                         x_dist="normal", routing="uniform")
+
 ALL = {w.name: w for w in [TINY_RELU2, SWIGLU_E64, MID_ZIPF, DSV3_LIKE, PAGES_E384,
-                             PAGES_GB300_RELU2]}
+                             PAGES_GB300_RELU2, COMPUTE_PROBE]}
 
 
 def _gen(seed, device):
