@@ -115,12 +115,16 @@ typedef struct {
   size_t perm;           /* int32[rows_cap] route id t*K+k of a valid row   */
   size_t xq_codes;       /* W4A4: u8[rows_cap][Hp/2] permuted token codes   */
   size_t xq_sf;          /* W4A4: u8 swizzled over permuted rows, Hp/16 cols */
-  size_t xq_scale;       /* W4A4: f32[rows_cap] per-row token scale        */
+  size_t xq_scale;       /* f32[rows_cap] per-row token scale: W4A4 the
+                            NVFP4 row scale; W4A16 the power of two 2^k
+                            that x_perm's row was divided by              */
   size_t act;            /* W4A4: f32[rows_cap][Ip] activated FC1 rows      */
   size_t fc2q_codes;     /* W4A4: u8[rows_cap][Ip/2] requantized FC2 input  */
   size_t fc2q_sf;        /* W4A4: u8 swizzled over permuted rows, Ip/16 cols */
   size_t fc2q_scale;     /* W4A4: f32[rows_cap] FC2-input row scale s2      */
-  size_t x_perm;         /* W4A16: bf16[rows_cap][Hp] permuted token rows   */
+  size_t x_perm;         /* W4A16: f16[rows_cap][Hp] permuted token rows,
+                            each bf16 row times 2^-k (k from its largest
+                            magnitude, which lands in [2^14, 2^15))        */
   size_t act_bf16;       /* W4A16: bf16[rows_cap][Ip] activated FC1 rows    */
   size_t route;          /* bf16[rows_cap][Hp] per-route FC2 rows           */
   size_t tile_sync;      /* int32[2][rows_cap/128] then f32[rows_cap]: per
@@ -131,7 +135,7 @@ typedef struct {
 } moe_ws_layout;
 
 /* ABI version of this header (bumped on any incompatible change). */
-#define MOE_NVFP4_ABI_VERSION 2
+#define MOE_NVFP4_ABI_VERSION 3
 int32_t moe_nvfp4_abi_version(void);
 
 /* Human-readable text of a status code (static storage). */

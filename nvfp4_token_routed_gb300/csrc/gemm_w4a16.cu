@@ -7,20 +7,34 @@
 // E2M1 x E4M3 to BF16, accumulate in FP32, then apply the expert alpha; FC1's
 // activation comes before a BF16 handoff; FC2 applies alpha before BF16 output.
 //
+// Operand types: FC1 multiplies in f16 and FC2 in bf16, with the same exact
+// products.  The decoded weights (code x scale: at most 6 significant bits,
+// between 2^-10 and 2688) are exact in both.  FC1's token rows arrive in f16
+// from the gather, each bf16 row times a power of two 2^-k that puts its
+// largest magnitude in [2^14, 2^15), so every value down to 2^-28 of the row's
+// largest is exact; the epilogue multiplies by 2^k.  Scaling a row by a power
+// of two changes no rounding of the fp32 accumulation, so the result is that
+// of the bf16 product.  f16 is chosen for FC1 because the conversion
+// instructions decode E2M1 and E4M3 to f16 directly: about 15 cycles per eight
+// codes and sub-partition against 26 for the integer decode to bf16 that FC2's
+// bf16 handoff rows need (whose range an f16 row would need a scale for, and
+// FC1 items only see 64 or 128 features of a row).
+//
 // Structure (swap-AB as in the W4A4 kernel; weights are the M=128 operand and
 // are decoded on chip, never written back to global or shared memory):
 //   * warp 0: weight producer -- claims items and streams packed E2M1 weight
 //     slots (128 rows x 128 B = 256 K elements, 128-byte swizzle, so each row is
 //     read in 128-byte runs) with their E4M3 scale atoms (bulk copy)
 //   * the last warp: token producer -- one 3-D tiled copy per 256-K block: four
-//     64-element K chunks of the tile's bf16 rows (128-byte swizzle), chunk-major,
-//     in the smallest 16/32/64/128-row box that covers the tile
+//     64-element K chunks of the tile's 16-bit rows (128-byte swizzle),
+//     chunk-major, in the smallest 16/32/64/128-row box that covers the tile
 //   * warps 6..5+kDecodeWarps: decode -- kDecodeWarps/4 warps per TMEM lane
 //     quadrant; thread r of quadrant q owns weight row 32q+r: for each 128-K
 //     half of a packed slot its warps read the packed bytes and their scales
-//     from shared memory, form exact bf16 values of code x scale x 2^-8 with
-//     integer and bf16x2 instructions only (decode8_bf16; the epilogue's alpha
-//     carries the 2^8) and write them into a TMEM A slot (lane = row, 2 K
+//     from shared memory, form exact values of code x scale (FC1: f16 by the
+//     conversion instructions, decode8_f16) or code x scale x 2^-8 (FC2: bf16
+//     by integer and bf16x2 instructions only, decode8_bf16; the epilogue's
+//     alpha carries the 2^8) and write them into a TMEM A slot (lane = row, 2 K
 //     elements per column); the packed slot is released once read
 //   * warp 1 (also the TMEM allocator) and warp 6+kDecodeWarps: MMA issuers --
 //     tcgen05.mma.kind::f16 with A from TMEM and B from shared memory, K = 16
@@ -28,8 +42,9 @@
 //     issues the even K steps into one partial sum, the second the odd ones
 //     into another, each from a whole warp with elect.sync (a single-lane loop
 //     is bound by issue latency at small N)
-//   * warps 2-5: epilogue (alpha, activation, bf16 rounding), one TMEM lane per
-//     thread; SwiGLU pairs gate and up rows through shared memory as in W4A4
+//   * warps 2-5: epilogue (alpha, FC1's row scales 2^k, activation, bf16
+//     rounding), one TMEM lane per thread; SwiGLU pairs gate and up rows through
+//     shared memory as in W4A4
 //   * rings: packed-weight slots (4-9 of 18 KB, as many as shared memory holds
 //     next to a few token stages, each released as soon as the decode warps have
 //     read it into registers), TMEM slots of decoded weights (3 blocks of 256 K)
@@ -115,6 +130,7 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
   const ItemQueue Q{reinterpret_cast<int4*>(smem + kRingOff), R.bar(kBarItemFull),
                     R.bar(kBarItemEmpty)};
   float* xchg = reinterpret_cast<float*>(smem + kBarBytes);
+  float* s_rs = reinterpret_cast<float*>(smem + 1024);  // FC1: row scales of the current tile (128)
   uint8_t* rings = smem + kBarBytes + kXchgBytes;     // 1024-aligned
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -340,11 +356,19 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
             const int c = kChunksPerWarp * wq + cc;        // chunk within the half
             const uint4 raw = raws[h][cc];
             uint32_t sc0, sc1;
-            e4m3x2_scale_bf16x2(sw[h] >> (16 * (c & 1)), sc0, sc1);
-            decode8_bf16(raw.x, sc0, o[h][cc]);
-            decode8_bf16(raw.y, sc0, o[h][cc] + 4);
-            decode8_bf16(raw.z, sc1, o[h][cc] + 8);
-            decode8_bf16(raw.w, sc1, o[h][cc] + 12);
+            if constexpr (MODE == kFc2) {
+              e4m3x2_scale_bf16x2(sw[h] >> (16 * (c & 1)), sc0, sc1);
+              decode8_bf16(raw.x, sc0, o[h][cc]);
+              decode8_bf16(raw.y, sc0, o[h][cc] + 4);
+              decode8_bf16(raw.z, sc1, o[h][cc] + 8);
+              decode8_bf16(raw.w, sc1, o[h][cc] + 12);
+            } else {
+              e4m3x2_scale_f16x2(sw[h] >> (16 * (c & 1)), sc0, sc1);
+              decode8_f16(raw.x, sc0, o[h][cc]);
+              decode8_f16(raw.y, sc0, o[h][cc] + 4);
+              decode8_f16(raw.z, sc1, o[h][cc] + 8);
+              decode8_f16(raw.w, sc1, o[h][cc] + 12);
+            }
           }
         }
         // the TMEM slot's previous MMAs are done
@@ -387,7 +411,8 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
       const TileInfo cur = queue_pop_warp(Q, qp, abort_flag, a.status);
       if (cur.rows == 0) break;
       const int n16 = (cur.rows + 15) & ~15;
-      const uint32_t idesc = idesc_bf16(128, n16);
+      // FC1: f16 weights and f16 token rows; FC2: bf16 weights and bf16 rows
+      const uint32_t idesc = MODE == kFc2 ? idesc_bf16(128, n16) : idesc_f16(128, n16);
       const int chunk_bytes = box_rows(n16) * kChunkRowBytes;  // this tile's chunk stride
       const int buf = local % nbuf;
       const uint32_t acc_par = ((uint32_t)(local / nbuf) & 1u) ^ 1u;
@@ -446,11 +471,16 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
       const int row0 = cur.tt * kTileRows;
       const int buf = local % nbuf;
       const uint32_t acc_par = (uint32_t)(local / nbuf) & 1u;
-      // the decoded weights carry a factor 2^-8 (exactly undone here)
-      const float alpha = rows ? a.alpha[cur.e] * kDecodeUnscale : 0.0f;
+      // FC2: the bf16-decoded weights carry a factor 2^-8 (exactly undone here).
+      // FC1: each token column was multiplied by a power of two 2^-k when its
+      // f16 row was formed; 2^k, the row scale, undoes it exactly.
+      const float alpha = rows ? a.alpha[cur.e] * (MODE == kFc2 ? kDecodeUnscale : 1.0f) : 0.0f;
+      const float rs = MODE != kFc2 && r < rows ? a.row_scale[(size_t)row0 + r] : 0.0f;
       if (rows == 0 || !wait_or_abort(R.bar(kBarAccFull + buf), acc_par, abort_flag, a.status))
         *epi_stop = 1;
       named_bar_sync(1, 128);
+      // every thread is past the previous tile's reads of s_rs
+      if constexpr (MODE != kFc2) s_rs[r] = rs;
       const bool stop = *epi_stop != 0;
       named_bar_sync(1, 128);
       if (stop) break;
@@ -487,7 +517,7 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
           const int ncol = min(32, n16 - c0);
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (j < ncol) mine[j] = __fmul_rn(v[j], alpha);
+            if (j < ncol) mine[j] = __fmul_rn(__fmul_rn(v[j], alpha), s_rs[c0 + j]);
           named_bar_sync(1, 128);
           const int jend = min(j0 + 16, min(ncol, rows - c0));
           for (int j = j0; j < jend; ++j) {
@@ -520,12 +550,13 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
             const int col = c0 + j;
             if (col >= rows) break;
             const size_t p = (size_t)row0 + col;
-            const float y = __fmul_rn(v[j], alpha);
             if constexpr (MODE == kFc1Relu2) {
+              const float y = __fmul_rn(__fmul_rn(v[j], alpha), s_rs[col]);
               const float t = fmaxf(y, 0.0f);
               a.route_out[p * a.I + mt * 128 + (r & ~7) + k8_pos(r & 7)] =
                   __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(t, t)));
             } else {
+              const float y = __fmul_rn(v[j], alpha);
               a.route_out[p * a.H + mt * 128 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
             }
           }

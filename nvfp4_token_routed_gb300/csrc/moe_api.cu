@@ -117,6 +117,7 @@ void compute_layout(const moe_dims* d, int32_t T, int32_t K, int32_t w4a16, moe_
     L->fc2q_scale = take(sizeof(float) * rows);
   } else {
     L->x_perm = take(sizeof(uint16_t) * (size_t)rows * H);
+    L->xq_scale = take(sizeof(float) * rows);
     L->act_bf16 = take(sizeof(uint16_t) * (size_t)rows * I);
   }
   L->route = take(sizeof(uint16_t) * (size_t)rows * H);
@@ -581,6 +582,7 @@ static moe_status forward_w4a16_impl(const moe_dims* d, const moe_nvfp4_weights*
   RouteArgs r = route_args(d, T, K, topk_ids, o.ids_int64, ws, L, 1);
   r.xb = x_bf16;
   r.pb = at<uint8_t>(ws, L.x_perm);
+  r.ps = at<float>(ws, L.xq_scale);
   if (launch_route(r, s) != cudaSuccess) return MOE_ERR_CUDA;
   mark(1, s);
 
@@ -592,6 +594,7 @@ static moe_status forward_w4a16_impl(const moe_dims* d, const moe_nvfp4_weights*
   g.w_rows = N1;
   g.sfa = w->fc1_sf;
   g.alpha = w->fc1_alpha;
+  g.row_scale = at<float>(ws, L.xq_scale);
   g.tiles = at<int4>(ws, L.tiles);
   g.status = at<int32_t>(ws, L.status);
   g.item_counter = g.status + kStatusItemCtr;

@@ -3,6 +3,7 @@
 // scan, scatter + gather), the FC2-input requantization and the deterministic
 // top-k finalize.  Every kernel moves data in 16-byte vectors, one warp per row.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -379,8 +380,13 @@ __global__ void __launch_bounds__(kChunk) route_scatter_kernel(
 
 // Row gather of one route (one warp): the token's quantized row and its block
 // scales (W4A4; rows already padded to Hp by the quantizer) or its bf16 row
-// with the Hp - H padding columns zeroed (W4A16, each group of 8 values in the
-// K order 0,4,1,5,2,6,3,7 of the decoded weights) into permuted row p.
+// (W4A16) into permuted row p.  W4A16 rows go to the FC1 GEMM as f16, which it
+// multiplies with f16-decoded weights: the row is multiplied by 2^-k, k chosen
+// from its largest magnitude so that it lands in [2^14, 2^15), and 2^k is the
+// row's scale.  Every bf16 value of magnitude at least 2^-14 after the scaling
+// (all within 2^28 of the row's largest) is exact in f16; smaller ones round to
+// f16's subnormal step, far below the fp32 accumulation's own rounding.  The
+// Hp - H padding columns are zeroed.
 struct GatherArgs {
   int K, H, Hp;
   const uint8_t* xc;
@@ -398,9 +404,37 @@ __device__ __forceinline__ void gather_route_row(const GatherArgs& g, int idx, i
   if constexpr (kW4A16) {
     const uint4* src = g.xb + (size_t)t * (g.H / 8);
     uint4* dst = g.pb + (size_t)p * (g.Hp / 8);
-    // in the K order of the decoded weights it meets in the W4A16 GEMM
-    for (int i = lane; i < g.H / 8; i += 32) dst[i] = k8_order(__ldg(src + i));
+    // largest magnitude (bf16 bits without the sign order like the magnitudes;
+    // halves compared separately)
+    uint32_t m = 0;
+    for (int i = lane; i < g.H / 8; i += 32) {
+      const uint4 v = __ldg(src + i);
+      m = __vmaxu2(m, __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                               __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu)));
+    }
+    uint32_t mx = max(m & 0xFFFFu, m >> 16);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    // amax in [2^(e-127), 2^(e-126)) for biased exponent e: k = e - 141; no
+    // scaling for a zero row or an Inf/NaN; 2^-k kept a normal fp32
+    const int e = (int)(mx >> 7);
+    const int k = (mx == 0 || e == 255) ? 0 : max(e - 141, -126);
+    const float down = __uint_as_float((uint32_t)(127 - k) << 23);
+    for (int i = lane; i < g.H / 8; i += 32) {
+      const uint4 v = __ldg(src + i);
+      const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+      uint32_t out[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float lo = __fmul_rn(__uint_as_float(in[j] << 16), down);
+        const float hi = __fmul_rn(__uint_as_float(in[j] & 0xFFFF0000u), down);
+        const __half2 h = __floats2half2_rn(lo, hi);
+        out[j] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      dst[i] = make_uint4(out[0], out[1], out[2], out[3]);
+    }
     for (int i = g.H / 8 + lane; i < g.Hp / 8; i += 32) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (lane == 0) g.ps[p] = __uint_as_float((uint32_t)(127 + k) << 23);
   } else {
     const uint4* src = reinterpret_cast<const uint4*>(g.xc + (size_t)t * (g.Hp / 2));
     uint4* dst = reinterpret_cast<uint4*>(g.pc + (size_t)p * (g.Hp / 2));

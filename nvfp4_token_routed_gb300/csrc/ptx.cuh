@@ -243,6 +243,16 @@ __device__ __forceinline__ uint32_t idesc_bf16(uint32_t M, uint32_t N) {
   return d;
 }
 
+// Instruction descriptor of kind::f16 with f16 A/B and fp32 accumulate (A and B
+// format fields 0 = f16).
+__device__ __forceinline__ uint32_t idesc_f16(uint32_t M, uint32_t N) {
+  uint32_t d = 0;
+  d |= 1u << 4;   // D format: f32
+  d |= ((N >> 3) & 0x3F) << 17;
+  d |= ((M >> 4) & 0x1F) << 24;
+  return d;
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T with 1x16 UE4M3 block scales read from TMEM.
 __device__ __forceinline__ void mma_mxf4nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                              uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
@@ -378,8 +388,8 @@ __device__ __forceinline__ uint32_t cvt_e4m3(float v) {
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(out) : "f"(v), "f"(v));
   return out & 0xFFu;
 }
-// Decoding NVFP4 weights to bf16 without conversion instructions (the
-// conversion pipe is a small fraction of the integer and FMA pipes):
+// Decoding NVFP4 weights to bf16 (PTX converts E2M1 and E4M3 to f16 only) with
+// integer and bf16x2 instructions:
 //   * an E2M1 code c = s e1 e0 m0 written as the bf16 bits s<<15 | (c & 7)<<6
 //     reads as its E2M1 value x 2^-126 -- the exponent field is e1e0 and the top
 //     mantissa bit m0, and E2M1's subnormal (0.5) lands on a bf16 subnormal of
@@ -424,6 +434,29 @@ __device__ __forceinline__ void decode8_bf16(uint32_t w, uint32_t scale, uint32_
   asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[1]) : "r"(x1), "r"(scale));
   asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[2]) : "r"(x2), "r"(scale));
   asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[3]) : "r"(x3), "r"(scale));
+}
+
+// Decoding NVFP4 weights to f16 with the conversion instructions: E2M1 and
+// UE4M3 values are f16 normals (or zero), and code x scale has at most 6
+// significant bits between 2^-10 and 2688, so the f16 product is exact.
+// Two UE4M3 bytes (low 16 bits of b, first in the low byte) -> f16x2 words
+// holding the first (s0) and the second (s1) scale in both halves.
+__device__ __forceinline__ void e4m3x2_scale_f16x2(uint32_t b, uint32_t& s0, uint32_t& s1) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((uint16_t)(b & 0xFFFFu)));
+  s0 = __byte_perm(h, 0, 0x1010);
+  s1 = __byte_perm(h, 0, 0x3232);
+}
+// 8 E2M1 codes (one 32-bit word, code j in nibble j) -> 4 f16x2 words of
+// code x scale in natural K order: word i holds codes 2i (low half) and 2i + 1.
+__device__ __forceinline__ void decode8_f16(uint32_t w, uint32_t scale, uint32_t* o) {
+  asm("{\n .reg .b8 t0, t1, t2, t3;\n mov.b32 {t0, t1, t2, t3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, t0;\n cvt.rn.f16x2.e2m1x2 %1, t1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, t2;\n cvt.rn.f16x2.e2m1x2 %3, t3;\n}"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(w));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(o[i]) : "r"(scale));
 }
 
 // Position of element i (0..7) of a group of 8 in the K order that decode8_bf16

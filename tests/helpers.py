@@ -49,9 +49,9 @@ def unpack_codes(packed):
     return np.stack([packed & 15, packed >> 4], axis=-1).reshape(*packed.shape[:-1], -1)
 
 
-# K order of each group of 8 values in the W4A16 GEMM's bf16 operands (the order
-# in which the GEMM decodes a 32-bit word of eight E2M1 codes): the permuted
-# token rows (x_perm) and the bf16 activated rows (act_bf16) are stored so.
+# K order of each group of 8 values in the W4A16 FC2 GEMM's bf16 operands (the
+# order in which it decodes a 32-bit word of eight E2M1 codes to bf16): the bf16
+# activated rows (act_bf16) are stored so.
 K8_ORDER = np.array([0, 4, 1, 5, 2, 6, 3, 7])
 
 

@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert M.moe_nvfp4_abi_version() == 2
+    assert M.moe_nvfp4_abi_version() == 3
     for code in range(9):
         assert M.moe_nvfp4_status_string(code)
     assert M.moe_nvfp4_status_string(5).startswith("unsupported device")

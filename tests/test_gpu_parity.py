@@ -208,8 +208,20 @@ def test_w4a16_permuted_rows_and_routing(name):
     rmap = _rows_map(g, o)
     perm = g.view("perm", torch.int32, (g.L["rows_cap"],))
     assert np.array_equal(perm[rmap], o.res["perm"])
-    xp = g.view("x_perm", torch.int16, (g.L["rows_cap"], wl.H))[rmap].view(np.uint16)
-    assert np.array_equal(from_k8_order(xp), to_np_u16(x)[o.res["perm"] // wl.K])
+    # f16 rows, each the bf16 row times 2^-k with its largest magnitude in
+    # [2^14, 2^15); 2^k is the row scale.  Exact down to f16's normal range,
+    # within half an f16 subnormal step below it.
+    xp = g.view("x_perm", torch.int16, (g.L["rows_cap"], wl.H))[rmap].view(np.float16)
+    rs = g.view("xq_scale", torch.float32, (g.L["rows_cap"],))[rmap].astype(np.float64)
+    want = bf16_np(to_np_u16(x)[o.res["perm"] // wl.K]).astype(np.float64)
+    amax = np.abs(want).max(axis=1)
+    assert np.all(rs == 2.0 ** (np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 14)
+                  * (amax > 0) + (amax == 0))
+    assert np.all(np.abs(want / rs[:, None]).max(axis=1) < 2.0 ** 15)
+    got = xp.astype(np.float64) * rs[:, None]
+    normal = np.abs(want) >= rs[:, None] * 2.0 ** -14
+    assert np.array_equal(got[normal], want[normal])
+    assert np.all(np.abs(got - want)[~normal] <= (rs[:, None] * 2.0 ** -25 * np.ones_like(want))[~normal])
 
 
 @pytest.mark.parametrize("name", list(CASES))
