@@ -207,7 +207,9 @@ def algorithmic_bytes(wl, R, U, w4a16=False):
         fc1 = w1 + 2 * T * H + 2 * R * I
         fc2 = w2 + 2 * R * I + 2 * R * H
         layer = w1 + w2 + 2 * T * H + 2 * 2 * R * I + 4 * R * H + 2 * T * H + 8 * T * K
-        ws = 2 * 2 * R * H                               # permuted bf16 rows: written, read
+        # the f16 copies of the token rows (written, read) and of the handoff
+        # rows (the bf16 rows read twice by the conversion, the f16 rows written)
+        ws = 2 * 2 * R * H + 3 * 2 * R * I
     else:
         fc1 = w1 + T * H * 9 / 16 + R * I * 9 / 16
         fc2 = w2 + R * I * 9 / 16 + 2 * R * H

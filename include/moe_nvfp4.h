@@ -125,13 +125,18 @@ typedef struct {
   size_t x_perm;         /* W4A16: f16[rows_cap][Hp] permuted token rows,
                             each bf16 row times 2^-k (k from its largest
                             magnitude, which lands in [2^14, 2^15))        */
-  size_t act_bf16;       /* W4A16: bf16[rows_cap][Ip] activated FC1 rows    */
+  size_t act_bf16;       /* W4A16: bf16[rows_cap][Ip] activated FC1 rows
+                            (the bf16 handoff)                              */
   size_t route;          /* bf16[rows_cap][Hp] per-route FC2 rows           */
   size_t tile_sync;      /* int32[2][rows_cap/128] then f32[rows_cap]: per
                             token tile the FC1 items stored and the FC2-input
                             ready flag, per row the activated row's amax, of
                             the one-launch FC1 -> FC2 path, taken when
                             T*K <= min(2048, 8*E)                           */
+  size_t act_f16;        /* W4A16: f16[rows_cap][Ip] act_bf16's rows times
+                            2^-k, k from each row's largest magnitude, which
+                            lands in [2^14, 2^15) (the FC2 GEMM's operand)  */
+  size_t act_scale;      /* W4A16: f32[rows_cap] 2^k of each act_f16 row    */
 } moe_ws_layout;
 
 /* ABI version of this header (bumped on any incompatible change). */
@@ -173,7 +178,8 @@ size_t moe_nvfp4_workspace_bytes(const moe_dims* d, int32_t T_max, int32_t K, in
  * moe_nvfp4_forward_w4a16 (w4a16 = 1) call launches for T tokens with top-K:
  * routing and the row gather (one kernel up to 32 routes, two up to 2048,
  * four beyond), the grouped GEMMs (W4A4: one launch when T*K <= min(2048, 8*E), else FC1, the
- * FC2-input requant and FC2; W4A16: FC1 and FC2) and the finalize; 0 for
+ * FC2-input requant and FC2; W4A16: FC1, the conversion of the bf16 handoff
+ * rows to the f16 FC2 operand, and FC2) and the finalize; 0 for
  * T == 0.  Host only, no device work.  Returns -1 for invalid arguments. */
 int32_t moe_nvfp4_forward_kernel_count(const moe_dims* d, int32_t T, int32_t K, int32_t w4a16);
 

@@ -44,7 +44,7 @@ class moe_nvfp4_weights(C.Structure):
 _LAYOUT_FIELDS = ["total", "rows_cap", "status", "counts", "group_row0", "tiles",
                   "chunk_counts", "chunk_prefix", "inv", "perm", "xq_codes", "xq_sf",
                   "xq_scale", "act", "fc2q_codes", "fc2q_sf", "fc2q_scale", "x_perm", "act_bf16",
-                  "route", "tile_sync"]
+                  "route", "tile_sync", "act_f16", "act_scale"]
 
 
 class moe_forward_opts(C.Structure):

@@ -7,18 +7,17 @@
 // E2M1 x E4M3 to BF16, accumulate in FP32, then apply the expert alpha; FC1's
 // activation comes before a BF16 handoff; FC2 applies alpha before BF16 output.
 //
-// Operand types: FC1 multiplies in f16 and FC2 in bf16, with the same exact
-// products.  The decoded weights (code x scale: at most 6 significant bits,
-// between 2^-10 and 2688) are exact in both.  FC1's token rows arrive in f16
-// from the gather, each bf16 row times a power of two 2^-k that puts its
-// largest magnitude in [2^14, 2^15), so every value down to 2^-28 of the row's
-// largest is exact; the epilogue multiplies by 2^k.  Scaling a row by a power
-// of two changes no rounding of the fp32 accumulation, so the result is that
-// of the bf16 product.  f16 is chosen for FC1 because the conversion
-// instructions decode E2M1 and E4M3 to f16 directly: about 15 cycles per eight
-// codes and sub-partition against 26 for the integer decode to bf16 that FC2's
-// bf16 handoff rows need (whose range an f16 row would need a scale for, and
-// FC1 items only see 64 or 128 features of a row).
+// Operand types: both GEMMs multiply in f16, with the products of the bf16
+// contract.  The decoded weights (code x scale: at most 6 significant bits,
+// between 2^-10 and 2688) are exact in f16.  The bf16 rows (FC1: the token
+// rows, from the gather; FC2: the bf16 handoff rows, converted after FC1) arrive
+// in f16, each times a power of two 2^-k that puts its largest magnitude in
+// [2^14, 2^15), so every value down to 2^-28 of the row's largest is exact; the
+// epilogue multiplies by 2^k.  Scaling a row by a power of two changes no
+// rounding of the fp32 accumulation, so the result is that of the bf16
+// product.  f16 is chosen because the conversion instructions decode E2M1 and
+// E4M3 to f16 directly: about 15 cycles per eight codes and SM sub-partition,
+// against 26 for an integer decode to bf16 (measured on GB300).
 //
 // Structure (swap-AB as in the W4A4 kernel; weights are the M=128 operand and
 // are decoded on chip, never written back to global or shared memory):
@@ -31,18 +30,17 @@
 //   * warps 6..5+kDecodeWarps: decode -- kDecodeWarps/4 warps per TMEM lane
 //     quadrant; thread r of quadrant q owns weight row 32q+r: for each 128-K
 //     half of a packed slot its warps read the packed bytes and their scales
-//     from shared memory, form exact values of code x scale (FC1: f16 by the
-//     conversion instructions, decode8_f16) or code x scale x 2^-8 (FC2: bf16
-//     by integer and bf16x2 instructions only, decode8_bf16; the epilogue's
-//     alpha carries the 2^8) and write them into a TMEM A slot (lane = row, 2 K
-//     elements per column); the packed slot is released once read
+//     from shared memory, form the exact f16 values of code x scale with the
+//     conversion instructions (decode8_f16) and write them into a TMEM A slot
+//     (lane = row, 2 K elements per column); the packed slot is released once
+//     read
 //   * warp 1 (also the TMEM allocator) and warp 6+kDecodeWarps: MMA issuers --
 //     tcgen05.mma.kind::f16 with A from TMEM and B from shared memory, K = 16
 //     per instruction, N = the tile's token count rounded up to 16; the first
 //     issues the even K steps into one partial sum, the second the odd ones
 //     into another, each from a whole warp with elect.sync (a single-lane loop
 //     is bound by issue latency at small N)
-//   * warps 2-5: epilogue (alpha, FC1's row scales 2^k, activation, bf16
+//   * warps 2-5: epilogue (alpha, the row scales 2^k, activation, bf16
 //     rounding), one TMEM lane per thread; SwiGLU pairs gate and up rows through
 //     shared memory as in W4A4
 //   * rings: packed-weight slots (4-9 of 18 KB, as many as shared memory holds
@@ -72,7 +70,7 @@ constexpr int kSfaBytes = 4 * kAtom;        // 4 K-atoms (4 scale columns each)
 constexpr int kRawSlotBytes = kRawBytes + kSfaBytes;
 constexpr int kBK = kRawK;                  // K elements per token stage / decoded TMEM slot
 constexpr int kChunks = kBK / 64;           // 64-element (128-byte) K chunks per token stage
-constexpr int kChunkRowBytes = 128;         // 64 bf16 per row per K chunk
+constexpr int kChunkRowBytes = 128;         // 64 f16 per row per K chunk
 constexpr int kACols = kBK / 2;             // TMEM columns of one decoded A slot
 constexpr int kMaxRaw = 10;                 // packed-weight slots (released once read)
 constexpr int kMaxRing = 3;                 // TMEM slots of decoded A (blocks being decoded / multiplied)
@@ -130,7 +128,7 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
   const ItemQueue Q{reinterpret_cast<int4*>(smem + kRingOff), R.bar(kBarItemFull),
                     R.bar(kBarItemEmpty)};
   float* xchg = reinterpret_cast<float*>(smem + kBarBytes);
-  float* s_rs = reinterpret_cast<float*>(smem + 1024);  // FC1: row scales of the current tile (128)
+  float* s_rs = reinterpret_cast<float*>(smem + 1024);  // row scales of the current tile (128)
   uint8_t* rings = smem + kBarBytes + kXchgBytes;     // 1024-aligned
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -356,19 +354,11 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
             const int c = kChunksPerWarp * wq + cc;        // chunk within the half
             const uint4 raw = raws[h][cc];
             uint32_t sc0, sc1;
-            if constexpr (MODE == kFc2) {
-              e4m3x2_scale_bf16x2(sw[h] >> (16 * (c & 1)), sc0, sc1);
-              decode8_bf16(raw.x, sc0, o[h][cc]);
-              decode8_bf16(raw.y, sc0, o[h][cc] + 4);
-              decode8_bf16(raw.z, sc1, o[h][cc] + 8);
-              decode8_bf16(raw.w, sc1, o[h][cc] + 12);
-            } else {
-              e4m3x2_scale_f16x2(sw[h] >> (16 * (c & 1)), sc0, sc1);
-              decode8_f16(raw.x, sc0, o[h][cc]);
-              decode8_f16(raw.y, sc0, o[h][cc] + 4);
-              decode8_f16(raw.z, sc1, o[h][cc] + 8);
-              decode8_f16(raw.w, sc1, o[h][cc] + 12);
-            }
+            e4m3x2_scale_f16x2(sw[h] >> (16 * (c & 1)), sc0, sc1);
+            decode8_f16(raw.x, sc0, o[h][cc]);
+            decode8_f16(raw.y, sc0, o[h][cc] + 4);
+            decode8_f16(raw.z, sc1, o[h][cc] + 8);
+            decode8_f16(raw.w, sc1, o[h][cc] + 12);
           }
         }
         // the TMEM slot's previous MMAs are done
@@ -411,8 +401,7 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
       const TileInfo cur = queue_pop_warp(Q, qp, abort_flag, a.status);
       if (cur.rows == 0) break;
       const int n16 = (cur.rows + 15) & ~15;
-      // FC1: f16 weights and f16 token rows; FC2: bf16 weights and bf16 rows
-      const uint32_t idesc = MODE == kFc2 ? idesc_bf16(128, n16) : idesc_f16(128, n16);
+      const uint32_t idesc = idesc_f16(128, n16);  // f16 weights and f16 rows
       const int chunk_bytes = box_rows(n16) * kChunkRowBytes;  // this tile's chunk stride
       const int buf = local % nbuf;
       const uint32_t acc_par = ((uint32_t)(local / nbuf) & 1u) ^ 1u;
@@ -434,7 +423,7 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
         for (int kp = 0; kp < kBK / 32; ++kp) {
           const int ks = 2 * kp + part;
           const uint64_t bdesc = smem_desc(sb + (ks >> 2) * chunk_bytes + (ks & 3) * 32, 16, 1024, 2);
-          mma_bf16_ts_warp(acc, acol + 8 * ks, bdesc, idesc, (kb == 0 && kp == 0) ? 0u : 1u);
+          mma_f16_ts_warp(acc, acol + 8 * ks, bdesc, idesc, (kb == 0 && kp == 0) ? 0u : 1u);
         }
         issued = true;
         tc_commit_warp(R.bar(kBarFree + slot));
@@ -471,16 +460,15 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
       const int row0 = cur.tt * kTileRows;
       const int buf = local % nbuf;
       const uint32_t acc_par = (uint32_t)(local / nbuf) & 1u;
-      // FC2: the bf16-decoded weights carry a factor 2^-8 (exactly undone here).
-      // FC1: each token column was multiplied by a power of two 2^-k when its
-      // f16 row was formed; 2^k, the row scale, undoes it exactly.
-      const float alpha = rows ? a.alpha[cur.e] * (MODE == kFc2 ? kDecodeUnscale : 1.0f) : 0.0f;
-      const float rs = MODE != kFc2 && r < rows ? a.row_scale[(size_t)row0 + r] : 0.0f;
+      // each token column's f16 row was multiplied by a power of two 2^-k when
+      // it was formed; 2^k, the row scale, undoes it exactly
+      const float alpha = rows ? a.alpha[cur.e] : 0.0f;
+      const float rs = r < rows ? a.row_scale[(size_t)row0 + r] : 0.0f;
       if (rows == 0 || !wait_or_abort(R.bar(kBarAccFull + buf), acc_par, abort_flag, a.status))
         *epi_stop = 1;
       named_bar_sync(1, 128);
       // every thread is past the previous tile's reads of s_rs
-      if constexpr (MODE != kFc2) s_rs[r] = rs;
+      s_rs[r] = rs;
       const bool stop = *epi_stop != 0;
       named_bar_sync(1, 128);
       if (stop) break;
@@ -496,7 +484,6 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
         const int fl = r & 63;
         const int j0 = 16 * (r >> 6);
         const int f = mt * 64 + fl;
-        const int fo = (f & ~7) | k8_pos(f & 7);  // FC2 meets it in the decode's K order
         const float* xg = xchg + fl * 33;             // gate sums of feature fl
         const float* xu = xchg + (64 + fl) * 33;      // up sums of feature fl
         float* mine = xchg + r * 33;
@@ -529,7 +516,7 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
               yu = fmaxf(fminf(yu, a.swiglu_limit), -a.swiglu_limit);
             }
             const float act = __fmul_rn(__fdiv_rn(yg, __fadd_rn(1.0f, expf(-yg))), yu);
-            a.route_out[p * a.I + fo] = __bfloat16_as_ushort(__float2bfloat16_rn(act));
+            a.route_out[p * a.I + f] = __bfloat16_as_ushort(__float2bfloat16_rn(act));
           }
           named_bar_sync(1, 128);  // the chunk's sums are read before the next one lands
         }
@@ -550,13 +537,12 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
             const int col = c0 + j;
             if (col >= rows) break;
             const size_t p = (size_t)row0 + col;
+            const float y = __fmul_rn(__fmul_rn(v[j], alpha), s_rs[col]);
             if constexpr (MODE == kFc1Relu2) {
-              const float y = __fmul_rn(__fmul_rn(v[j], alpha), s_rs[col]);
               const float t = fmaxf(y, 0.0f);
-              a.route_out[p * a.I + mt * 128 + (r & ~7) + k8_pos(r & 7)] =
+              a.route_out[p * a.I + mt * 128 + r] =
                   __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(t, t)));
             } else {
-              const float y = __fmul_rn(v[j], alpha);
               a.route_out[p * a.H + mt * 128 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
             }
           }

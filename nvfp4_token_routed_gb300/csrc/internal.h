@@ -127,6 +127,10 @@ void launch_prepare_fc(int E, int N, int D, int Np, int Dp, int swiglu_I, const 
                        uint8_t* codes, uint8_t* sf, float* alpha, const float* a_scale,
                        cudaStream_t s);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
+// W4A16: the bf16 activated rows of the valid routes as f16 rows times 2^-k,
+// 2^k per row in scale (the f16 FC2 GEMM's operand).
+void launch_act_f16(int TK, int Ip, const int32_t* inv, const void* act, void* act16,
+                    float* scale, cudaStream_t s);
 void launch_route_topk(int T, int E, int K, const float* logits, int32_t* ids, float* w,
                        cudaStream_t s);
 void launch_requant(int TK, int I, const int32_t* inv, const float* act, uint8_t* qc, uint8_t* qsf,

@@ -119,6 +119,8 @@ void compute_layout(const moe_dims* d, int32_t T, int32_t K, int32_t w4a16, moe_
     L->x_perm = take(sizeof(uint16_t) * (size_t)rows * H);
     L->xq_scale = take(sizeof(float) * rows);
     L->act_bf16 = take(sizeof(uint16_t) * (size_t)rows * I);
+    L->act_f16 = take(sizeof(uint16_t) * (size_t)rows * I);
+    L->act_scale = take(sizeof(float) * rows);
   }
   L->route = take(sizeof(uint16_t) * (size_t)rows * H);
   L->tile_sync = take(sizeof(int32_t) * (2 * (size_t)(tiles ? tiles : 1) + (size_t)rows));
@@ -353,7 +355,8 @@ int32_t moe_nvfp4_forward_kernel_count(const moe_dims* d, int32_t T, int32_t K, 
   if (T == 0) return 0;
   const int64_t TK = (int64_t)T * K;
   const bool fused = !w4a16 && TK <= kFusedMaxRoutes && TK <= kFusedRoutesPerExpert * d->E;
-  const int gemms = w4a16 ? 2 : fused ? 1 : 3;  // W4A4 three: FC1, requant, FC2
+  // W4A4 three: FC1, requant, FC2; W4A16 three: FC1, the f16 FC2 operand, FC2
+  const int gemms = w4a16 ? 3 : fused ? 1 : 3;
   return route_kernel_launches(TK) + gemms + 1;  // routing and gather, GEMMs, finalize
 }
 
@@ -575,7 +578,7 @@ static moe_status forward_w4a16_impl(const moe_dims* d, const moe_nvfp4_weights*
   if (!make_tmap_bytes(&tmA1, w->fc1_codes, H / 2, (uint64_t)d->E * N1, 128) ||
       !make_token_maps_3d(&tmB1, at<uint8_t>(ws, L.x_perm), 2 * (uint64_t)H, L.rows_cap) ||
       !make_tmap_bytes(&tmA2, w->fc2_codes, I / 2, (uint64_t)d->E * H, 128) ||
-      !make_token_maps_3d(&tmB2, at<uint8_t>(ws, L.act_bf16), 2 * (uint64_t)I, L.rows_cap))
+      !make_token_maps_3d(&tmB2, at<uint8_t>(ws, L.act_f16), 2 * (uint64_t)I, L.rows_cap))
     return MOE_ERR_CUDA;
 
   mark(0, s);
@@ -605,6 +608,8 @@ static moe_status forward_w4a16_impl(const moe_dims* d, const moe_nvfp4_weights*
   int grid = (int)std::min<int64_t>(sms, tiles_cap * g.m_tiles);
   if (launch_gemm_w4a16(tmA1, tmB1, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
   mark(2, s);
+  launch_act_f16(T * K, I, at<int32_t>(ws, L.inv), at<uint8_t>(ws, L.act_bf16),
+                 at<uint8_t>(ws, L.act_f16), at<float>(ws, L.act_scale), s);
   mark(3, s);
 
   GemmArgs g2 = g;
@@ -614,6 +619,7 @@ static moe_status forward_w4a16_impl(const moe_dims* d, const moe_nvfp4_weights*
   g2.w_rows = H;
   g2.sfa = w->fc2_sf;
   g2.alpha = w->fc2_alpha;
+  g2.row_scale = at<float>(ws, L.act_scale);
   g2.item_counter = g.status + kStatusItemCtr + 1;
   g2.route_out = at<uint16_t>(ws, L.route);
   grid = (int)std::min<int64_t>(sms, tiles_cap * g2.m_tiles);

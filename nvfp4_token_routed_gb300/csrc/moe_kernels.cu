@@ -378,15 +378,50 @@ __global__ void __launch_bounds__(kChunk) route_scatter_kernel(
   if (idx < TK) inv[idx] = p;
 }
 
+// One warp: a bf16 row of n8 x 8 values -> f16 times 2^-k, k chosen from the
+// row's largest magnitude so that it lands in [2^14, 2^15) (no scaling for a
+// zero row or an Inf/NaN); returns 2^k, the row's scale.  Every value of
+// magnitude at least 2^-14 after the scaling (all within 2^28 of the largest)
+// is exact in f16; smaller ones round to f16's subnormal step, far below the
+// rounding of the fp32 accumulation they meet.  dst may be src.
+__device__ __forceinline__ float bf16_row_to_f16(const uint4* src, uint4* dst, int n8, int lane) {
+  // largest magnitude (bf16 bits without the sign order like the magnitudes;
+  // halves compared separately)
+  uint32_t m = 0;
+  for (int i = lane; i < n8; i += 32) {
+    const uint4 v = src[i];
+    m = __vmaxu2(m, __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                             __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu)));
+  }
+  uint32_t mx = max(m & 0xFFFFu, m >> 16);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  // largest in [2^(e-127), 2^(e-126)) for biased exponent e: k = e - 141,
+  // with 2^-k kept a normal fp32
+  const int e = (int)(mx >> 7);
+  const int k = (mx == 0 || e == 255) ? 0 : max(e - 141, -126);
+  const float down = __uint_as_float((uint32_t)(127 - k) << 23);
+  for (int i = lane; i < n8; i += 32) {
+    const uint4 v = src[i];
+    const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float lo = __fmul_rn(__uint_as_float(in[j] << 16), down);
+      const float hi = __fmul_rn(__uint_as_float(in[j] & 0xFFFF0000u), down);
+      const __half2 h = __floats2half2_rn(lo, hi);
+      out[j] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    dst[i] = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+  return __uint_as_float((uint32_t)(127 + k) << 23);
+}
+
 // Row gather of one route (one warp): the token's quantized row and its block
 // scales (W4A4; rows already padded to Hp by the quantizer) or its bf16 row
 // (W4A16) into permuted row p.  W4A16 rows go to the FC1 GEMM as f16, which it
-// multiplies with f16-decoded weights: the row is multiplied by 2^-k, k chosen
-// from its largest magnitude so that it lands in [2^14, 2^15), and 2^k is the
-// row's scale.  Every bf16 value of magnitude at least 2^-14 after the scaling
-// (all within 2^28 of the row's largest) is exact in f16; smaller ones round to
-// f16's subnormal step, far below the fp32 accumulation's own rounding.  The
-// Hp - H padding columns are zeroed.
+// multiplies with f16-decoded weights, as bf16_row_to_f16 forms them, its
+// scale 2^k in ps.  The Hp - H padding columns are zeroed.
 struct GatherArgs {
   int K, H, Hp;
   const uint8_t* xc;
@@ -404,37 +439,9 @@ __device__ __forceinline__ void gather_route_row(const GatherArgs& g, int idx, i
   if constexpr (kW4A16) {
     const uint4* src = g.xb + (size_t)t * (g.H / 8);
     uint4* dst = g.pb + (size_t)p * (g.Hp / 8);
-    // largest magnitude (bf16 bits without the sign order like the magnitudes;
-    // halves compared separately)
-    uint32_t m = 0;
-    for (int i = lane; i < g.H / 8; i += 32) {
-      const uint4 v = __ldg(src + i);
-      m = __vmaxu2(m, __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
-                               __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu)));
-    }
-    uint32_t mx = max(m & 0xFFFFu, m >> 16);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-    // amax in [2^(e-127), 2^(e-126)) for biased exponent e: k = e - 141; no
-    // scaling for a zero row or an Inf/NaN; 2^-k kept a normal fp32
-    const int e = (int)(mx >> 7);
-    const int k = (mx == 0 || e == 255) ? 0 : max(e - 141, -126);
-    const float down = __uint_as_float((uint32_t)(127 - k) << 23);
-    for (int i = lane; i < g.H / 8; i += 32) {
-      const uint4 v = __ldg(src + i);
-      const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-      uint32_t out[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float lo = __fmul_rn(__uint_as_float(in[j] << 16), down);
-        const float hi = __fmul_rn(__uint_as_float(in[j] & 0xFFFF0000u), down);
-        const __half2 h = __floats2half2_rn(lo, hi);
-        out[j] = *reinterpret_cast<const uint32_t*>(&h);
-      }
-      dst[i] = make_uint4(out[0], out[1], out[2], out[3]);
-    }
+    const float rs = bf16_row_to_f16(src, dst, g.H / 8, lane);
     for (int i = g.H / 8 + lane; i < g.Hp / 8; i += 32) dst[i] = make_uint4(0u, 0u, 0u, 0u);
-    if (lane == 0) g.ps[p] = __uint_as_float((uint32_t)(127 + k) << 23);
+    if (lane == 0) g.ps[p] = rs;
   } else {
     const uint4* src = reinterpret_cast<const uint4*>(g.xc + (size_t)t * (g.Hp / 2));
     uint4* dst = reinterpret_cast<uint4*>(g.pc + (size_t)p * (g.Hp / 2));
@@ -620,6 +627,31 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
     launch_pdl(gather_rows_kernel<false>, dim3(gblocks), dim3(128), 0, s, a.TK,
                (const int32_t*)a.inv, gather_args(a));
   return cudaGetLastError();
+}
+
+// ============================================================== W4A16 FC2 operand
+// Each valid route's bf16 activated row (the FC1 handoff) as f16 times a power
+// of two, its scale 2^k (bf16_row_to_f16), for the f16 FC2 GEMM.  One warp per
+// route.
+__global__ void __launch_bounds__(256) act_f16_kernel(int TK, int Ip, const int32_t* __restrict__ inv,
+                                                      const uint4* act, uint4* act16,
+                                                      float* __restrict__ scale) {
+  pdl_wait();
+  pdl_trigger();
+  const int idx = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (idx >= TK) return;
+  const int p = inv[idx];
+  if (p < 0) return;
+  const float rs = bf16_row_to_f16(act + (size_t)p * (Ip / 8), act16 + (size_t)p * (Ip / 8),
+                                   Ip / 8, lane);
+  if (lane == 0) scale[p] = rs;
+}
+
+void launch_act_f16(int TK, int Ip, const int32_t* inv, const void* act, void* act16,
+                    float* scale, cudaStream_t s) {
+  launch_pdl(act_f16_kernel, dim3((TK + 7) / 8), dim3(256), 0, s, TK, Ip, inv,
+             static_cast<const uint4*>(act), static_cast<uint4*>(act16), scale);
 }
 
 // ============================================================== FC2-input requant

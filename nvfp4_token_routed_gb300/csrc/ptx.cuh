@@ -232,17 +232,6 @@ __device__ __forceinline__ uint32_t idesc_mxf4nvf4(uint32_t M, uint32_t N) {
   return d;
 }
 
-// Instruction descriptor of kind::f16 with bf16 A/B and fp32 accumulate.
-__device__ __forceinline__ uint32_t idesc_bf16(uint32_t M, uint32_t N) {
-  uint32_t d = 0;
-  d |= 1u << 4;   // D format: f32
-  d |= 1u << 7;   // A: bf16
-  d |= 1u << 10;  // B: bf16
-  d |= ((N >> 3) & 0x3F) << 17;
-  d |= ((M >> 4) & 0x1F) << 24;
-  return d;
-}
-
 // Instruction descriptor of kind::f16 with f16 A/B and fp32 accumulate (A and B
 // format fields 0 = f16).
 __device__ __forceinline__ uint32_t idesc_f16(uint32_t M, uint32_t N) {
@@ -265,32 +254,14 @@ __device__ __forceinline__ void mma_mxf4nvf4(uint32_t d_tmem, uint64_t adesc, ui
       : "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]^T, bf16 inputs (A: lane = row, 2 K elements
-// per 32-bit column, lower half first).
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // Whole-warp forms: every lane of a converged warp executes them with the same
 // (warp-uniform) operands and elect.sync picks the one lane that issues.  Run
 // this way, the descriptor arithmetic stays on the uniform datapath and a warp
 // issues an MMA every ~13 ns, against ~25-70 ns from a single-lane branch.
-__device__ __forceinline__ void mma_bf16_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+// D[tmem] (+)= A[tmem] * B[smem]^T of kind::f16, the operand type (one type
+// for A and B) given by idesc; A: lane = row, 2 K elements per 32-bit column,
+// lower half first.
+__device__ __forceinline__ void mma_f16_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
                                                  uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
@@ -388,54 +359,6 @@ __device__ __forceinline__ uint32_t cvt_e4m3(float v) {
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(out) : "f"(v), "f"(v));
   return out & 0xFFu;
 }
-// Decoding NVFP4 weights to bf16 (PTX converts E2M1 and E4M3 to f16 only) with
-// integer and bf16x2 instructions:
-//   * an E2M1 code c = s e1 e0 m0 written as the bf16 bits s<<15 | (c & 7)<<6
-//     reads as its E2M1 value x 2^-126 -- the exponent field is e1e0 and the top
-//     mantissa bit m0, and E2M1's subnormal (0.5) lands on a bf16 subnormal of
-//     the same relative step;
-//   * two UE4M3 block scales become an exact f16x2 (E4M3 subnormals are f16
-//     normals); shifting each half right by 3 moves the f16 fields onto bf16's
-//     and adding 230 to each exponent field makes scale x 2^118, a normal bf16
-//     (a zero scale gives 2^103 instead of 0, harmless: every code of an
-//     all-zero block is +-0, and +-0 times a finite scale is +-0);
-//   * their bf16 product is code x scale x 2^-8: at most 6 significant bits and
-//     within bf16's normal range, so exact.  The GEMM epilogue multiplies the
-//     accumulator by alpha x 2^8 (exact) to undo the factor.
-constexpr float kDecodeUnscale = 256.0f;  // 2^8
-
-// Two UE4M3 bytes (low 16 bits of b, first in the low byte) -> bf16x2 words
-// holding (first x 2^118) and (second x 2^118) in both halves.
-__device__ __forceinline__ void e4m3x2_scale_bf16x2(uint32_t b, uint32_t& s0, uint32_t& s1) {
-  uint32_t h;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((uint16_t)(b & 0xFFFFu)));
-  const uint32_t t = (h >> 3) + 0x73007300u;
-  s0 = __byte_perm(t, 0, 0x1010);
-  s1 = __byte_perm(t, 0, 0x3232);
-}
-
-// 8 E2M1 codes (one 32-bit word, code j in nibble j) -> 4 bf16x2 words of
-// code x scale x 2^-8, the scale given by e4m3x2_scale_bf16x2.  Word i holds
-// codes i (low half) and i + 4 (high half): the two nibbles sit 16 bits apart
-// in the word already, so one mask isolates a pair, one multiply makes the
-// shifted copies that hold the magnitude bits (at bits 6-8) and the sign bit
-// (at bit 15), a mask keeps those bits, and one bf16x2 multiply applies the
-// scale.  (Pairs 2 and 3 come from the word shifted right by 8; pair 1 is
-// already 4 bits up, so its multiplier is 4160 / 16.)  The K order of the
-// decoded operand is therefore 0, 4, 1, 5, 2, 6, 3, 7 within each group of 8,
-// and the bf16 operand it meets in the MMA is stored in that order too.
-__device__ __forceinline__ void decode8_bf16(uint32_t w, uint32_t scale, uint32_t* o) {
-  const uint32_t w8 = w >> 8;
-  const uint32_t x0 = ((w & 0x000F000Fu) * 4160u) & 0x81C081C0u;   // codes 0, 4
-  const uint32_t x1 = ((w & 0x00F000F0u) * 260u) & 0x81C081C0u;    // codes 1, 5
-  const uint32_t x2 = ((w8 & 0x000F000Fu) * 4160u) & 0x81C081C0u;  // codes 2, 6
-  const uint32_t x3 = ((w8 & 0x00F000F0u) * 260u) & 0x81C081C0u;   // codes 3, 7
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[0]) : "r"(x0), "r"(scale));
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[1]) : "r"(x1), "r"(scale));
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[2]) : "r"(x2), "r"(scale));
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[3]) : "r"(x3), "r"(scale));
-}
-
 // Decoding NVFP4 weights to f16 with the conversion instructions: E2M1 and
 // UE4M3 values are f16 normals (or zero), and code x scale has at most 6
 // significant bits between 2^-10 and 2688, so the f16 product is exact.
@@ -457,15 +380,6 @@ __device__ __forceinline__ void decode8_f16(uint32_t w, uint32_t scale, uint32_t
       : "r"(w));
 #pragma unroll
   for (int i = 0; i < 4; ++i) asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(o[i]) : "r"(scale));
-}
-
-// Position of element i (0..7) of a group of 8 in the K order that decode8_bf16
-// gives the decoded weights: 0, 4, 1, 5, 2, 6, 3, 7.
-__device__ __forceinline__ int k8_pos(int i) { return i < 4 ? 2 * i : 2 * i - 7; }
-// 8 bf16 values in natural order (one 16-byte vector) -> the same in that order.
-__device__ __forceinline__ uint4 k8_order(const uint4& v) {
-  return make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.x, v.z, 0x7632),
-                    __byte_perm(v.y, v.w, 0x5410), __byte_perm(v.y, v.w, 0x7632));
 }
 
 // E4M3 byte -> fp32, exact (bias 7, subnormal step 2^-9).

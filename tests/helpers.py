@@ -49,19 +49,23 @@ def unpack_codes(packed):
     return np.stack([packed & 15, packed >> 4], axis=-1).reshape(*packed.shape[:-1], -1)
 
 
-# K order of each group of 8 values in the W4A16 FC2 GEMM's bf16 operands (the
-# order in which it decodes a 32-bit word of eight E2M1 codes to bf16): the bf16
-# activated rows (act_bf16) are stored so.
-K8_ORDER = np.array([0, 4, 1, 5, 2, 6, 3, 7])
-
-
-def from_k8_order(rows):
-    """Rows stored with each group of 8 values in K8_ORDER -> natural order."""
-    r = np.asarray(rows)
-    g = r.reshape(*r.shape[:-1], r.shape[-1] // 8, 8)
-    nat = np.empty_like(g)
-    nat[..., K8_ORDER] = g
-    return nat.reshape(r.shape)
+def check_scaled_f16_rows(f16_rows, scales, want):
+    """The W4A16 GEMMs' f16 operand rows: each row of `want` (bf16 values as
+    float) times 2^-k, with its largest magnitude in [2^14, 2^15) and 2^k in
+    `scales`; exact down to f16's normal range, within half an f16 subnormal
+    step below it."""
+    got16 = np.asarray(f16_rows).view(np.float16).astype(np.float64)
+    rs = np.asarray(scales, np.float64)
+    want = np.asarray(want, np.float64)
+    amax = np.abs(want).max(axis=1)
+    k = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 14, 0.0)
+    assert np.array_equal(rs, 2.0 ** k)
+    assert np.all(np.abs(want / rs[:, None]).max(axis=1) < 2.0 ** 15)
+    got = got16 * rs[:, None]
+    normal = np.abs(want) >= rs[:, None] * 2.0 ** -14
+    assert np.array_equal(got[normal], want[normal])
+    tol = np.broadcast_to(rs[:, None] * 2.0 ** -25, want.shape)
+    assert np.all(np.abs(got - want)[~normal] <= tol[~normal])
 
 
 def rel_l2(a, b):

@@ -84,8 +84,10 @@ def test_workspace_layout_is_aligned_disjoint_and_monotone(lib, act, w4a16):
         assert len(set(offs)) == len(offs)
         TK = T * 8
         assert L["rows_cap"] % 128 == 0 and L["rows_cap"] >= TK + min(64, TK) * 127
-        used = ("x_perm", "act_bf16") if w4a16 else ("xq_codes", "act", "fc2q_codes")
-        unused = ("xq_codes", "act", "fc2q_codes") if w4a16 else ("x_perm", "act_bf16")
+        used = (("x_perm", "xq_scale", "act_bf16", "act_f16", "act_scale") if w4a16
+                else ("xq_codes", "xq_scale", "act", "fc2q_codes"))
+        unused = (("xq_codes", "act", "fc2q_codes") if w4a16
+                  else ("x_perm", "act_bf16", "act_f16", "act_scale"))
         assert all(L[k] > 0 for k in used) and all(L[k] == 0 for k in unused)
 
 
@@ -184,18 +186,19 @@ def test_binding_rejects_cpu_tensors():
 def test_forward_kernel_count(lib):
     """Launches of one forward call: routing and gather (one kernel up to 32
     routes, two up to 2048, four beyond), GEMMs (W4A4: one launch when
-    T*K <= min(2048, 8E), else FC1, requant, FC2; W4A16: FC1, FC2), finalize."""
+    T*K <= min(2048, 8E), else FC1, requant, FC2; W4A16: FC1, the f16 FC2
+    operand, FC2), finalize."""
     e64 = M.dims(64, 2048, 1024, "swiglu")
     e256 = M.dims(256, 7168, 2048, "relu2")
     count = M.moe_nvfp4_forward_kernel_count
     assert count(e64, 128, 8) == 2 + 3 + 1              # 1024 routes > 8 per expert
-    assert count(e64, 128, 8, True) == 2 + 2 + 1
+    assert count(e64, 128, 8, True) == 2 + 3 + 1
     assert count(e64, 64, 8) == 2 + 1 + 1               # 512 routes = 8 per expert: one launch
     assert count(e256, 1, 8) == 1 + 1 + 1               # 8 routes: rows gathered by the routing block
     assert count(e256, 4, 8) == 1 + 1 + 1               # 32 routes
     assert count(e256, 5, 8) == 2 + 1 + 1               # 40 routes: separate gather
     assert count(e256, 256, 8) == 2 + 1 + 1             # 2048 routes
     assert count(e256, 257, 8) == 4 + 3 + 1             # 2056 routes: three routing kernels
-    assert count(e256, 4096, 8, True) == 4 + 2 + 1
+    assert count(e256, 4096, 8, True) == 4 + 3 + 1
     assert count(e256, 0, 8) == 0
     assert count(e256, 4, 0) == -1 and count(e256, 4, 33) == -1 and count(e256, -1, 8) == -1

@@ -23,7 +23,7 @@ import nvfp4_token_routed_gb300 as M
 from nvfp4_token_routed_gb300 import workloads as W
 from oracle import oracle as O
 
-from helpers import (TILE_ROWS, bf16_np, from_k8_order, rel_l2, signed_step, stored_fc1_rows,
+from helpers import (TILE_ROWS, bf16_np, rel_l2, signed_step, stored_fc1_rows,
                      to_np_u16, unpack_codes, unswizzle)
 
 pytestmark = pytest.mark.gpu
@@ -196,7 +196,7 @@ def test_full_size_workload(wl, T, variant):
     else:
         # the bf16 handoff of the sample's routes
         act = M.ws_view(ws, L, "act_bf16", torch.int16, (rc, Ip))
-        act = from_k8_order(act[torch.as_tensor(gp, device=DEV)].cpu().numpy().view(np.uint16))
+        act = act[torch.as_tensor(gp, device=DEV)].cpu().numpy().view(np.uint16)
         act = act[:, :wl.I]
         assert rel_l2(bf16_np(act), bf16_np(res["act"][op])) <= 1e-2
     got = out[torch.as_tensor(sample, device=DEV)].cpu().view(torch.int16).numpy().view(np.uint16)

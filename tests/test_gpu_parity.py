@@ -13,7 +13,7 @@ import nvfp4_token_routed_gb300 as M
 from nvfp4_token_routed_gb300 import workloads as W
 from oracle import oracle as O
 
-from helpers import (TILE_ROWS, OracleRun, bf16_np, from_k8_order, rel_l2, signed_step,
+from helpers import (TILE_ROWS, OracleRun, bf16_np, check_scaled_f16_rows, rel_l2, signed_step,
                      stored_fc1_rows, to_np_u16, unpack_codes, unswizzle)
 
 pytestmark = pytest.mark.gpu
@@ -208,20 +208,10 @@ def test_w4a16_permuted_rows_and_routing(name):
     rmap = _rows_map(g, o)
     perm = g.view("perm", torch.int32, (g.L["rows_cap"],))
     assert np.array_equal(perm[rmap], o.res["perm"])
-    # f16 rows, each the bf16 row times 2^-k with its largest magnitude in
-    # [2^14, 2^15); 2^k is the row scale.  Exact down to f16's normal range,
-    # within half an f16 subnormal step below it.
-    xp = g.view("x_perm", torch.int16, (g.L["rows_cap"], wl.H))[rmap].view(np.float16)
-    rs = g.view("xq_scale", torch.float32, (g.L["rows_cap"],))[rmap].astype(np.float64)
-    want = bf16_np(to_np_u16(x)[o.res["perm"] // wl.K]).astype(np.float64)
-    amax = np.abs(want).max(axis=1)
-    assert np.all(rs == 2.0 ** (np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 14)
-                  * (amax > 0) + (amax == 0))
-    assert np.all(np.abs(want / rs[:, None]).max(axis=1) < 2.0 ** 15)
-    got = xp.astype(np.float64) * rs[:, None]
-    normal = np.abs(want) >= rs[:, None] * 2.0 ** -14
-    assert np.array_equal(got[normal], want[normal])
-    assert np.all(np.abs(got - want)[~normal] <= (rs[:, None] * 2.0 ** -25 * np.ones_like(want))[~normal])
+    # the FC1 GEMM's f16 token rows
+    xp = g.view("x_perm", torch.int16, (g.L["rows_cap"], wl.H))[rmap]
+    rs = g.view("xq_scale", torch.float32, (g.L["rows_cap"],))[rmap]
+    check_scaled_f16_rows(xp, rs, bf16_np(to_np_u16(x)[o.res["perm"] // wl.K]))
 
 
 @pytest.mark.parametrize("name", list(CASES))
@@ -229,12 +219,16 @@ def test_w4a16_handoff_route_rows_and_output(name):
     wl, g, o, x = _run16(name)
     rmap = _rows_map(g, o)
     act = g.view("act_bf16", torch.int16, (g.L["rows_cap"], wl.I))[rmap].view(np.uint16)
-    a_g, a_o = bf16_np(from_k8_order(act)), bf16_np(o.res["act"])
+    a_g, a_o = bf16_np(act), bf16_np(o.res["act"])
     assert rel_l2(a_g, a_o) <= 4e-3
     # bf16 rounding of an fp32-accumulated vs an fp64 value: one bf16 step apart
     # at most, except where cancellation leaves a value near zero (at most 0.1%)
     step = np.abs(a_g.view(np.int32) - a_o.view(np.int32)) >> 16
     assert (step > 1).mean() <= 1e-3
+    # the FC2 GEMM's f16 rows: the handoff rows, scaled
+    a16 = g.view("act_f16", torch.int16, (g.L["rows_cap"], wl.I))[rmap]
+    ars = g.view("act_scale", torch.float32, (g.L["rows_cap"],))[rmap]
+    check_scaled_f16_rows(a16, ars, a_g)
     route = g.view("route", torch.int16, (g.L["rows_cap"], wl.H))[rmap].view(np.uint16)
     assert rel_l2(bf16_np(route), bf16_np(o.res["route"])) <= 1e-2
     out = g.out.cpu().view(torch.int16).numpy().view(np.uint16)
