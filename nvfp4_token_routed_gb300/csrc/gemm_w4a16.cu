@@ -48,8 +48,8 @@
 //     read it into registers), TMEM slots of decoded weights (3 blocks of 256 K)
 //     and token stages (2-8 blocks of 256 K, loaded ahead of the MMAs
 //     independently of the decode); each item's
-//     accumulator is split into even / odd K-step partial sums; 1-2 items in
-//     flight; every wait bounded.
+//     accumulator is split into even / odd K-step partial sums; 2 items in
+//     flight up to 96-token tiles, 1 beyond; every wait bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -106,11 +106,14 @@ constexpr int kNumBars = kBarDrain + kIssuers;
 constexpr int kFlagsOff = 8 * kNumBars;
 constexpr int kRingOff = 768;
 static_assert(kFlagsOff + 16 <= kRingOff && kRingOff + 16 * kItemSlots <= 1024, "flag area");
-// Token boxes are 16 << box_log(n16) rows: the smallest of 16/32/64/128 >= n16.
-__device__ __forceinline__ int box_log(int n16) {
-  return n16 <= 16 ? 0 : n16 <= 32 ? 1 : n16 <= 64 ? 2 : 3;
+// Token boxes: the smallest of 16/32/64/96/128 rows >= n16; box_map(n16) is its
+// tensor map (maps 0-3: 16 << i rows, map 4: 96 rows).
+__device__ __forceinline__ int box_map(int n16) {
+  return n16 <= 16 ? 0 : n16 <= 32 ? 1 : n16 <= 64 ? 2 : n16 <= 96 ? 4 : 3;
 }
-__device__ __forceinline__ int box_rows(int n16) { return 16 << box_log(n16); }
+__device__ __forceinline__ int box_rows(int n16) {
+  return n16 <= 16 ? 16 : n16 <= 32 ? 32 : n16 <= 64 ? 64 : n16 <= 96 ? 96 : 128;
+}
 }  // namespace w4a16
 
 template <int MODE>
@@ -158,7 +161,7 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
     *epi_stop = 0;
     fence_barrier_init();
     prefetch_tmap(&tmA);
-    for (int i = 0; i < 4; ++i) prefetch_tmap(&tmB.box[i]);
+    for (int i = 0; i < 5; ++i) prefetch_tmap(&tmB.box[i]);
   }
   __syncwarp();  // thread 0's set-up branch rejoins its warp before the barrier
   if (warp == 1) {
@@ -178,12 +181,17 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
   // each, chunk-major, so chunk c of a tile starts c x box_rows x 128 bytes in.
   const int stage_bytes = kChunks * box_rows(max_n16) * kChunkRowBytes;  // multiple of 1024
   // Each item accumulates into two partial sums (even and odd K steps, each
-  // issued by its own warp), added in a fixed order in the epilogue.  The split never depends on the batch, so results stay bitwise
-  // batch invariant.  nbuf items are in flight (one when tiles exceed 64 tokens).
+  // issued by its own warp), added in a fixed order in the epilogue.  The
+  // split never depends on the batch, so results stay bitwise batch invariant.
+  // Two items are in flight (the epilogue of one overlaps the MMAs of the
+  // next) up to 96-token tiles, where the accumulators leave TMEM room for a
+  // single decoded A slot (measured on GB300 at 65-96-token tiles: FC1 and FC2
+  // 16% and 17% faster than two A slots with one item in flight); one item
+  // beyond.
   const int acc_cols = (max_n16 + 31) & ~31;
   const int nacc = kIssuers;
   const int acc_stride = nacc * acc_cols;                  // TMEM columns per item
-  const int nbuf = max_n16 <= 64 ? 2 : 1;                  // accumulator buffers
+  const int nbuf = max_n16 <= 96 ? 2 : 1;                  // accumulator buffers
   const int a_base = nbuf * acc_stride;                    // decoded A slots follow the accumulators
   // Shared memory goes first to packed-weight slots: the weight stream needs
   // its bytes in flight to cover the memory latency under load (measured on
@@ -274,8 +282,9 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
       while (ok) {
         const TileInfo cur = queue_pop_thread(Q, qp, abort_flag, a.status);
         if (cur.rows == 0) break;
-        const int bl = box_log((cur.rows + 15) & ~15);
-        const uint32_t tx = (uint32_t)kChunks * (16u << bl) * kChunkRowBytes;
+        const int n16 = (cur.rows + 15) & ~15;
+        const int bl = box_map(n16);
+        const uint32_t tx = (uint32_t)(kChunks * box_rows(n16) * kChunkRowBytes);
         const int b_row = cur.tt * kTileRows;
         for (int kb = 0; kb < a.K / kBK; ++kb) {
           if (!wait_or_abort(R.bar(kBarTokEmpty + stage), phase ^ 1, abort_flag, a.status)) {

@@ -176,7 +176,7 @@ struct W4A4Args {
 // boxes of 16, 32, 64 and 128 rows (128-byte swizzle), so that a tile of n rows
 // (a multiple of 16) arrives in at most three copies.
 struct TokenMaps {
-  CUtensorMap box[4];
+  CUtensorMap box[5];  // 16, 32, 64, 128 rows; [4] 96 rows (W4A16 only)
 };
 // Tensor maps of both phases: weights, tokens (four box heights) and the output
 // rows as TMA store target, 16-row boxes of the tile's features (FC1 ReLU2: fp32

@@ -185,17 +185,18 @@ bool make_token_maps(TokenMaps* t, const void* base, uint64_t row_bytes, uint64_
   return true;
 }
 
-// The four token-stage maps of a bf16 [rows][row_bytes] buffer for the W4A16
+// The five token-stage maps of a 16-bit [rows][row_bytes] buffer for the W4A16
 // GEMM: a 3-D view (128-byte chunk of a row, row, chunk index) whose box
-// (128 B, 16 << i rows, 4 chunks) lands chunk-major in shared memory, i.e. four
-// 128-byte-swizzled K-major chunks (256 K) of box-height rows, in one copy.
+// (128 B, 16/32/64/128/96 rows, 4 chunks) lands chunk-major in shared memory,
+// i.e. four 128-byte-swizzled K-major chunks (256 K) of box-height rows, in one
+// copy.
 bool make_token_maps_3d(TokenMaps* t, const void* base, uint64_t row_bytes, uint64_t rows) {
   auto fn = encode_fn();
   if (!fn) return false;
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < 5; ++i) {
     cuuint64_t dims[3] = {128, rows, row_bytes / 128};
     cuuint64_t strides[2] = {row_bytes, 128};
-    cuuint32_t box[3] = {128, 16u << i, 4};
+    cuuint32_t box[3] = {128, i < 4 ? 16u << i : 96u, 4};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(&t->box[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
