@@ -222,3 +222,35 @@ def test_w4a16_batch_invariance(e64):
     wb = torch.cat([wts[tgt], wts[tgt][rep]]).contiguous()
     out = M.forward_w4a16(w, xb, ib, wb)
     assert torch.equal(out[:7].view(torch.int16), alone.view(torch.int16))
+
+
+def test_w4a16_token_rows_of_any_magnitude():
+    """The W4A16 GEMMs carry each bf16 row as f16 times a power of two: rows far
+    outside f16's range (1e-12, 1e6 and 1e15 in magnitude), a zero row and a
+    row spanning 2^40 of dynamic range meet the oracle's fp64 expert like
+    ordinary rows, and a row's output does not depend on its neighbours."""
+    wl = W.Workload("swiglu_T8_H256_I256_E4_K2", 8, 256, 256, 4, 2, "swiglu")
+    w1, w2 = W.make_weights(wl)
+    w = M.prepare_weights(w1.to(DEV), w2.to(DEV), wl.act)
+    x = W.make_x(wl).float()
+    scale = torch.tensor([1.0, 1e-12, 1e6, 1e15, 0.0, 1.0, 3e-5, 1.0]).unsqueeze(1)
+    x = x * scale
+    x[5, ::2] *= 2.0 ** -40                        # a row spanning 2^40
+    x = x.to(torch.bfloat16)
+    ids, wts = W.make_routing(wl)
+    out = M.forward_w4a16(w, x.to(DEV), ids.to(DEV), wts.to(DEV))
+    torch.cuda.synchronize()
+    Wt = O.Weights(to_np_u16(w1), to_np_u16(w2))
+    ref = O.forward_w4a16(Wt, to_np_u16(x), ids.numpy(), wts.numpy(), wl.E, wl.H, wl.I, wl.act)
+    got = bf16_np(to_np_u16(out.cpu()))
+    want = bf16_np(ref["out"])
+    for t in range(wl.T):
+        if t == 4:
+            assert not got[t].any()                # a zero row gives a zero output
+            continue
+        assert np.isfinite(got[t]).all(), t
+        assert rel_l2(got[t], want[t]) <= 2e-2, t
+    # each token alone gives its row of the batch, bit for bit
+    for t in range(wl.T):
+        one = M.forward_w4a16(w, x[t:t + 1].to(DEV), ids[t:t + 1].to(DEV), wts[t:t + 1].to(DEV))
+        assert torch.equal(one.view(torch.int16), out[t:t + 1].view(torch.int16)), t
