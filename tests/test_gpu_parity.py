@@ -38,7 +38,7 @@ def _inputs(wl):
     return x, w1, w2, ids, wts
 
 
-class GpuRun:
+class GpuForward:
     def __init__(self, wl, x, w1, w2, ids, wts):
         dev = "cuda"
         self.wl = wl
@@ -63,7 +63,7 @@ def _run(name):
     if name not in _cache:
         wl = CASES[name]
         x, w1, w2, ids, wts = _inputs(wl)
-        _cache[name] = (wl, GpuRun(wl, x, w1, w2, ids, wts), OracleRun(wl, x, w1, w2, ids, wts))
+        _cache[name] = (wl, GpuForward(wl, x, w1, w2, ids, wts), OracleRun(wl, x, w1, w2, ids, wts))
     return _cache[name]
 
 
@@ -172,7 +172,7 @@ def test_route_rows_and_output_rel_l2(name):
 
 # ----------------------------------------------------------------------------- W4A16
 
-class GpuRun16:
+class GpuForward16:
     def __init__(self, wl, x, w1, w2, ids, wts):
         dev = "cuda"
         self.wl = wl
@@ -194,7 +194,7 @@ def _run16(name):
     if name not in _cache16:
         wl = CASES[name]
         x, w1, w2, ids, wts = _inputs(wl)
-        _cache16[name] = (wl, GpuRun16(wl, x, w1, w2, ids, wts),
+        _cache16[name] = (wl, GpuForward16(wl, x, w1, w2, ids, wts),
                           OracleRun(wl, x, w1, w2, ids, wts, w4a16=True), x)
     return _cache16[name]
 
