@@ -401,18 +401,26 @@ __device__ __forceinline__ float bf16_row_to_f16(const uint4* src, uint4* dst, i
   const int e = (int)(mx >> 7);
   const int k = (mx == 0 || e == 255) ? 0 : max(e - 141, -126);
   const float down = __uint_as_float((uint32_t)(127 - k) << 23);
-  for (int i = lane; i < n8; i += 32) {
-    const uint4 v = src[i];
-    const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-    uint32_t out[4];
+  // four vectors per lane in flight before their stores
+  for (int i0 = 0; i0 < n8; i0 += 128) {
+    uint4 v[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float lo = __fmul_rn(__uint_as_float(in[j] << 16), down);
-      const float hi = __fmul_rn(__uint_as_float(in[j] & 0xFFFF0000u), down);
-      const __half2 h = __floats2half2_rn(lo, hi);
-      out[j] = *reinterpret_cast<const uint32_t*>(&h);
+    for (int q = 0; q < 4; ++q)
+      if (i0 + lane + 32 * q < n8) v[q] = src[i0 + lane + 32 * q];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (i0 + lane + 32 * q >= n8) continue;
+      const uint32_t in[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+      uint32_t out[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float lo = __fmul_rn(__uint_as_float(in[j] << 16), down);
+        const float hi = __fmul_rn(__uint_as_float(in[j] & 0xFFFF0000u), down);
+        const __half2 h = __floats2half2_rn(lo, hi);
+        out[j] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      dst[i0 + lane + 32 * q] = make_uint4(out[0], out[1], out[2], out[3]);
     }
-    dst[i] = make_uint4(out[0], out[1], out[2], out[3]);
   }
   return __uint_as_float((uint32_t)(127 + k) << 23);
 }
