@@ -27,51 +27,68 @@ namespace moe {
 // that encode scale and no per-token scale is written.
 // Rows of up to 512 * NB values (NB blocks of 16 per lane) are loaded once into
 // registers, all their loads in flight together; longer rows are read twice.
-template <int NB>
+// NB: blocks of 16 values a lane holds in registers (0: rows of any length, read
+// twice); S: warps sharing a row (S = 2 halves the registers a warp needs for
+// rows of 4097-8192 values, so that twice the rows are in flight).
+template <int NB, int S>
 __global__ void __launch_bounds__(256) quantize_tokens_kernel(int T, int H, int Hp,
                                                               const uint4* __restrict__ x,
                                                               uint8_t* __restrict__ codes,
                                                               uint8_t* __restrict__ sf,
                                                               float* __restrict__ scale,
                                                               const float* __restrict__ static_enc) {
+  __shared__ float s_max[8];
   pdl_wait();
   pdl_trigger();
-  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int t = gw / S;          // row; warp gw % S of its S holds its blocks lane + 32 (S j + part)
+  const int part = gw % S;
   const int lane = threadIdx.x & 31;
-  if (t >= T) return;
+  const int wib = threadIdx.x >> 5;
   const uint4* row = x + (size_t)t * (H / 8);
   const int nb = H / 16;
-  if (NB > 0 && nb <= 32 * NB) {
-    // lane l holds blocks l, l + 32, ...: two 16-byte vectors each
+  if (NB > 0 && nb <= 32 * NB * S) {
+    // lane l holds blocks l + 32 (S j + part): two 16-byte vectors each
     uint4 r[NB > 0 ? NB : 1][2];
     float m = 0.0f;
+    if (t < T) {
 #pragma unroll
-    for (int j = 0; j < NB; ++j) {
-      const int b = lane + 32 * j;
-      if (b < nb) {
-        r[j][0] = __ldcs(row + 2 * b);
-        r[j][1] = __ldcs(row + 2 * b + 1);
+      for (int j = 0; j < NB; ++j) {
+        const int b = lane + 32 * (S * j + part);
+        if (b < nb) {
+          r[j][0] = __ldcs(row + 2 * b);
+          r[j][1] = __ldcs(row + 2 * b + 1);
+        }
       }
-    }
 #pragma unroll
-    for (int j = 0; j < NB; ++j)
-      if (lane + 32 * j < nb) m = fmaxf(m, fmaxf(bf16x8_absmax(r[j][0]), bf16x8_absmax(r[j][1])));
-    if (static_enc) m = 1.0f;  // any non-zero value: the static path quantizes every real block
+      for (int j = 0; j < NB; ++j)
+        if (lane + 32 * (S * j + part) < nb)
+          m = fmaxf(m, fmaxf(bf16x8_absmax(r[j][0]), bf16x8_absmax(r[j][1])));
+    }
     m = warp_max(m);
+    if (S > 1) {
+      // the row's warps are neighbours in the block: exchange their maxima
+      if (lane == 0) s_max[wib] = m;
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < S; ++i) m = fmaxf(m, s_max[(wib / S) * S + i]);
+    }
+    if (t >= T) return;
+    if (static_enc) m = 1.0f;  // any non-zero value: the static path quantizes every real block
     uint2* crow = reinterpret_cast<uint2*>(codes + (size_t)t * (Hp / 2));
     uint8_t* srow = sf + (size_t)t * (Hp / 16);
-    for (int b = (m == 0.0f ? 0 : nb) + lane; b < Hp / 16; b += 32) {
+    for (int b = (m == 0.0f ? 0 : nb) + lane + 32 * part; b < Hp / 16; b += 32 * S) {
       crow[b] = make_uint2(0u, 0u);
       srow[b] = 0;
     }
     if (m == 0.0f) {
-      if (lane == 0) scale[t] = 0.0f;
+      if (lane == 0 && part == 0) scale[t] = 0.0f;
       return;
     }
     const float enc = static_enc ? *static_enc : __fdiv_rn(kRecipeMax, m);
 #pragma unroll
     for (int j = 0; j < NB; ++j) {
-      const int b = lane + 32 * j;
+      const int b = lane + 32 * (S * j + part);
       if (b < nb) {
         float v[16];
         bf16x16_to_f32(r[j][0], r[j][1], v);
@@ -80,9 +97,10 @@ __global__ void __launch_bounds__(256) quantize_tokens_kernel(int T, int H, int 
         crow[b] = q;
       }
     }
-    if (lane == 0 && !static_enc) scale[t] = __fmul_rn(m, kRecipeInv);
+    if (lane == 0 && part == 0 && !static_enc) scale[t] = __fmul_rn(m, kRecipeInv);
     return;
   }
+  if (S > 1 || t >= T) return;  // (S > 1 launches only when rows fit the registers)
   float m = 1.0f;  // any non-zero value: the static path quantizes every real block
   if (!static_enc) {
     m = 0.0f;
@@ -113,9 +131,12 @@ __global__ void __launch_bounds__(256) quantize_tokens_kernel(int T, int H, int 
 void launch_quantize_tokens(int T, int H, int Hp, const void* x, uint8_t* codes, uint8_t* sf,
                             float* scale, const float* static_enc, cudaStream_t s) {
   const int warps = 8;
-  const int blocks = (T + warps - 1) / warps;
-  auto* k = H <= 2048 ? quantize_tokens_kernel<4> : H <= 8192 ? quantize_tokens_kernel<16>
-                                                              : quantize_tokens_kernel<0>;
+  // rows of up to 2048 values: one warp, 4 blocks a lane; up to 8192: two warps
+  // per row, 8 blocks a lane each; beyond: one warp, the row read twice
+  const int S = H <= 2048 ? 1 : H <= 8192 ? 2 : 1;
+  const int blocks = (int)(((int64_t)T * S + warps - 1) / warps);
+  auto* k = H <= 2048 ? quantize_tokens_kernel<4, 1>
+                      : H <= 8192 ? quantize_tokens_kernel<8, 2> : quantize_tokens_kernel<0, 1>;
   launch_pdl(k, dim3(blocks), dim3(warps * 32), 0, s, T, H, Hp, static_cast<const uint4*>(x),
              codes, sf, scale, static_enc);
 }
