@@ -111,6 +111,25 @@ static_assert(kFlagsOff + 16 <= kRingOff && kRingOff + 16 * kItemSlots <= 1024, 
 __device__ __forceinline__ int box_map(int n16) {
   return n16 <= 16 ? 0 : n16 <= 32 ? 1 : n16 <= 64 ? 2 : n16 <= 96 ? 4 : 3;
 }
+// Work items of a launch whose token tiles are split in halves (split = 2):
+// item = base x split + h, base numbered as tile_decode numbers items, half h
+// the tile's rows 64 h .. 64 h + 63.  The second half of a tile of at most 64
+// rows decodes with rows -1 (no work); past the end, rows 0.  The half rides
+// in bits 16.. of TileInfo::mt.
+constexpr int kSplitRows = 64;
+__device__ __forceinline__ int4 split_raw(const GemmArgs& a, int item, int n_items, int split) {
+  return tile_raw(a, item / split, n_items / split);
+}
+__device__ __forceinline__ TileInfo split_decode(const GemmArgs& a, int item, int n_items,
+                                                 int split, const int4& raw) {
+  TileInfo t = tile_decode(a, item / split, n_items / split, raw);
+  if (split == 1 || t.rows == 0) return t;
+  const int h = item % split;
+  const int rows = h == 0 ? min(kSplitRows, t.rows) : t.rows - kSplitRows;
+  t.rows = rows > 0 ? rows : -1;
+  t.mt |= h << 16;
+  return t;
+}
 __device__ __forceinline__ int box_rows(int n16) {
   return n16 <= 16 ? 16 : n16 <= 32 ? 32 : n16 <= 64 ? 64 : n16 <= 96 ? 96 : 128;
 }
@@ -175,8 +194,16 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
   pdl_wait();
   pdl_trigger();
 
-  const int n_items = a.status[kStatusTiles] * a.m_tiles;
-  const int max_n16 = (a.status[kStatusMaxRows] + 15) & ~15;
+  // Launches with tiles of more than 96 tokens run each tile as two items of up
+  // to kSplitRows rows (the weight tile decoded once per half, its second read
+  // an L2 hit on a neighbouring CTA), so that two items are in flight next to
+  // two decoded A slots in TMEM.  Measured on GB300: H7168/I2048/E256 top-8
+  // T=4096 (128-token tiles) FC2 1268 -> 1104 us; at 65-96-token tiles two
+  // whole items and one A slot are faster (E384 T=4096 FC1 2291 vs 2630 us).
+  const int max_rows = a.status[kStatusMaxRows];
+  const int split = max_rows > 96 ? 2 : 1;
+  const int n_items = a.status[kStatusTiles] * a.m_tiles * split;
+  const int max_n16 = (min(max_rows, kSplitRows * (3 - split)) + 15) & ~15;
   // A token stage is one 3-D box: kChunks 64-K chunks of box_rows(n16) rows
   // each, chunk-major, so chunk c of a tile starts c x box_rows x 128 bytes in.
   const int stage_bytes = kChunks * box_rows(max_n16) * kChunkRowBytes;  // multiple of 1024
@@ -228,19 +255,22 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
       // the raw values are only used an item later, so neither the atomic's nor
       // the load's latency stalls the copy stream.
       int item = blockIdx.x;
-      TileInfo cur = tile_info(a, item, n_items);        // rows == 0 past the end
+      // rows == 0 past the end, -1 for an empty half (neither published nor loaded)
+      TileInfo cur = split_decode(a, item, n_items, split, split_raw(a, item, n_items, split));
       int next = (int)gridDim.x + (item < n_items ? atomicAdd(a.item_counter, 1) : n_items);
-      int4 next_raw = tile_raw(a, next, n_items);
+      int4 next_raw = split_raw(a, next, n_items, split);
       int claim = next < n_items ? atomicAdd(a.item_counter, 1) : n_items;  // raw counter value
       while (ok) {
-        if (!queue_push(Q, qp, cur, abort_flag, a.status) || cur.rows == 0) break;
+        if (cur.rows >= 0 && (!queue_push(Q, qp, cur, abort_flag, a.status) || cur.rows == 0))
+          break;
         const int next2 = (int)gridDim.x + claim;         // claimed one item ago
-        const int4 next2_raw = tile_raw(a, next2, n_items);
+        const int4 next2_raw = split_raw(a, next2, n_items, split);
         claim = next2 < n_items ? atomicAdd(a.item_counter, 1) : n_items;
-        const TileInfo nxt = tile_decode(a, next, n_items, next_raw);  // loaded one item ago
-        const int a_row = cur.e * a.w_rows + cur.mt * 128;
-        const uint8_t* sfa0 = a.sfa + (size_t)cur.e * plane + (size_t)cur.mt * atoms * kAtom;
-        for (int kr = 0; kr < kraw; ++kr) {
+        const TileInfo nxt = split_decode(a, next, n_items, split, next_raw);  // loaded one item ago
+        const int mt = cur.mt & 0xFFFF;
+        const int a_row = cur.e * a.w_rows + mt * 128;
+        const uint8_t* sfa0 = a.sfa + (size_t)cur.e * plane + (size_t)mt * atoms * kAtom;
+        for (int kr = 0; kr < (cur.rows > 0 ? kraw : 0); ++kr) {
           if (!wait_or_abort(R.bar(kBarRawEmpty + rs), rphase ^ 1, abort_flag, a.status)) {
             ok = false;
             break;
@@ -285,7 +315,7 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
         const int n16 = (cur.rows + 15) & ~15;
         const int bl = box_map(n16);
         const uint32_t tx = (uint32_t)(kChunks * box_rows(n16) * kChunkRowBytes);
-        const int b_row = cur.tt * kTileRows;
+        const int b_row = cur.tt * kTileRows + kSplitRows * (cur.mt >> 16);
         for (int kb = 0; kb < a.K / kBK; ++kb) {
           if (!wait_or_abort(R.bar(kBarTokEmpty + stage), phase ^ 1, abort_flag, a.status)) {
             ok = false;
@@ -463,10 +493,10 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
     QueuePos qp;
     while (true) {
       const TileInfo cur = queue_pop_warp(Q, qp, abort_flag, a.status);
-      const int mt = cur.mt;
+      const int mt = cur.mt & 0xFFFF;
       const int rows = cur.rows;
       const int n16 = (rows + 15) & ~15;
-      const int row0 = cur.tt * kTileRows;
+      const int row0 = cur.tt * kTileRows + kSplitRows * (cur.mt >> 16);
       const int buf = local % nbuf;
       const uint32_t acc_par = (uint32_t)(local / nbuf) & 1u;
       // each token column's f16 row was multiplied by a power of two 2^-k when
