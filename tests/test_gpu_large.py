@@ -7,7 +7,8 @@ their FC2-input requantization (the pages' bound), their per-route rows and
 their final outputs (relative L2 <= 1e-2).
 
 The sweep points are those of the mid-scale Zipf layer (T=2048), the
-H7168/I2048/E256 top-8 SwiGLU layer (T in {1, 16, 128, 512, 4096}) and the
+H7168/I2048/E256 top-8 SwiGLU layer (T in {1, 16, 128, 512, 4096}; W4A16 at
+128 and 4096) and the
 pages' benchmark shape H7168/I3072/E384 top-6 (W4A4 at T in {512, 1024, 4096},
 W4A16 at T in {512, 1024, 4096}).  Each layer's weights are drawn and prepared
 once for all its sweep points.
@@ -33,7 +34,7 @@ SAMPLE = 32
 # (layer, T, variant); cases of one layer are adjacent so its weights are drawn once
 CASES = [(W.MID_ZIPF, 2048, "w4a4")]
 CASES += [(W.DSV3_LIKE, T, "w4a4") for T in (1, 16, 128, 512, 4096)]
-CASES += [(W.DSV3_LIKE, 128, "w4a16")]
+CASES += [(W.DSV3_LIKE, T, "w4a16") for T in (128, 4096)]   # 4096: 128-token tiles in halves
 CASES += [(W.PAGES_E384, T, "w4a4") for T in (512, 1024, 4096)]
 CASES += [(W.PAGES_E384, T, "w4a16") for T in (512, 1024, 4096)]
 
