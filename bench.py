@@ -360,7 +360,15 @@ def run_ours(args, rank, world, local_rank):
         g.manual_seed(W.BASE_SEED + 5)
         logits_d = torch.randn(T, wl.E, generator=g, device=dev)
 
+    # GEMM spans (profiling pass only): the earliest CTA start and latest CTA end
+    # of each grouped GEMM launch by the GPU's global timer, reset every step
+    span = torch.zeros(4, dtype=torch.int64, device=dev)
+    span_init = torch.tensor([-1, 0, -1, 0], dtype=torch.int64, device=dev)
+    span_on = [False]
+
     def step():
+        if span_on[0]:
+            span.copy_(span_init)
         if logits_d is not None:
             M.moe_nvfp4_route_topk(logits_d, ids_d, wts_d, stream)
         if args.w4a16:
@@ -430,10 +438,12 @@ def run_ours(args, rank, world, local_rank):
             e.record()
     torch.cuda.synchronize()
     M.moe_nvfp4_profile_events(marks)
+    span_on[0] = True
+    M.moe_nvfp4_profile_spans(span)
     graph_marked = capture()
     M.moe_nvfp4_profile_events([])
     M.moe_nvfp4_profile_events(marks)
-    fc1_ms, fc2_ms = [], []
+    fc1_ms, fc2_ms, fc1_span, fc2_span = [], [], [], []
     with torch.cuda.stream(stream):
         for i in range(args.steps):
             flush.zero_()
@@ -441,8 +451,15 @@ def run_ours(args, rank, world, local_rank):
             marks[5].synchronize()
             fc1_ms.append(marks[1].elapsed_time(marks[2]))
             fc2_ms.append(marks[3].elapsed_time(marks[4]))
+            sv = span.tolist()
+            if sv[1] > 0:
+                fc1_span.append((sv[1] - sv[0]) * 1e-6)   # ns -> ms
+            if sv[3] > 0:
+                fc2_span.append((sv[3] - sv[2]) * 1e-6)
     torch.cuda.synchronize()
     M.moe_nvfp4_profile_events([])
+    M.moe_nvfp4_profile_spans(None)
+    span_on[0] = False
 
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = max_over_ranks(sum(step_ms), world, dev)
@@ -528,6 +545,8 @@ def run_ours(args, rank, world, local_rank):
     B = algorithmic_bytes(wl, R, U, args.w4a16)
     fc1_mean = statistics.fmean(fc1_ms)
     fc2_mean = statistics.fmean(fc2_ms)
+    fc1_span_mean = statistics.fmean(fc1_span) if fc1_span else None
+    fc2_span_mean = statistics.fmean(fc2_span) if fc2_span else None
     # the W4A4 forward runs FC1, the FC2-input requant and FC2 as one launch when
     # T*K <= min(2048, 8*E) (moe_nvfp4.h): the roofline is then that launch's,
     # FC1 and FC2 bytes over the FC1 marker interval (the FC2 one is empty)
@@ -579,7 +598,13 @@ def run_ours(args, rank, world, local_rank):
                      "fc2_tensor_frac": (None if fused else
                                          F["fc2"] / (fc2_mean * 1e-3) / 1e12 / tpeak),
                      "timing": "CUDA events recorded by the library around the FC1 launch, "
-                               "over a second pass of the same K steps"},
+                               "over a second pass of the same K steps",
+                     # the launch's own span (earliest CTA start to latest CTA end by the
+                     # GPU's global timer, same pass): the event interval minus launch latency
+                     "kernel_span_us": None if fc1_span_mean is None else fc1_span_mean * 1e3,
+                     "span_frac": (None if fc1_span_mean is None else
+                                   kernel_bytes / (fc1_span_mean * 1e-3) / 1e9 / hbm),
+                     "fc2_span_us": None if fc2_span_mean is None else fc2_span_mean * 1e3},
         "layer_roofline": ({"bound": "tensor", "algorithmic_flops": layer_flops,
                             "achieved": layer_tflops, "peak": tpeak, "unit": "TFLOP/s",
                             "frac": layer_tflops / tpeak, "hbm_frac": layer_gbs / hbm}

@@ -341,10 +341,21 @@ moe_status moe_nvfp4_forward_noalloc(const moe_dims* d, const moe_nvfp4_weights*
 /* Profiling hook: register `n` cudaEvent_t handles (host pointer to an array of
  * event handles; n == 0 or events == NULL unregisters).  While registered,
  * every forward records events[0] before its first stage and events[i] after
- * stage i (1 routing, 2 FC1, 3 FC2-input requant or nothing for W4A16,
- * 4 FC2, 5 finalize) on its stream, for i < n.  Process-wide, not thread-safe;
- * for benchmarks only.  The events must stay alive while registered. */
+ * stage i (1 routing, 2 FC1, 3 the FC2-input requant (W4A4) or the f16
+ * conversion of the handoff rows (W4A16), 4 FC2, 5 finalize) on its stream,
+ * for i < n.  Process-wide, not thread-safe; for benchmarks only.  The events
+ * must stay alive while registered. */
 moe_status moe_nvfp4_profile_events(void* const* events, int32_t n);
+
+/* Profiling hook: register a device buffer of four uint64 (NULL unregisters;
+ * 8-byte aligned, else MOE_ERR_MISALIGNED).  While registered, the grouped
+ * GEMM launches of every forward fold the GPU's %globaltimer (ns) into it:
+ * [0] / [1] the earliest CTA start / latest CTA end of the FC1 launch (or of
+ * the one FC1 -> FC2 launch), [2] / [3] those of the FC2 launch, by atomic
+ * min / max.  The caller sets [0], [2] to UINT64_MAX and [1], [3] to 0 before
+ * a forward.  A launch's span excludes its launch latency, which event pairs
+ * around it include.  Process-wide, not thread-safe; for benchmarks only. */
+moe_status moe_nvfp4_profile_spans(void* device_spans);
 
 #ifdef __cplusplus
 }

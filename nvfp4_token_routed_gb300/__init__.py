@@ -87,6 +87,7 @@ def lib():
         L.moe_nvfp4_forward_noalloc.argtypes = [C.POINTER(moe_dims), C.POINTER(moe_nvfp4_weights),
                                                 i32, i32, vp, vp, vp, vp, vp, vp, vp]
         L.moe_nvfp4_profile_events.argtypes = [C.POINTER(C.c_void_p), i32]
+        L.moe_nvfp4_profile_spans.argtypes = [vp]
         L.moe_nvfp4_prepare_weights_per_tensor.argtypes = [
             C.POINTER(moe_dims), vp, vp, vp, vp, C.POINTER(moe_nvfp4_weights), vp]
         L.moe_nvfp4_quantize_tokens_static.argtypes = [i32, i32, vp, vp, vp, vp, vp]
@@ -108,7 +109,7 @@ def lib():
                   "moe_nvfp4_weight_sizes", "moe_nvfp4_prepare_weights",
                   "moe_nvfp4_quantize_tokens", "moe_nvfp4_workspace_layout", "moe_nvfp4_forward",
                   "moe_nvfp4_forward_w4a16", "moe_nvfp4_read_status", "moe_nvfp4_profile_events",
-                  "moe_nvfp4_forward_noalloc"]:
+                  "moe_nvfp4_profile_spans", "moe_nvfp4_forward_noalloc"]:
             getattr(L, f).restype = C.c_int
         _lib = L
     return _lib
@@ -293,6 +294,18 @@ def moe_nvfp4_profile_events(events):
         return
     arr = (C.c_void_p * len(events))(*[e.cuda_event for e in events])
     _check(lib().moe_nvfp4_profile_events(arr, len(events)), "moe_nvfp4_profile_events")
+
+
+def moe_nvfp4_profile_spans(spans):
+    """Register a CUDA int64 tensor of 4 elements (or None to unregister) that
+    the grouped GEMM launches fold their %globaltimer spans into: [0]/[1] the
+    FC1 (or one-launch) launch's earliest CTA start / latest CTA end, [2]/[3]
+    the FC2 launch's.  Reset [0], [2] to the maximum and [1], [3] to 0 first."""
+    if spans is not None and (not spans.is_cuda or spans.dtype != torch.int64
+                              or spans.numel() < 4 or not spans.is_contiguous()):
+        raise ValueError("spans: a contiguous CUDA int64 tensor of 4 elements")
+    _check(lib().moe_nvfp4_profile_spans(None if spans is None else _ptr(spans)),
+           "moe_nvfp4_profile_spans")
 
 
 # ------------------------------------------------------------------ allocating helpers

@@ -193,6 +193,7 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   pdl_wait();
   pdl_trigger();
+  if (a.span && threadIdx.x == 0) atomicMin(a.span, (unsigned long long)globaltimer());
 
   // Launches with tiles of more than 96 tokens run each tile as two items of up
   // to kSplitRows rows (the weight tile decoded once per half, its second read
@@ -599,6 +600,7 @@ __global__ void __launch_bounds__(w4a16::kThreads, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  if (a.span && threadIdx.x == 0) atomicMax(a.span + 1, (unsigned long long)globaltimer());
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);

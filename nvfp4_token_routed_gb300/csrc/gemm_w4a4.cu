@@ -251,6 +251,7 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   pdl_wait();
   pdl_trigger();
+  if (a.span && threadIdx.x == 0) atomicMin(a.span, (unsigned long long)globaltimer());
 
   const int n_tiles = a.status[kStatusTiles];
   const ItemSpace sp{a.run_fc1 ? n_tiles * a.ph[0].m_tiles : 0, a.fused ? n_tiles : 0,
@@ -686,6 +687,7 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  if (a.span && threadIdx.x == 0) atomicMax(a.span + 1, (unsigned long long)globaltimer());
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);

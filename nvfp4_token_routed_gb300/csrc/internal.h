@@ -80,6 +80,7 @@ struct GemmArgs {
   uint16_t* route_out; // FC2: [rows][H] bf16
   int H;
   float swiglu_limit;  // > 0: clamped SwiGLU (W4A16 FC1)
+  unsigned long long* span;  // profiling: [0] min CTA start, [1] max CTA end (%globaltimer), or null
 };
 
 // Launch with programmatic stream serialization: the kernel may start while the
@@ -170,6 +171,7 @@ struct W4A4Args {
   float* qs;                // FC2-input row scales
   const float* a2_static;   // per-tensor recipe: static FC2-input encode scale (else null)
   float swiglu_limit;       // > 0: clamped SwiGLU (gate <= L, |up| <= L)
+  unsigned long long* span; // profiling: [0] min CTA start, [1] max CTA end (%globaltimer), or null
 };
 
 // Token-tile tensor maps of one operand: the same [rows][row_bytes] buffer with

@@ -218,10 +218,12 @@ moe_status check_weights(const moe_nvfp4_weights* w) {
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-// Profiling events (moe_nvfp4_profile_events).
+// Profiling events (moe_nvfp4_profile_events) and GEMM spans
+// (moe_nvfp4_profile_spans).
 constexpr int kMaxProfileEvents = 8;
 cudaEvent_t g_prof[kMaxProfileEvents];
 int g_nprof = 0;
+unsigned long long* g_span = nullptr;
 
 // Stage boundaries of a forward: 0 before routing, 1 before FC1, 2 before the
 // requant, 3 before FC2, 4 before the finalize, 5 at the end.  Each stage is an
@@ -487,6 +489,7 @@ static moe_status forward_w4a4_impl(const moe_dims* d, const moe_nvfp4_weights* 
   g.tiles = at<int4>(ws, L.tiles);
   g.status = at<int32_t>(ws, L.status);
   g.item_counter = g.status + kStatusItemCtr;
+  g.span = g_span;  // FC1's (or the one launch's) span
   g.fc1_done = at<int32_t>(ws, L.tile_sync);
   g.rq_done = g.fc1_done + tiles_cap;
   g.row_amax = reinterpret_cast<float*>(g.rq_done + tiles_cap);
@@ -517,6 +520,7 @@ static moe_status forward_w4a4_impl(const moe_dims* d, const moe_nvfp4_weights* 
     W4A4Args g2 = g;
     g2.run_fc1 = 0;
     g2.run_fc2 = 1;
+    g2.span = g_span ? g_span + 2 : nullptr;
     g2.item_counter = g.status + kStatusItemCtr + 1;
     grid = (int)std::min<int64_t>(sms, tiles_cap * g2.ph[1].m_tiles);
     if (launch_gemm_w4a4(maps, g2, act, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -605,6 +609,7 @@ static moe_status forward_w4a16_impl(const moe_dims* d, const moe_nvfp4_weights*
   g.route_out = at<uint16_t>(ws, L.act_bf16);
   g.I = I;
   g.H = H;
+  g.span = g_span;
   g.swiglu_limit = o.swiglu_limit;
   int grid = (int)std::min<int64_t>(sms, tiles_cap * g.m_tiles);
   if (launch_gemm_w4a16(tmA1, tmB1, g, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -622,6 +627,7 @@ static moe_status forward_w4a16_impl(const moe_dims* d, const moe_nvfp4_weights*
   g2.alpha = w->fc2_alpha;
   g2.row_scale = at<float>(ws, L.act_scale);
   g2.item_counter = g.status + kStatusItemCtr + 1;
+  g2.span = g_span ? g_span + 2 : nullptr;
   g2.route_out = at<uint16_t>(ws, L.route);
   grid = (int)std::min<int64_t>(sms, tiles_cap * g2.m_tiles);
   if (launch_gemm_w4a16(tmA2, tmB2, g2, grid, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -670,6 +676,12 @@ moe_status moe_nvfp4_profile_events(void* const* events, int32_t n) {
   for (int i = 0; i < kMaxProfileEvents; ++i)
     g_prof[i] = i < n ? static_cast<cudaEvent_t>(events[i]) : nullptr;
   g_nprof = n;
+  return MOE_OK;
+}
+
+moe_status moe_nvfp4_profile_spans(void* device_spans) {
+  if (device_spans && !aligned(device_spans, 8)) return MOE_ERR_MISALIGNED;
+  g_span = static_cast<unsigned long long*>(device_spans);
   return MOE_OK;
 }
 

@@ -173,6 +173,12 @@ def test_profile_events_argument_checks(lib):
     assert lib.moe_nvfp4_profile_events(None, -1) == 1
 
 
+def test_profile_spans_argument_checks(lib):
+    import ctypes as C
+    assert lib.moe_nvfp4_profile_spans(C.c_void_p(4100)) == 3  # MOE_ERR_MISALIGNED
+    assert lib.moe_nvfp4_profile_spans(None) == 0
+
+
 def test_binding_rejects_cpu_tensors():
     import torch
     w = _FakeWeights(M.dims(8, 256, 512, "relu2"))
