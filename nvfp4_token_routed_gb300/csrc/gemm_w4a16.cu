@@ -26,7 +26,7 @@
 //     read in 128-byte runs) with their E4M3 scale atoms (bulk copy)
 //   * the last warp: token producer -- one 3-D tiled copy per 256-K block: four
 //     64-element K chunks of the tile's 16-bit rows (128-byte swizzle),
-//     chunk-major, in the smallest 16/32/64/128-row box that covers the tile
+//     chunk-major, in the smallest 16/32/64/96/128-row box that covers the item
 //   * warps 6..5+kDecodeWarps: decode -- kDecodeWarps/4 warps per TMEM lane
 //     quadrant; thread r of quadrant q owns weight row 32q+r: for each 128-K
 //     half of a packed slot its warps read the packed bytes and their scales
@@ -45,11 +45,12 @@
 //     shared memory as in W4A4
 //   * rings: packed-weight slots (4-9 of 18 KB, as many as shared memory holds
 //     next to a few token stages, each released as soon as the decode warps have
-//     read it into registers), TMEM slots of decoded weights (3 blocks of 256 K)
-//     and token stages (2-8 blocks of 256 K, loaded ahead of the MMAs
-//     independently of the decode); each item's
-//     accumulator is split into even / odd K-step partial sums; 2 items in
-//     flight up to 96-token tiles, 1 beyond; every wait bounded.
+//     read it into registers), TMEM slots of decoded weights (1-3 blocks of
+//     256 K) and token stages (2-8 blocks of 256 K, loaded ahead of the MMAs
+//     independently of the decode); each item's accumulator is split into even
+//     / odd K-step partial sums; two items in flight (launches with tiles of
+//     more than 96 tokens run each tile as two items of up to 64 rows); every
+//     wait bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
