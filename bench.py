@@ -444,6 +444,7 @@ def run_ours(args, rank, world, local_rank):
     M.moe_nvfp4_profile_events([])
     M.moe_nvfp4_profile_events(marks)
     fc1_ms, fc2_ms, fc1_span, fc2_span = [], [], [], []
+    stage_ms = []  # per step: the five intervals between the library's stage markers
     with torch.cuda.stream(stream):
         for i in range(args.steps):
             flush.zero_()
@@ -451,6 +452,7 @@ def run_ours(args, rank, world, local_rank):
             marks[5].synchronize()
             fc1_ms.append(marks[1].elapsed_time(marks[2]))
             fc2_ms.append(marks[3].elapsed_time(marks[4]))
+            stage_ms.append([marks[j].elapsed_time(marks[j + 1]) for j in range(5)])
             sv = span.tolist()
             if sv[1] > 0:
                 fc1_span.append((sv[1] - sv[0]) * 1e-6)   # ns -> ms
@@ -612,6 +614,11 @@ def run_ours(args, rank, world, local_rank):
                            {"bound": "hbm", "algorithmic_bytes": B["layer"],
                             "achieved": layer_gbs, "peak": hbm, "unit": "GB/s",
                             "frac": layer_gbs / hbm, "tensor_frac": layer_tflops / tpeak}),
+        # the layer stage by stage: CUDA events recorded by the library between its
+        # kernels in the marked pass (each interval includes its kernels' launch
+        # latency; with the one-launch path requant and FC2 are empty)
+        "stages_us": {name: statistics.fmean(v[j] for v in stage_ms) * 1e3
+                      for j, name in enumerate(("route", "fc1", "requant", "fc2", "finalize"))},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "copies": "pinned host memory, each step's input and output copies overlapping "
