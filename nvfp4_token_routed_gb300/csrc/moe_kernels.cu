@@ -6,6 +6,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "internal.h"
@@ -446,11 +447,12 @@ __device__ __forceinline__ float bf16_row_to_f16(const uint4* src, uint4* dst, i
   return __uint_as_float((uint32_t)(127 + k) << 23);
 }
 
-// Row gather of one route (one warp): the token's quantized row and its block
-// scales (W4A4; rows already padded to Hp by the quantizer) or its bf16 row
-// (W4A16) into permuted row p.  W4A16 rows go to the FC1 GEMM as f16, which it
-// multiplies with f16-decoded weights, as bf16_row_to_f16 forms them, its
-// scale 2^k in ps.  The Hp - H padding columns are zeroed.
+// Row gather of one route (one warp): the token's quantized row, its row scale
+// and (kScales) its block scales (W4A4; rows already padded to Hp by the
+// quantizer) or its bf16 row (W4A16) into permuted row p.  W4A16 rows go to the
+// FC1 GEMM as f16, which it multiplies with f16-decoded weights, as
+// bf16_row_to_f16 forms them, its scale 2^k in ps.  The Hp - H padding columns
+// are zeroed.
 struct GatherArgs {
   int K, H, Hp;
   const uint8_t* xc;
@@ -461,8 +463,12 @@ struct GatherArgs {
   float* ps;
   const uint4* xb;
   uint4* pb;
+  // W4A4 block scales by token tile (gather_tile_scales)
+  const int4* tiles;
+  const int32_t* status;
+  const int32_t* perm;
 };
-template <bool kW4A16>
+template <bool kW4A16, bool kScales = true>
 __device__ __forceinline__ void gather_route_row(const GatherArgs& g, int idx, int p, int lane) {
   const int t = idx / g.K;
   if constexpr (kW4A16) {
@@ -475,12 +481,51 @@ __device__ __forceinline__ void gather_route_row(const GatherArgs& g, int idx, i
     const uint4* src = reinterpret_cast<const uint4*>(g.xc + (size_t)t * (g.Hp / 2));
     uint4* dst = reinterpret_cast<uint4*>(g.pc + (size_t)p * (g.Hp / 2));
     for (int i = lane; i < g.Hp / 32; i += 32) dst[i] = __ldg(src + i);
-    const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(g.xsf + (size_t)t * (g.Hp / 16));
-    const uint32_t c16 = (uint32_t)(g.Hp / 16);
-    for (int j = lane; j < g.Hp / 64; j += 32)
-      *reinterpret_cast<uint32_t*>(g.psf + sf_offset(p, 4 * j, c16)) = __ldg(ssrc + j);
+    if constexpr (kScales) {
+      const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(g.xsf + (size_t)t * (g.Hp / 16));
+      const uint32_t c16 = (uint32_t)(g.Hp / 16);
+      for (int j = lane; j < g.Hp / 64; j += 32)
+        *reinterpret_cast<uint32_t*>(g.psf + sf_offset(p, 4 * j, c16)) = __ldg(ssrc + j);
+    }
     if (lane == 0) g.ps[p] = g.xs ? g.xs[t] : 1.0f;  // per-tensor tokens carry no row scale
   }
+}
+
+// W4A4 block scales of token tile tt, scale words jw0 .. jw0 + kTileScaleWords - 1
+// of its rows (word j: the E4M3 scales of columns 4j .. 4j + 3), one warp.  In
+// the 128x4-swizzled plane the 16-byte chunk `lane` of a 512-byte atom holds
+// word j of rows lane, lane + 32, lane + 64 and lane + 96 of the tile (the
+// layout sf_offset maps), so the lane assembles that chunk from the four rows'
+// tokens and the warp stores the atom whole: one coalesced store instead of 32
+// scattered 4-byte ones.  Padding rows of the tile get zero scales.
+constexpr int kTileScaleWords = 4;
+__device__ __forceinline__ void gather_tile_scales(const GatherArgs& g, int tt, int jw0, int lane) {
+  const int4 tl = g.tiles[tt];  // {expert, expert's first tile, expert's tiles, routes}
+  const int rows = min(kTileRows, tl.w - kTileRows * (tt - tl.y));
+  const int nw = g.Hp / 64;     // scale words per row = atoms per 128-row block
+  const uint32_t* src[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int r = lane + 32 * q;
+    src[q] = r < rows ? reinterpret_cast<const uint32_t*>(
+                            g.xsf + (size_t)(g.perm[tt * kTileRows + r] / g.K) * (g.Hp / 16))
+                      : nullptr;
+  }
+  uint4 v[kTileScaleWords];
+#pragma unroll
+  for (int u = 0; u < kTileScaleWords; ++u) {
+    const int j = jw0 + u;
+    if (j < nw) {
+      v[u].x = src[0] ? __ldg(src[0] + j) : 0u;
+      v[u].y = src[1] ? __ldg(src[1] + j) : 0u;
+      v[u].z = src[2] ? __ldg(src[2] + j) : 0u;
+      v[u].w = src[3] ? __ldg(src[3] + j) : 0u;
+    }
+  }
+  uint8_t* chunk = g.psf + (size_t)tt * nw * 512 + lane * 16;
+#pragma unroll
+  for (int u = 0; u < kTileScaleWords; ++u)
+    if (jw0 + u < nw) *reinterpret_cast<uint4*>(chunk + (size_t)(jw0 + u) * 512) = v[u];
 }
 
 // Small batches (TK <= kSmallRoutes): count, scan and scatter in one block of
@@ -600,18 +645,31 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
 
 // Gather: one warp per route copies its token's row to the route's permuted row.
 // W4A4 rows are already padded to Hp by the quantizer; W4A16 copies H bf16
-// values and zero-fills the Hp - H padding columns.
+// values and zero-fills the Hp - H padding columns.  W4A4 launches start with
+// `scale_blocks` blocks whose warps write the block scales tile by tile
+// (gather_tile_scales), ahead of the route blocks so that their chains of
+// dependent loads overlap the row copies: warp w takes tile w / jchunks and
+// words kTileScaleWords * (w % jchunks) onwards; warps past the scan's tile
+// count have nothing to do.
 template <bool kW4A16>
 __global__ void __launch_bounds__(128) gather_rows_kernel(int TK, const int32_t* __restrict__ inv,
-                                                          const GatherArgs g) {
+                                                          const GatherArgs g, int scale_blocks,
+                                                          int jchunks) {
   pdl_wait();
   pdl_trigger();
-  const int idx = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
+  if (!kW4A16 && (int)blockIdx.x < scale_blocks) {
+    const int w = ((int)blockIdx.x * (int)blockDim.x + (int)threadIdx.x) >> 5;
+    const int tt = w / jchunks;
+    if (tt >= g.status[kStatusTiles]) return;
+    gather_tile_scales(g, tt, kTileScaleWords * (w % jchunks), lane);
+    return;
+  }
+  const int idx = (((int)blockIdx.x - scale_blocks) * (int)blockDim.x + (int)threadIdx.x) >> 5;
   if (idx >= TK) return;
   const int p = inv[idx];
   if (p < 0) return;
-  gather_route_row<kW4A16>(g, idx, p, lane);
+  gather_route_row<kW4A16, false>(g, idx, p, lane);
 }
 
 // Kernels launch_route issues for TK routes: routing and the row gather.
@@ -620,8 +678,9 @@ int route_kernel_launches(int64_t TK) {
 }
 
 static GatherArgs gather_args(const RouteArgs& a) {
-  return GatherArgs{a.K,  a.H,  a.Hp, a.xc, a.xsf, a.xs, a.pc, a.psf, a.ps,
-                    static_cast<const uint4*>(a.xb), static_cast<uint4*>(a.pb)};
+  return GatherArgs{a.K,   a.H,   a.Hp, a.xc, a.xsf, a.xs, a.pc, a.psf, a.ps,
+                    static_cast<const uint4*>(a.xb), static_cast<uint4*>(a.pb),
+                    a.tiles, a.status, a.perm};
 }
 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
@@ -649,12 +708,19 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
   // 4-warp blocks: small enough in registers to share an SM with a GEMM CTA,
   // which can then start (programmatic launch) before the gather is done
   const int gblocks = (a.TK + 3) / 4;
-  if (a.w4a16)
+  if (a.w4a16) {
     launch_pdl(gather_rows_kernel<true>, dim3(gblocks), dim3(128), 0, s, a.TK,
-               (const int32_t*)a.inv, gather_args(a));
-  else
-    launch_pdl(gather_rows_kernel<false>, dim3(gblocks), dim3(128), 0, s, a.TK,
-               (const int32_t*)a.inv, gather_args(a));
+               (const int32_t*)a.inv, gather_args(a), 0, 1);
+  } else {
+    // the scale warps cover every tile the workspace can hold: its rows are TK
+    // plus up to 127 padding rows for each of min(TK, E) experts, in whole tiles
+    const int64_t pad_groups = std::min<int64_t>(a.TK, a.E);
+    const int64_t tiles_cap = (a.TK + pad_groups * (kTileRows - 1) + kTileRows - 1) / kTileRows;
+    const int jchunks = (a.Hp / 64 + kTileScaleWords - 1) / kTileScaleWords;
+    const int64_t sblocks = (tiles_cap * jchunks + 3) / 4;
+    launch_pdl(gather_rows_kernel<false>, dim3((unsigned)(gblocks + sblocks)), dim3(128), 0, s,
+               a.TK, (const int32_t*)a.inv, gather_args(a), (int)sblocks, jchunks);
+  }
   return cudaGetLastError();
 }
 
