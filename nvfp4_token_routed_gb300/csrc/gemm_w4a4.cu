@@ -36,11 +36,14 @@
 //     instruction, N = the tile's token count rounded up to 16
 //   * warps 2-5: epilogue, one TMEM lane (= one weight row) per thread; each
 //     chunk of up to 32 tokens is staged in shared memory as [token][feature]
-//     rows and one thread writes it with TMA tensor stores
+//     rows and one thread writes it with TMA tensor stores (two 16 KB staging
+//     buffers; one 8 KB buffer of 16-token chunks in squared-ReLU FC1 launches
+//     with tiles of more than 96 tokens)
 //   * the shared-memory stage ring is sized at run time from the largest token
-//     tile of the launch (5 stages at 128 tokens, 8 at 16); two accumulator
-//     buffers (four when no tile exceeds 64 tokens) let the epilogue of one tile
-//     overlap the MMAs of the next ones.
+//     tile of the launch and the staging buffers (5 stages at 128 tokens, 6 in
+//     those squared-ReLU FC1 launches, 8 at 16); two accumulator buffers (four
+//     when no tile exceeds 64 tokens) let the epilogue of one tile overlap the
+//     MMAs of the next ones.
 //   * every wait is bounded; on timeout the CTA records an error flag, drains its
 //     own copies and MMAs, frees TMEM and returns.
 // SwiGLU: the stored FC1 rows interleave 64-row blocks [gate | up], so TMEM
@@ -75,7 +78,6 @@ constexpr int kEpiBufBytes = 16384;
 constexpr int kEpiBytes = 2 * kEpiBufBytes;
 constexpr int kBarBytes = 2048;             // barriers, flags, item ring; then 128 row scales
 constexpr int kSmemBytes = 227 * 1024;      // dynamic shared memory of every launch
-constexpr int kStageBudget = kSmemBytes - 1024 - kBarBytes - kEpiBytes;
 constexpr int kThreads = 352;               // 11 warps
 // barrier indices
 constexpr int kBarFull = 0;
@@ -209,8 +211,7 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
   const ItemQueue Q{reinterpret_cast<int4*>(smem + kRingOff), R.bar(kBarItemFull),
                     R.bar(kBarItemEmpty)};
   float* s_scale = reinterpret_cast<float*>(smem + 1024);  // row scales of the current tile (128)
-  uint8_t* epi_buf = smem + kBarBytes;               // kEpiBytes, 1024-aligned
-  uint8_t* stages = smem + kBarBytes + kEpiBytes;     // 1024-aligned
+  uint8_t* epi_buf = smem + kBarBytes;               // epilogue staging, 1024-aligned
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // prologue that reads nothing the previous kernel writes: barriers, TMEM
@@ -267,7 +268,17 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
   const int nbuf = max_n16 <= 64 ? 4 : 2;                 // accumulator buffers
   const int slot_cols = 32;                               // scale columns per stage (A 16, B 16)
   const int sf_base = nbuf * acc_stride;
-  int n_stages = kStageBudget / stage_bytes;
+  // Squared-ReLU FC1 launches with 97-128-token tiles stage the epilogue through
+  // one 8 KB buffer in 16-token chunks: that leaves room for a sixth 36 KB
+  // stage, 108 KB of weights in flight instead of 90 KB.  Every other launch
+  // uses two 16 KB buffers in 32-token chunks (FC2's short items and the
+  // SwiGLU pairing were measured slower with the single buffer).
+  const bool narrow_epi =
+      ACT == kFc1Relu2 && a.run_fc1 && !a.run_fc2 && max_n16 > 96;
+  const int epi_bytes = narrow_epi ? kEpiBufBytes / 2 : kEpiBytes;  // multiple of 1024
+  const int cw = narrow_epi ? 16 : 32;                // tokens per epilogue chunk
+  uint8_t* stages = smem + kBarBytes + epi_bytes;     // 1024-aligned
+  int n_stages = (kSmemBytes - 1024 - kBarBytes - epi_bytes) / stage_bytes;
   if (n_stages > kMaxStages) n_stages = kMaxStages;
   while (n_stages > 2 && sf_base + n_stages * slot_cols > kTmemCols) --n_stages;
 
@@ -563,23 +574,29 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
       s_r = row_scale(cur);
       tc_fence_after();
       const uint32_t acc = tmem + lane_addr + buf * acc_stride;
-      for (int c0 = 0; c0 < n16; c0 += 32) {
-        const int ncol = min(32, n16 - c0);
+      for (int c0 = 0; c0 < n16; c0 += cw) {
+        const int ncol = min(cw, n16 - c0);
         float v[32];
         tmem_ld16(acc + c0, *reinterpret_cast<float(*)[16]>(v));
         if (ncol > 16) tmem_ld16(acc + c0 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
         tmem_wait_ld();
-        if (c0 + 32 >= n16) {
+        if (c0 + cw >= n16) {
           // every TMEM read of this accumulator is done: the MMA may reuse it
           tc_fence_before();
           mbar_arrive(R.bar(kBarAccEmpty + buf));
         }
-        // staging buffer eb is free once the store issued from it two chunks ago has read it
-        if (issuer) bulk_wait_group_read<1>();
+        // staging buffer eb is free once the store issued from it two chunks ago (one
+        // chunk ago with the single buffer) has read it
+        if (issuer) {
+          if (narrow_epi)
+            bulk_wait_group_read<0>();
+          else
+            bulk_wait_group_read<1>();
+        }
         named_bar_sync(1, 128);
         uint8_t* ob = epi_buf + eb * kEpiBufBytes;
-        // the chunk's 32 token scales, read up front (the loops below then hold
-        // no shared-memory load behind a store)
+        // the chunk's token scales, read up front (32; a 16-token chunk uses the
+        // first 16), so the loops below hold no shared-memory load behind a store
         float y[32];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -601,7 +618,7 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
         } else if constexpr (ACT == kFc1Swiglu) {
           // lanes 0-63: gate rows of features mt*64 + (r & 63); lanes 64-127: up rows
           float* g = reinterpret_cast<float*>(ob);
-          float* u = g + 32 * 64;
+          float* u = g + cw * 64;
           float* dst = r < 64 ? g : u;
 #pragma unroll
           for (int j = 0; j < 32; ++j)
@@ -660,11 +677,11 @@ __global__ void __launch_bounds__(w4a4::kThreads, 1)
           for (int k = 0; k < nf / 4; ++k) mx = fmaxf(mx, fabsf(srow[k]));
           mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
           mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
-          if (part == 0 && c0 + j < rows)
+          if (part == 0 && j < ncol && c0 + j < rows)
             atomicMax(reinterpret_cast<unsigned int*>(a.row_amax) + row0 + c0 + j,
                       __float_as_uint(mx));
         }
-        eb ^= 1;
+        if (!narrow_epi) eb ^= 1;
       }
       ++local;
       if (a.fused && ph == 0) {
